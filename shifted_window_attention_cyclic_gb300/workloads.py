@@ -1,0 +1,136 @@
+"""Seeded synthetic workloads shaped like the pages' grids.
+
+This module holds only problem sizes and seeded random inputs; it contains
+none of the attention arithmetic, so both the CUDA path's tests/benchmark and
+the CPU oracle may take their inputs from it.
+
+Grids (stand-ins for datasets that are not used here):
+  * tiny_fp32      16x32, window 4x8, shift (2,4), both dims shift-masked
+  * grid1deg       2 x 180x360 (the 1-degree ocean grid of the Samudra page),
+                   window 6x12, shift (3,6), lon periodic, forward only
+  * ragged         181x362, window 8x8, shift (4,4): windows that the grid
+                   does not divide, in both dims
+  * eddy_ocean     256x540 (Wenhai's 2041x4320 grid after 4x4 patches and one
+                   2x down-sampling, TERRA Eq. (2), padded to 256 rows),
+                   window 8x12, shift (4,6), blocked land mask p=0.3
+  * depth3d        16 levels x 192x384, window 2x8x8, shift (1,4,4), land mask
+                   whose probability grows from 0.3 (level 0) to 0.6 (level 15)
+
+Recipe: numpy Generator(PCG64(20260 + index)); draws in the fixed order
+Q, K, V, bias, dO, land-xi. Q/K/V/dO ~ N(0,1), bias ~ N(0, 0.02), drawn in
+float32 and rounded to bf16 (round-to-nearest-even) for the bf16 workloads.
+Land: one uniform xi per (batch, 8x8 lat-lon patch, aligned at (0,0), clipped
+at the edges); a token is land iff xi < p(level); the same xi serves every
+depth level, so land only grows with depth.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    index: int
+    dtype: str            # "f32" or "bf16": storage and I/O type of q, k, v, o, dq, dk, dv
+    batch: int
+    grid: tuple           # outermost first
+    window: tuple
+    shift: tuple
+    periodic: tuple
+    heads: int
+    head_dim: int
+    land_p: tuple | None  # None = no land; else (p at level 0, p at last level)
+    backward: bool
+
+    @property
+    def has_land(self):
+        return self.land_p is not None
+
+    @property
+    def channels(self):
+        return self.heads * self.head_dim
+
+    @property
+    def tokens(self):
+        return int(np.prod(self.grid))
+
+    @property
+    def seed(self):
+        return 20260 + self.index
+
+
+WORKLOADS = {
+    "tiny_fp32": Workload("tiny_fp32", 0, "f32", 1, (16, 32), (4, 8), (2, 4), (0, 0), 2, 16, None, True),
+    "grid1deg": Workload("grid1deg", 1, "bf16", 2, (180, 360), (6, 12), (3, 6), (0, 1), 8, 32, None, False),
+    "ragged": Workload("ragged", 2, "bf16", 1, (181, 362), (8, 8), (4, 4), (0, 1), 12, 32, None, True),
+    "eddy_ocean": Workload("eddy_ocean", 3, "bf16", 1, (256, 540), (8, 12), (4, 6), (0, 1), 16, 32, (0.3, 0.3), True),
+    "depth3d": Workload("depth3d", 4, "bf16", 1, (16, 192, 384), (2, 8, 8), (1, 4, 4), (0, 0, 1), 8, 32,
+                        (0.3, 0.6), True),
+}
+
+
+def custom(grid, window, shift, periodic, heads, head_dim, batch=1, dtype="bf16", land_p=None,
+           seed_index=100, name="custom"):
+    """A small workload for sweeps and edge cases, with the same recipe."""
+    return Workload(name, seed_index, dtype, batch, tuple(grid), tuple(window), tuple(shift),
+                    tuple(periodic), heads, head_dim, land_p, True)
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); returns float32."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if np.isnan(x).any():
+        raise ValueError("round_bf16: NaN input")
+    u = x.reshape(-1).view(np.uint32)
+    out = np.empty_like(u)
+    step = 1 << 24
+    for a in range(0, u.size, step):
+        c = u[a:a + step]
+        out[a:a + step] = (c + np.uint32(0x7FFF) + ((c >> np.uint32(16)) & np.uint32(1))) & np.uint32(0xFFFF0000)
+    return out.view(np.float32).reshape(x.shape)
+
+
+def land_mask(wl: Workload, xi: np.ndarray) -> np.ndarray:
+    """uint8 [B, *grid] from the per-patch uniforms xi [B, ceil(lat/8), ceil(lon/8)]."""
+    lat, lon = wl.grid[-2], wl.grid[-1]
+    patch = np.repeat(np.repeat(xi, 8, axis=1), 8, axis=2)[:, :lat, :lon]
+    if len(wl.grid) == 2:
+        return (patch < wl.land_p[0]).astype(np.uint8)
+    levels = wl.grid[0]
+    out = np.empty((wl.batch,) + tuple(wl.grid), np.uint8)
+    for z in range(levels):
+        p = wl.land_p[0] + (wl.land_p[1] - wl.land_p[0]) * (z / max(levels - 1, 1))
+        out[:, z] = patch < p
+    return out
+
+
+def generate(wl: Workload, with_dout: bool = True):
+    """Seeded host inputs: dict of float32 arrays q, k, v [B, *grid, C],
+    bias [rows, heads], dout (or None), and land uint8 [B, *grid] (or None).
+    bf16 workloads carry bf16-rounded values in float32 containers."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed))
+    shape = (wl.batch,) + tuple(wl.grid) + (wl.channels,)
+    rows = int(np.prod([2 * w - 1 for w in wl.window]))
+
+    def normal(shape_, std=1.0):
+        x = rng.standard_normal(shape_, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        return round_bf16(x) if wl.dtype == "bf16" else x
+
+    q = normal(shape)
+    k = normal(shape)
+    v = normal(shape)
+    bias = rng.standard_normal((rows, wl.heads), dtype=np.float32) * np.float32(0.02)
+    dout = normal(shape)
+    if not with_dout:
+        dout = None
+    land = None
+    if wl.has_land:
+        lat, lon = wl.grid[-2], wl.grid[-1]
+        xi = rng.random((wl.batch, -(-lat // 8), -(-lon // 8)))
+        land = land_mask(wl, xi)
+    return {"q": q, "k": k, "v": v, "bias": bias, "dout": dout, "land": land}
