@@ -1,0 +1,380 @@
+#!/usr/bin/env python3
+"""Benchmark: shifted-window attention forward + backward on one GB300.
+
+A step is one pass of the whole path over one batch of the depth3d workload
+(16 levels x 192 x 384 tokens, C=256, 8 heads x 32, window 2x8x8, shift
+(1,4,4), lon periodic, land mask growing with depth; bf16): swin_attn_fwd then
+swin_attn_bwd (dQ, dK, dV, dBias). Every input tensor (604 MB each) is larger
+than the 129 MB L2, so no flush runs between steps.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle on the
+same workload instead (bounded samples of windows, fp64).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "window-attention Mtokens/s fwd & fwd+bwd (bf16) and % of roofline, 1 GB300"
+WORKLOAD = "depth3d"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def workload_counts(wl, win_src, land):
+    """Algorithmic FLOPs and bytes per step (forward, backward)."""
+    n_real = (win_src >= 0).sum(1).astype(np.float64)  # real slots per window
+    N = wl.batch * wl.tokens
+    C, H, e = wl.channels, wl.heads, 2 if wl.dtype == "bf16" else 4
+    rows = int(np.prod([2 * w - 1 for w in wl.window]))
+    fwd_flop = 4.0 * wl.batch * float((n_real ** 2).sum()) * C
+    bwd_flop = 2.5 * fwd_flop
+    land_b = N if land is not None else 0
+    bias_b = rows * H * 4
+    fwd_bytes = 4 * N * C * e + 4 * N * H + land_b + bias_b                 # q,k,v in; o, lse out
+    bwd_bytes = 7 * N * C * e + 4 * N * H + land_b + 2 * bias_b             # q,k,v,dO,lse in; dq,dk,dv, dbias out
+    return fwd_flop, bwd_flop, fwd_bytes, bwd_bytes
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "shifted_window_attention_cyclic_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_hash):
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, only if it was captured from the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    if t.get("kernel_source_hash") != kernel_hash:
+        return None
+    return t.get("bwd_dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[4:8]):
+                    if val.lower().startswith("active"):
+                        reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def oracle_sample_rate(wl, x, windows, seed=0):
+    """Time the oracle (fwd + bwd, fp64) on `windows` windows; returns (tokens, seconds)."""
+    import oracle
+    pb = oracle.Problem(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.has_land)
+    rng = np.random.default_rng(seed)
+    ids = rng.choice(wl.batch * pb.nwin, size=windows, replace=False)
+    win_src = oracle.tables(pb)[0]
+    tokens = int(sum((win_src[i % pb.nwin] >= 0).sum() for i in ids))
+    t0 = time.perf_counter()
+    oracle.fwd_windows(pb, x["q"], x["k"], x["v"], x["bias"], x["land"], win_ids=ids)
+    oracle.bwd_windows(pb, x["q"], x["k"], x["v"], x["bias"], x["land"], x["dout"], win_ids=ids)
+    return tokens, time.perf_counter() - t0
+
+
+def cpu_baseline(wl, x, target_s=12.0):
+    import oracle
+    oracle.build()
+    tok, dt = oracle_sample_rate(wl, x, 16, seed=1)
+    per_window = dt / 16
+    windows = int(max(16, min(wl.batch * 9216, target_s / max(per_window, 1e-6))))
+    tok, dt = oracle_sample_rate(wl, x, windows, seed=2)
+    return {"value": tok / dt / 1e6, "unit": "Mtokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d random windows of %s (%d tokens), fwd+bwd, fp64 C oracle, %.1f s" %
+                      (windows, wl.name, tok, dt)}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return 0
+    from shifted_window_attention_cyclic_gb300 import workloads
+    import oracle
+    oracle.build()
+    x = workloads.generate(wl)
+    # size each step so that the whole run stays within ~2 minutes of CPU time
+    tok, dt = oracle_sample_rate(wl, x, 8, seed=3)
+    per_window = dt / 8
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    windows = int(max(1, min(512, budget / max(per_window, 1e-6))))
+    for s in range(args.warmup):
+        oracle_sample_rate(wl, x, windows, seed=100 + s)
+    total_tok, total_t = 0, 0.0
+    for s in range(args.steps):
+        tok, dt = oracle_sample_rate(wl, x, windows, seed=1000 + s)
+        total_tok += tok
+        total_t += dt
+    value = total_tok / total_t / 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, shapes of the pages' workloads)",
+            "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "Mtokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": "%d random windows per step of %s, fwd+bwd, fp64 C oracle" %
+                                       (windows, wl.name)},
+            "e2e": {"value": value, "unit": "Mtokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(wl):
+    return {"workload": "%s: B=%d grid %s C=%d heads %dx%d window %s shift %s periodic %s land p %s %s" %
+                        (wl.name, wl.batch, "x".join(map(str, wl.grid)), wl.channels, wl.heads, wl.head_dim,
+                         "x".join(map(str, wl.window)), tuple(wl.shift), tuple(wl.periodic), wl.land_p, wl.dtype),
+            "global_batch": wl.batch, "tokens_per_batch": wl.batch * wl.tokens,
+            "parallelism": "replicas (independent problem per GPU)",
+            "l2": "inputs larger than L2 (each tensor %.0f MB > 129 MB), no flush" %
+                  (wl.batch * wl.tokens * wl.channels * 2 / 1e6)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernels", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    from shifted_window_attention_cyclic_gb300 import workloads
+    wl = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    import __graft_entry__
+    __graft_entry__.build_library()
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+
+    x = workloads.generate(wl)
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch,
+                               wl.dtype, wl.has_land, args.kernels)
+    win_src = C.swin_attn_plan_tables(attn.plan)[0]
+    fwd_flop, bwd_flop, fwd_bytes, bwd_bytes = workload_counts(wl, win_src, x["land"])
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    host = {k_: torch.from_numpy(x[k_]).to(tdt).pin_memory() for k_ in ("q", "k", "v", "dout")}
+    host["bias"] = torch.from_numpy(x["bias"]).pin_memory()
+    host["land"] = torch.from_numpy(x["land"]).pin_memory()
+    d = {k_: t.to(dev) for k_, t in host.items()}
+    o = torch.empty(attn.shape, dtype=tdt, device=dev)
+    lse = torch.empty(attn.lse_shape, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty(attn.shape, dtype=tdt, device=dev) for _ in range(3))
+    dbias = attn.new_bias()
+    ws = attn.workspace()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], d["bias"], d["land"], o, lse, stream)
+        C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, d["bias"], d["land"], dq, dk, dv, dbias,
+                        ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert C.swin_attn_status(attn.plan) == 0
+
+    # timed region: K steps, events per launch on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], d["bias"], d["land"], o, lse, stream)
+        e1.record(stream)
+        C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, d["bias"], d["land"], dq, dk, dv, dbias,
+                        ws, stream)
+        e2.record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    assert C.swin_attn_status(attn.plan) == 0
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = wl.batch * wl.tokens
+    value = world * tokens / (ms_per_step * 1e-3) / 1e6
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms)
+    peaks, peak_kind = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    tflops = peaks["bf16_tflops_sustained"]
+    fwd_roof_us = max(fwd_flop / (tflops * 1e12), fwd_bytes / (hbm * 1e9)) * 1e6
+    bwd_roof_us = max(bwd_flop / (tflops * 1e12), bwd_bytes / (hbm * 1e9)) * 1e6
+    bwd_gbs = bwd_bytes / (bwd_avg * 1e-3) / 1e9
+    khash = kernel_source_hash()
+
+    # end to end through the public API with host buffers: H2D inputs, fwd, bwd, D2H results
+    host_out = {k_: torch.empty(attn.shape, dtype=tdt).pin_memory() for k_ in ("o", "dq", "dk", "dv")}
+    host_out["dbias"] = torch.empty_like(dbias, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def e2e_step():
+        for k_, t in host.items():
+            d[k_].copy_(t, non_blocking=True)
+        step()
+        host_out["o"].copy_(o, non_blocking=True)
+        host_out["dq"].copy_(dq, non_blocking=True)
+        host_out["dk"].copy_(dk, non_blocking=True)
+        host_out["dv"].copy_(dv, non_blocking=True)
+        host_out["dbias"].copy_(dbias, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, x)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic (seeded, shapes of the pages' workloads)",
+            "config": config_of(wl),
+            "fwd": {"mtok_s": tokens / (fwd_avg * 1e-3) / 1e6, "us": fwd_avg * 1e3, "roof_us": fwd_roof_us,
+                    "roof_frac": fwd_roof_us / (fwd_avg * 1e3), "tflops": fwd_flop / (fwd_avg * 1e-3) / 1e12,
+                    "alg_bytes": fwd_bytes},
+            "bwd": {"us": bwd_avg * 1e3, "roof_us": bwd_roof_us, "roof_frac": bwd_roof_us / (bwd_avg * 1e3),
+                    "tflops": bwd_flop / (bwd_avg * 1e-3) / 1e12, "alg_bytes": bwd_bytes},
+            "fwd_bwd": {"mtok_s": value / world, "roof_frac": (fwd_roof_us + bwd_roof_us) / (ms_per_step * 1e3)},
+            "roofline": {"bound": "hbm", "kernel": "swin_attn_bwd (main kernel + dBias fold)",
+                         "achieved": bwd_gbs, "peak": hbm, "unit": "GB/s", "frac": bwd_gbs / hbm,
+                         "peak_source": peak_kind, "traffic": profiled_traffic(khash),
+                         "alg_bytes_per_launch": bwd_bytes},
+            "clocks": clocks,
+            "e2e": {"value": world * tokens / (e2e_ms * 1e-3) / 1e6, "unit": "Mtokens/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "impl_kernels": {1: "simt", 2: "tcgen05"}[attn.info.impl],
+            "kernel_source_hash": khash,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

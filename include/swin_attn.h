@@ -1,0 +1,167 @@
+/*
+ * swin_attn.h -- C ABI of a single-GPU (GB300, sm_103a) library for
+ * shifted-window multi-head self-attention (SW-MSA) over a lat-lon(-depth)
+ * token grid: cyclic shift, ragged edge windows, periodic longitude seam,
+ * shift-boundary (region) mask, land mask, relative-position bias, softmax,
+ * PV and the reverse routing back to the grid; forward and backward.
+ *
+ * Where the operation is defined (page title, section):
+ *  - "TERRA: A Hierarchical Parallel Training and Memory Orchestration
+ *    Framework for High-Resolution AI-based Earth Modeling", Sec. IV.D
+ *    "Differentiable Token Routes": window coordinate and in-window offset of
+ *    a token follow from its global grid coordinate; a window shift changes
+ *    the coordinate; the backward applies the inverse route. Sec. V.A, Eq. (4):
+ *    ragged contiguous window ranges (used here to split work over CTAs).
+ *  - "4D Parallelism Unlocks Exascale Bayesian Neural Networks for
+ *    High-Fidelity Atmospheric Modeling", Model Architecture: the domain is
+ *    rolled by floor(window/2) between attention layers; Swin-style window
+ *    attention with a relative-position bias.
+ *
+ * Definition computed (all dims outermost first; G grid, w window, s shift):
+ *   rolled position p_d = (u_d - s_d) mod G_d of the token at coordinate u;
+ *   window floor(p_d / w_d), slot p_d mod w_d (ceil(G_d / w_d) windows per dim,
+ *   the last one may be short: its missing slots are pads);
+ *   region bit d = [dim d not periodic and s_d > 0 and p_d >= G_d - s_d];
+ *   key j is visible to query i iff same window, same region bits, j not land;
+ *   s_ij = hd^-1/2 q_i.k_j + bias[row(i,j), h],
+ *   row(i,j) = sum_d (sig_i,d - sig_j,d + w_d - 1) * prod_{e>d} (2 w_e - 1);
+ *   O_i = softmax over visible j of s_ij, times V; land queries give O = 0.
+ *
+ * Conventions for every entry point:
+ *  - Returns SWIN_OK (0) or a negative status; nothing is launched when an
+ *    argument check fails.
+ *  - Tensors are owned by the caller, device-resident, contiguous; every
+ *    q/k/v/o/dout/dq/dk/dv pointer must be 16-byte aligned.
+ *  - q, k, v, o, dout, dq, dk, dv: [B, grid..., C] channel-last, C = heads *
+ *    head_dim, head h in channels [h*hd, (h+1)*hd); element type = desc.dtype.
+ *  - bias, dbias: float32 [rows][heads], rows = prod(2 w_d - 1).
+ *  - lse: float32 [B][heads][grid...] natural-log log-sum-exp per query
+ *    (-inf for land queries).
+ *  - land: uint8 [B, grid...], nonzero = land.
+ *  - fwd/bwd allocate nothing and are asynchronous on `stream`.
+ */
+#ifndef SWIN_ATTN_H
+#define SWIN_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define SWIN_OK 0
+#define SWIN_ERR_INVALID_ARG (-1) /* NULL/inconsistent argument or descriptor */
+#define SWIN_ERR_UNSUPPORTED (-2) /* window > 128 slots, head_dim not 16/32, ... */
+#define SWIN_ERR_ALIGNMENT (-3)   /* a tensor pointer is not 16-byte aligned */
+#define SWIN_ERR_WORKSPACE (-4)   /* workspace NULL or smaller than required */
+#define SWIN_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
+#define SWIN_ERR_TIMEOUT (-6)     /* a kernel gave up a bounded wait (device status word) */
+#define SWIN_ERR_DEVICE (-7)      /* a kernel recorded another device-side error */
+
+/* Element types of q, k, v, o, dout, dq, dk, dv. */
+#define SWIN_F32 0
+#define SWIN_BF16 1
+
+/* Kernel family. AUTO picks the tensor-core path for bf16 with head_dim 32. */
+#define SWIN_IMPL_AUTO 0
+#define SWIN_IMPL_SIMT 1   /* fp32 FFMA kernels (any supported dtype) */
+#define SWIN_IMPL_TC 2     /* tcgen05/TMEM kernels (bf16, head_dim 32) */
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *swin_stream_t;
+
+/* Opaque plan. Owns its device-side tables and status word. */
+typedef struct swin_attn_plan_s *swin_attn_plan_t;
+
+typedef struct {
+  int32_t ndim;        /* 2: (lat, lon); 3: (depth, lat, lon) */
+  int32_t impl;        /* SWIN_IMPL_* */
+  int64_t batch;       /* B >= 1 */
+  int32_t grid[3];     /* G_d >= 1, outermost first; prod(G) < 2^31 */
+  int32_t window[3];   /* w_d >= 1; prod(w) <= 128 */
+  int32_t shift[3];    /* 0 <= s_d < w_d, s_d < G_d (or 0); all zero = W-MSA */
+  int32_t periodic[3]; /* 1 = cyclic neighbour (no region bit), 0 = region-masked */
+  int32_t heads;       /* >= 1 */
+  int32_t head_dim;    /* 16 or 32 */
+  int32_t dtype;       /* SWIN_F32 or SWIN_BF16 */
+  int32_t has_land;    /* 1 = a land mask is passed to fwd/bwd */
+} swin_attn_desc;
+
+/* Sizes and launch shapes of a plan (all counts, no pointers). */
+typedef struct {
+  int64_t windows_per_image;
+  int64_t tokens_per_image;
+  int32_t slots;       /* n = prod(w) */
+  int32_t bias_rows;   /* prod(2 w_d - 1) */
+  int32_t impl;        /* resolved SWIN_IMPL_SIMT or SWIN_IMPL_TC */
+  int32_t fwd_ctas;    /* persistent CTAs of the forward kernel */
+  int32_t bwd_ctas;    /* persistent CTAs of the backward kernel */
+  int32_t num_sms;
+  int64_t work_items;  /* heads * B * windows_per_image (one window and head each) */
+  int64_t dbias_slots; /* partial dBias tables in the workspace */
+} swin_attn_plan_info;
+
+/* Validate `desc` and build a plan on the current CUDA device: routing tables
+ * (win_src, region, tok_dst, relidx) are computed on the device by the same
+ * routing function the kernels use, and the work partition is fixed.
+ * Synchronous; allocates device memory owned by the plan.
+ * Errors: INVALID_ARG (NULL, bad sizes, shift >= window), UNSUPPORTED
+ * (slots > 128, head_dim, dtype, impl not available for the dtype), CUDA. */
+int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out);
+
+/* Copy `plan`'s sizes into *info (host). Errors: INVALID_ARG. */
+int swin_attn_plan_get_info(swin_attn_plan_t plan, swin_attn_plan_info *info);
+
+/* Copy the routing tables of one image to HOST buffers (any may be NULL):
+ *   win_src [nwin][n] int32: grid token feeding slot s of window w, -1 = pad;
+ *   region  [nwin][n] uint8: region bits of that token (bit d for dim d), 0 for pads;
+ *   tok_dst [N] int32: w*n + s of every token (the inverse route);
+ *   relidx  [n][n] int32: bias row of the slot pair (query i, key j).
+ * Synchronous. Errors: INVALID_ARG, CUDA. */
+int swin_attn_plan_tables(swin_attn_plan_t plan, int32_t *win_src, uint8_t *region,
+                          int32_t *tok_dst, int32_t *relidx);
+
+/* Bytes of device workspace swin_attn_bwd needs (partial dBias tables). */
+size_t swin_attn_workspace_bytes(swin_attn_plan_t plan);
+
+/* Forward. q, k, v, o as above; bias may be NULL (zero bias); land required
+ * iff desc.has_land; lse may be NULL (inference) else receives the float32
+ * log-sum-exp. Pad slots write nothing; every grid token is written once.
+ * Errors: INVALID_ARG, ALIGNMENT, CUDA (launch). */
+int swin_attn_fwd(swin_attn_plan_t plan, const void *q, const void *k, const void *v,
+                  const float *bias, const uint8_t *land, void *o, float *lse,
+                  swin_stream_t stream);
+
+/* Backward of L = sum(O * dout): writes dq, dk, dv (every token) and
+ * OVERWRITES dbias (may be NULL: not computed). lse is the forward's output
+ * for the same inputs (required). delta_i = sum_j P_ij dP_ij is recomputed
+ * in-kernel, so O is not an input. workspace: device, >=
+ * swin_attn_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored.
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, CUDA. */
+int swin_attn_bwd(swin_attn_plan_t plan, const void *q, const void *k, const void *v,
+                  const void *dout, const float *lse, const float *bias,
+                  const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,
+                  void *workspace, size_t workspace_bytes, swin_stream_t stream);
+
+/* Synchronise `stream`, read and clear the plan's device status word.
+ * Returns SWIN_OK, SWIN_ERR_TIMEOUT, SWIN_ERR_DEVICE or SWIN_ERR_CUDA. */
+int swin_attn_status(swin_attn_plan_t plan, swin_stream_t stream);
+
+/* Free the plan's device memory (synchronises the device). NULL is a no-op. */
+void swin_attn_plan_destroy(swin_attn_plan_t plan);
+
+/* Static message for a status code. */
+const char *swin_attn_strerror(int status);
+
+/* TERRA Sec. V.A, Eq. (4): rank r of P ranks owns the contiguous window-index
+ * range [floor(r*M/P), floor((r+1)*M/P)). Host-only, used for the CTA work
+ * split. Errors: INVALID_ARG (M < 0, P < 1, r outside [0, P), NULL). */
+int swin_attn_window_range(int64_t M, int64_t P, int64_t r, int64_t *L, int64_t *R);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWIN_ATTN_H */

@@ -424,7 +424,7 @@ int oracle_bwd(const oracle_desc *d, const float *q, const float *k,
           for (int j = 0; j < n; ++j)
             dS[i * n + j] = P[i * n + j] * (dP[i * n + j] - delta);
         }
-        for (int s = 0; s < n; ++s) {
+        for (int s = 0; s < n && (dq_win || dk_win || dv_win); ++s) {
           double *gq = dq_win ? dq_win + (x * n + s) * C + (int64_t)h * hd : NULL;
           double *gk = dk_win ? dk_win + (x * n + s) * C + (int64_t)h * hd : NULL;
           double *gv = dv_win ? dv_win + (x * n + s) * C + (int64_t)h * hd : NULL;

@@ -1,0 +1,361 @@
+// swin_api.cu -- the C ABI (include/swin_attn.h): plan building, argument
+// checks, launches, the dBias fold and the device status word.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "swin_common.cuh"
+#include "swin_tc.cuh"
+
+using namespace swin;
+
+struct swin_attn_plan_s {
+  swin_attn_desc d;
+  Geo g;
+  int device;
+  int num_sms;
+  int impl;
+  int fwd_ctas, bwd_ctas;
+  int64_t items;
+  int64_t ws_slots;
+  int32_t *d_win_src;
+  uint8_t *d_region;
+  int32_t *d_tok_dst;
+  int32_t *d_relidx;
+  int *d_status;
+  int *d_slot_base;        // [bwd_ctas]
+  int *d_head_slot_begin;  // [heads + 1]
+};
+
+namespace {
+
+// ---- routing tables, built on the device with the kernels' own routing ----
+__global__ void tables_kernel(Geo g, int32_t *win_src, uint8_t *region, int32_t *tok_dst) {
+  const int64_t total = (int64_t)g.nwin * g.n;
+  for (int64_t x = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; x < total; x += (int64_t)gridDim.x * blockDim.x) {
+    const int omega = (int)(x / g.n), sigma = (int)(x % g.n);
+    int wc[3];
+    window_coords(g, omega, wc);
+    const SlotRoute r = slot_route(g, wc, sigma);
+    win_src[x] = r.src;
+    region[x] = (uint8_t)r.reg;
+    if (r.src >= 0) tok_dst[r.src] = (int32_t)x;
+  }
+}
+
+__global__ void relidx_kernel(Geo g, int32_t *relidx) {
+  const int wc[3] = {0, 0, 0};
+  for (int x = blockIdx.x * blockDim.x + threadIdx.x; x < g.n * g.n; x += gridDim.x * blockDim.x) {
+    const int i = x / g.n, j = x % g.n;
+    relidx[x] = slot_route(g, wc, i).rbase - slot_route(g, wc, j).roff;
+  }
+}
+
+// dbias[t][h] = sum over the workspace slots of head h, in slot order.
+__global__ void fold_kernel(FoldArgs a) {
+  const int x = blockIdx.x * blockDim.x + threadIdx.x;
+  if (x >= a.T * a.heads) return;
+  const int t = x / a.heads, h = x % a.heads;
+  float sum = 0.f;
+  for (int s = a.head_slot_begin[h]; s < a.head_slot_begin[h + 1]; ++s) sum += a.ws[(int64_t)s * a.T + t];
+  a.dbias[x] = sum;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_desc(const swin_attn_desc *d) {
+  if (!d) return SWIN_ERR_INVALID_ARG;
+  if (d->ndim != 2 && d->ndim != 3) return SWIN_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->heads < 1) return SWIN_ERR_INVALID_ARG;
+  if (d->dtype != SWIN_F32 && d->dtype != SWIN_BF16) return SWIN_ERR_UNSUPPORTED;
+  if (d->impl < SWIN_IMPL_AUTO || d->impl > SWIN_IMPL_TC) return SWIN_ERR_INVALID_ARG;
+  if (d->has_land != 0 && d->has_land != 1) return SWIN_ERR_INVALID_ARG;
+  int64_t tokens = 1, n = 1;
+  for (int a = 0; a < d->ndim; ++a) {
+    if (d->grid[a] < 1 || d->window[a] < 1) return SWIN_ERR_INVALID_ARG;
+    if (d->shift[a] < 0 || d->shift[a] >= d->window[a]) return SWIN_ERR_INVALID_ARG;
+    if (d->shift[a] > 0 && d->shift[a] >= d->grid[a]) return SWIN_ERR_INVALID_ARG;
+    if (d->periodic[a] != 0 && d->periodic[a] != 1) return SWIN_ERR_INVALID_ARG;
+    tokens *= d->grid[a];
+    n *= d->window[a];
+    if (tokens >= (int64_t(1) << 31) || n > 128) return SWIN_ERR_UNSUPPORTED;
+  }
+  if (n > 128) return SWIN_ERR_UNSUPPORTED;
+  if (d->head_dim != 16 && d->head_dim != 32) return SWIN_ERR_UNSUPPORTED;
+  if (d->batch * tokens * d->heads >= (int64_t(1) << 40)) return SWIN_ERR_UNSUPPORTED;
+  return SWIN_OK;
+}
+
+Geo make_geo(const swin_attn_desc *d) {
+  Geo g;
+  std::memset(&g, 0, sizeof(g));
+  g.lead = 3 - d->ndim;
+  for (int a = 0; a < 3; ++a) {
+    const int s = a - g.lead;
+    g.G[a] = s >= 0 ? d->grid[s] : 1;
+    g.w[a] = s >= 0 ? d->window[s] : 1;
+    g.s[a] = s >= 0 ? d->shift[s] : 0;
+    g.per[a] = s >= 0 ? d->periodic[s] : 0;
+    g.nw[a] = (g.G[a] + g.w[a] - 1) / g.w[a];
+  }
+  g.n = g.w[0] * g.w[1] * g.w[2];
+  g.nwin = g.nw[0] * g.nw[1] * g.nw[2];
+  g.tokens = g.G[0] * g.G[1] * g.G[2];
+  g.rstride[2] = 1;
+  g.rstride[1] = 2 * g.w[2] - 1;
+  g.rstride[0] = (2 * g.w[1] - 1) * (2 * g.w[2] - 1);
+  g.T = (2 * g.w[0] - 1) * g.rstride[0];
+  g.heads = d->heads;
+  g.hd = d->head_dim;
+  g.C = d->heads * d->head_dim;
+  g.batch = (int)d->batch;
+  g.has_land = d->has_land;
+  return g;
+}
+
+void free_plan(swin_attn_plan_s *p) {
+  if (!p) return;
+  cudaFree(p->d_win_src);
+  cudaFree(p->d_region);
+  cudaFree(p->d_tok_dst);
+  cudaFree(p->d_relidx);
+  cudaFree(p->d_status);
+  cudaFree(p->d_slot_base);
+  cudaFree(p->d_head_slot_begin);
+  delete p;
+}
+
+int current_device_matches(const swin_attn_plan_s *p) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SWIN_ERR_CUDA;
+  return dev == p->device ? SWIN_OK : SWIN_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *swin_attn_strerror(int status) {
+  switch (status) {
+    case SWIN_OK: return "ok";
+    case SWIN_ERR_INVALID_ARG: return "invalid argument";
+    case SWIN_ERR_UNSUPPORTED: return "unsupported problem (slots > 128, head_dim not 16/32, dtype or impl)";
+    case SWIN_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+    case SWIN_ERR_WORKSPACE: return "workspace missing or too small";
+    case SWIN_ERR_CUDA: return "CUDA runtime error";
+    case SWIN_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    case SWIN_ERR_DEVICE: return "a kernel recorded a device-side error";
+    default: return "unknown status";
+  }
+}
+
+int swin_attn_window_range(int64_t M, int64_t P, int64_t r, int64_t *L, int64_t *R) {
+  if (!L || !R || M < 0 || P < 1 || r < 0 || r >= P) return SWIN_ERR_INVALID_ARG;
+  eq4_range(M, P, r, *L, *R);
+  return SWIN_OK;
+}
+
+int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
+  if (!out) return SWIN_ERR_INVALID_ARG;
+  *out = nullptr;
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  swin_attn_plan_s *p = new (std::nothrow) swin_attn_plan_s;
+  if (!p) return SWIN_ERR_CUDA;
+  std::memset(p, 0, sizeof(*p));
+  p->d = *desc;
+  p->g = make_geo(desc);
+  const Geo &g = p->g;
+  if (cudaGetDevice(&p->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+    free_plan(p);
+    return SWIN_ERR_CUDA;
+  }
+  // kernel family
+  const bool tc_ok = tc_supported(g, desc->dtype);
+  if (desc->impl == SWIN_IMPL_TC && !tc_ok) {
+    free_plan(p);
+    return SWIN_ERR_UNSUPPORTED;
+  }
+  p->impl = desc->impl == SWIN_IMPL_AUTO ? (tc_ok ? SWIN_IMPL_TC : SWIN_IMPL_SIMT) : desc->impl;
+  p->items = (int64_t)g.heads * g.batch * g.nwin;
+  int fwd_bps = 1, bwd_bps = 1;
+  if (p->impl == SWIN_IMPL_SIMT) {
+    if (simt_occupancy(false, g, desc->dtype, &fwd_bps) || simt_occupancy(true, g, desc->dtype, &bwd_bps)) {
+      free_plan(p);
+      return SWIN_ERR_CUDA;
+    }
+  } else {
+    fwd_bps = tc_fwd_ctas_per_sm(g);
+    bwd_bps = tc_bwd_ctas_per_sm(g);
+  }
+  p->fwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, fwd_bps) * p->num_sms);
+  p->bwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, bwd_bps) * p->num_sms);
+  // workspace slots: one partial dBias table per (CTA, head it touches)
+  const int64_t per_head = (int64_t)g.batch * g.nwin;
+  std::vector<int> slot_base(p->bwd_ctas), slot_head;
+  for (int r = 0; r < p->bwd_ctas; ++r) {
+    int64_t L, R;
+    eq4_range(p->items, p->bwd_ctas, r, L, R);
+    slot_base[r] = (int)slot_head.size();
+    if (R > L)
+      for (int64_t h = L / per_head; h <= (R - 1) / per_head; ++h) slot_head.push_back((int)h);
+  }
+  p->ws_slots = (int64_t)slot_head.size();
+  std::vector<int> head_begin(g.heads + 1);
+  for (int h = 0; h <= g.heads; ++h)
+    head_begin[h] = (int)(std::lower_bound(slot_head.begin(), slot_head.end(), h) - slot_head.begin());
+  // device allocations
+  const int64_t nslots = (int64_t)g.nwin * g.n;
+  bool ok = cudaMalloc(&p->d_win_src, sizeof(int32_t) * nslots) == cudaSuccess &&
+            cudaMalloc(&p->d_region, nslots) == cudaSuccess &&
+            cudaMalloc(&p->d_tok_dst, sizeof(int32_t) * g.tokens) == cudaSuccess &&
+            cudaMalloc(&p->d_relidx, sizeof(int32_t) * g.n * g.n) == cudaSuccess &&
+            cudaMalloc(&p->d_status, sizeof(int)) == cudaSuccess &&
+            cudaMalloc(&p->d_slot_base, sizeof(int) * p->bwd_ctas) == cudaSuccess &&
+            cudaMalloc(&p->d_head_slot_begin, sizeof(int) * (g.heads + 1)) == cudaSuccess;
+  ok = ok && cudaMemset(p->d_status, 0, sizeof(int)) == cudaSuccess &&
+       cudaMemcpy(p->d_slot_base, slot_base.data(), sizeof(int) * p->bwd_ctas, cudaMemcpyHostToDevice) == cudaSuccess &&
+       cudaMemcpy(p->d_head_slot_begin, head_begin.data(), sizeof(int) * (g.heads + 1), cudaMemcpyHostToDevice) ==
+           cudaSuccess;
+  if (ok) {
+    const int blocks = (int)std::min<int64_t>((nslots + 255) / 256, 4096);
+    tables_kernel<<<blocks, 256>>>(g, p->d_win_src, p->d_region, p->d_tok_dst);
+    relidx_kernel<<<(g.n * g.n + 255) / 256, 256>>>(g, p->d_relidx);
+    ok = cudaGetLastError() == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
+  }
+  if (!ok) {
+    free_plan(p);
+    return SWIN_ERR_CUDA;
+  }
+  *out = p;
+  return SWIN_OK;
+}
+
+int swin_attn_plan_get_info(swin_attn_plan_t p, swin_attn_plan_info *info) {
+  if (!p || !info) return SWIN_ERR_INVALID_ARG;
+  info->windows_per_image = p->g.nwin;
+  info->tokens_per_image = p->g.tokens;
+  info->slots = p->g.n;
+  info->bias_rows = p->g.T;
+  info->impl = p->impl;
+  info->fwd_ctas = p->fwd_ctas;
+  info->bwd_ctas = p->bwd_ctas;
+  info->num_sms = p->num_sms;
+  info->work_items = p->items;
+  info->dbias_slots = p->ws_slots;
+  return SWIN_OK;
+}
+
+int swin_attn_plan_tables(swin_attn_plan_t p, int32_t *win_src, uint8_t *region, int32_t *tok_dst, int32_t *relidx) {
+  if (!p) return SWIN_ERR_INVALID_ARG;
+  const int64_t nslots = (int64_t)p->g.nwin * p->g.n;
+  bool ok = true;
+  if (win_src) ok = ok && cudaMemcpy(win_src, p->d_win_src, 4 * nslots, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (region) ok = ok && cudaMemcpy(region, p->d_region, nslots, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (tok_dst) ok = ok && cudaMemcpy(tok_dst, p->d_tok_dst, 4 * (int64_t)p->g.tokens, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (relidx) ok = ok && cudaMemcpy(relidx, p->d_relidx, 4 * p->g.n * p->g.n, cudaMemcpyDeviceToHost) == cudaSuccess;
+  return ok ? SWIN_OK : SWIN_ERR_CUDA;
+}
+
+size_t swin_attn_workspace_bytes(swin_attn_plan_t p) {
+  if (!p) return 0;
+  const size_t bytes = (size_t)p->ws_slots * p->g.T * sizeof(float);
+  return (bytes + 255) & ~size_t(255);
+}
+
+int swin_attn_fwd(swin_attn_plan_t p, const void *q, const void *k, const void *v, const float *bias,
+                  const uint8_t *land, void *o, float *lse, swin_stream_t stream) {
+  if (!p || !q || !k || !v || !o) return SWIN_ERR_INVALID_ARG;
+  if (p->d.has_land && !land) return SWIN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SWIN_ERR_ALIGNMENT;
+  if ((bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return SWIN_ERR_ALIGNMENT;
+  int rc = current_device_matches(p);
+  if (rc) return rc;
+  FwdArgs a;
+  a.g = p->g;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.bias = bias;
+  a.land = p->d.has_land ? land : nullptr;
+  a.o = o;
+  a.lse = lse;
+  a.status = p->d_status;
+  a.items = p->items;
+  a.ctas = p->fwd_ctas;
+  a.scale = 1.0f / sqrtf((float)p->g.hd);
+  if (p->impl == SWIN_IMPL_TC) return launch_fwd_tc(a, stream);
+  return launch_fwd_simt(a, p->d.dtype, stream);
+}
+
+int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *v, const void *dout,
+                  const float *lse, const float *bias, const uint8_t *land, void *dq, void *dk, void *dv,
+                  float *dbias, void *workspace, size_t workspace_bytes, swin_stream_t stream) {
+  if (!p || !q || !k || !v || !dout || !lse || !dq || !dk || !dv) return SWIN_ERR_INVALID_ARG;
+  if (p->d.has_land && !land) return SWIN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
+      !aligned16(dv))
+    return SWIN_ERR_ALIGNMENT;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
+      (dbias && (reinterpret_cast<uintptr_t>(dbias) & 3u)))
+    return SWIN_ERR_ALIGNMENT;
+  if (dbias) {
+    if (!workspace || workspace_bytes < swin_attn_workspace_bytes(p)) return SWIN_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SWIN_ERR_ALIGNMENT;
+  }
+  int rc = current_device_matches(p);
+  if (rc) return rc;
+  BwdArgs a;
+  a.g = p->g;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.dout = dout;
+  a.lse = lse;
+  a.bias = bias;
+  a.land = p->d.has_land ? land : nullptr;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.ws = dbias ? static_cast<float *>(workspace) : nullptr;
+  a.slot_base = p->d_slot_base;
+  a.status = p->d_status;
+  a.items = p->items;
+  a.ctas = p->bwd_ctas;
+  a.scale = 1.0f / sqrtf((float)p->g.hd);
+  rc = p->impl == SWIN_IMPL_TC ? launch_bwd_tc(a, stream) : launch_bwd_simt(a, p->d.dtype, stream);
+  if (rc || !dbias) return rc;
+  FoldArgs f;
+  f.ws = a.ws;
+  f.head_slot_begin = p->d_head_slot_begin;
+  f.dbias = dbias;
+  f.T = p->g.T;
+  f.heads = p->g.heads;
+  const int total = f.T * f.heads;
+  fold_kernel<<<(total + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(f);
+  return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
+}
+
+int swin_attn_status(swin_attn_plan_t p, swin_stream_t stream) {
+  if (!p) return SWIN_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return SWIN_ERR_CUDA;
+  int h = 0;
+  if (cudaMemcpy(&h, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return SWIN_ERR_CUDA;
+  if (h != kStatusOk && cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) return SWIN_ERR_CUDA;
+  if (h == kStatusTimeout) return SWIN_ERR_TIMEOUT;
+  return h == kStatusOk ? SWIN_OK : SWIN_ERR_DEVICE;
+}
+
+void swin_attn_plan_destroy(swin_attn_plan_t p) {
+  if (!p) return;
+  cudaDeviceSynchronize();
+  free_plan(p);
+}
+
+}  // extern "C"

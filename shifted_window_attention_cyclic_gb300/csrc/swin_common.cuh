@@ -1,0 +1,139 @@
+// swin_common.cuh -- geometry, routing and launch parameters shared by the
+// CUDA kernels of the SW-MSA library (sm_103a).
+//
+// Routing (TERRA, Sec. IV.D "Differentiable Token Routes"; BEAST page, Model
+// Architecture): slot sigma of window omega sits at rolled position
+// p_d = omega_d * w_d + sigma_d; it is a pad when p_d >= G_d in some dim, else
+// it is fed by the grid token u_d = (p_d + s_d) mod G_d (the roll by -s,
+// inverted). Region bit d = [dim d not periodic, s_d > 0, p_d >= G_d - s_d].
+// All kernels and the table builder call slot_route(), so the tables that the
+// plan exports are exactly the routing the kernels perform.
+#pragma once
+#include <cstdint>
+
+#include "../../include/swin_attn.h"
+
+namespace swin {
+
+// Geometry normalised to three dims: a 2-D problem gets a leading dim of
+// extent 1 (window 1, shift 0, not periodic), which leaves window/slot
+// flattening and bias rows unchanged.
+struct Geo {
+  int G[3], w[3], s[3], per[3], nw[3];
+  int lead;        // 3 - ndim: region bit of normalised dim a is (a - lead)
+  int n;           // slots per window
+  int nwin;        // windows per image
+  int tokens;      // tokens per image
+  int T;           // bias rows
+  int rstride[3];  // prod_{e>d} (2 w_e - 1)
+  int heads, hd, C;
+  int batch;
+  int has_land;
+};
+
+// Routing of one slot of one window (window coords already decoded).
+struct SlotRoute {
+  int src;    // token index inside the image, -1 for a pad
+  int reg;    // region bits (0 for pads)
+  int rbase;  // sum_d (sigma_d + w_d - 1) * rstride_d  (query side of the bias row)
+  int roff;   // sum_d sigma_d * rstride_d                (key side of the bias row)
+};
+
+__host__ __device__ __forceinline__ void window_coords(const Geo &g, int omega, int wc[3]) {
+  wc[2] = omega % g.nw[2];
+  int t = omega / g.nw[2];
+  wc[1] = t % g.nw[1];
+  wc[0] = t / g.nw[1];
+}
+
+__host__ __device__ __forceinline__ SlotRoute slot_route(const Geo &g, const int wc[3], int sigma) {
+  int sc[3];
+  sc[2] = sigma % g.w[2];
+  int t = sigma / g.w[2];
+  sc[1] = t % g.w[1];
+  sc[0] = t / g.w[1];
+  SlotRoute r;
+  r.rbase = 0;
+  r.roff = 0;
+  int src = 0, reg = 0;
+  bool pad = false;
+  for (int a = 0; a < 3; ++a) {
+    int p = wc[a] * g.w[a] + sc[a];
+    pad |= p >= g.G[a];
+    int u = p + g.s[a];
+    if (u >= g.G[a]) u -= g.G[a];
+    src = src * g.G[a] + u;
+    if (!g.per[a] && g.s[a] > 0 && p >= g.G[a] - g.s[a]) reg |= 1 << (a - g.lead);
+    r.rbase += (sc[a] + g.w[a] - 1) * g.rstride[a];
+    r.roff += sc[a] * g.rstride[a];
+  }
+  r.src = pad ? -1 : src;
+  r.reg = pad ? 0 : reg;
+  return r;
+}
+
+// Work items are (head, image, window), head-major: item = (h * B + b) * nwin + omega.
+struct Item {
+  int h, b, omega;
+};
+
+__host__ __device__ __forceinline__ Item decode_item(const Geo &g, int64_t it) {
+  Item x;
+  x.omega = (int)(it % g.nwin);
+  int64_t t = it / g.nwin;
+  x.b = (int)(t % g.batch);
+  x.h = (int)(t / g.batch);
+  return x;
+}
+
+// TERRA Eq. (4): contiguous range of CTA r among P over M items.
+__host__ __device__ __forceinline__ void eq4_range(int64_t M, int64_t P, int64_t r, int64_t &L, int64_t &R) {
+  L = (r * M) / P;
+  R = ((r + 1) * M) / P;
+}
+
+// Device status word values (first error wins).
+enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusBounds = 2 };
+
+struct FwdArgs {
+  Geo g;
+  const void *q, *k, *v;
+  const float *bias;
+  const uint8_t *land;
+  void *o;
+  float *lse;
+  int *status;
+  int64_t items;
+  int ctas;
+  float scale;  // hd^-1/2
+};
+
+struct BwdArgs {
+  Geo g;
+  const void *q, *k, *v, *dout;
+  const float *lse, *bias;
+  const uint8_t *land;
+  void *dq, *dk, *dv;
+  float *ws;              // [slots][T] partial dBias tables, or nullptr (dbias not wanted)
+  const int *slot_base;   // [ctas] first workspace slot of each CTA
+  int *status;
+  int64_t items;
+  int ctas;
+  float scale;
+};
+
+struct FoldArgs {
+  const float *ws;
+  const int *head_slot_begin;  // [heads + 1] slot range of every head
+  float *dbias;                // [T][heads]
+  int T, heads;
+};
+
+// Launchers implemented in the kernel translation units.
+int launch_fwd_simt(const FwdArgs &a, int dtype, void *stream);
+int launch_bwd_simt(const BwdArgs &a, int dtype, void *stream);
+int simt_fwd_smem(const Geo &g);
+int simt_bwd_smem(const Geo &g);
+int simt_occupancy(bool bwd, const Geo &g, int dtype, int *blocks_per_sm);
+
+}  // namespace swin

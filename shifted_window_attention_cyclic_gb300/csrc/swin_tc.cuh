@@ -1,0 +1,14 @@
+// swin_tc.cuh -- entry points of the tcgen05/TMEM kernels (bf16, head_dim 32).
+#pragma once
+#include "swin_common.cuh"
+
+namespace swin {
+
+// True when the tensor-core kernels take this problem.
+bool tc_supported(const Geo &g, int dtype);
+int tc_fwd_ctas_per_sm(const Geo &g);
+int tc_bwd_ctas_per_sm(const Geo &g);
+int launch_fwd_tc(const FwdArgs &a, void *stream);
+int launch_bwd_tc(const BwdArgs &a, void *stream);
+
+}  // namespace swin
