@@ -149,12 +149,14 @@ def oracle_sample_rate(wl, x, windows, seed=0):
     return tokens, time.perf_counter() - t0
 
 
-def cpu_baseline(wl, x, target_s=12.0):
+def cpu_baseline(wl, x, target_s=15.0):
     import oracle
     oracle.build()
-    tok, dt = oracle_sample_rate(wl, x, 16, seed=1)
-    per_window = dt / 16
-    windows = int(max(16, min(wl.batch * 9216, target_s / max(per_window, 1e-6))))
+    calib = 256
+    tok, dt = oracle_sample_rate(wl, x, calib, seed=1)
+    per_window = dt / calib
+    nwin = oracle.Problem(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim).nwin
+    windows = int(max(calib, min(wl.batch * nwin, target_s / max(per_window, 1e-6))))
     tok, dt = oracle_sample_rate(wl, x, windows, seed=2)
     return {"value": tok / dt / 1e6, "unit": "Mtokens/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "%d random windows of %s (%d tokens), fwd+bwd, fp64 C oracle, %.1f s" %

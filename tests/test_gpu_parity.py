@@ -105,7 +105,7 @@ SWEEP = [
     ((9, 40), (3, 12), (1, 6), (0, 1), 2, 32, 1, "f32", (0.4, 0.4)),
     ((4, 9, 21), (2, 4, 8), (1, 2, 4), (0, 0, 1), 2, 32, 1, "bf16", (0.2, 0.5)),
     ((3, 10, 13), (2, 3, 5), (1, 1, 2), (0, 1, 1), 1, 16, 2, "f32", (0.3, 0.6)),
-    ((12, 16), (12, 16), (0, 0), (0, 1), 2, 32, 1, "bf16", None),        # one window = global attention
+    ((8, 16), (8, 16), (0, 0), (0, 1), 2, 32, 1, "bf16", None),          # one window = global attention
     ((8, 128), (1, 128), (0, 64), (0, 1), 2, 32, 1, "bf16", None),       # n = 128 along lon only
     ((16, 24), (4, 6), (0, 0), (0, 1), 4, 32, 3, "bf16", (0.3, 0.3)),    # W-MSA, batch 3
     ((7, 7), (8, 8), (0, 0), (0, 0), 2, 32, 1, "bf16", None),            # window larger than grid
