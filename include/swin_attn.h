@@ -145,6 +145,14 @@ int swin_attn_bwd(swin_attn_plan_t plan, const void *q, const void *k, const voi
                   const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,
                   void *workspace, size_t workspace_bytes, swin_stream_t stream);
 
+/* Testing hook for the failure path of the tensor-core kernels. Every wait
+ * inside those kernels gives up after `wait_limit_ns` (default 1 s) and then
+ * records SWIN_ERR_TIMEOUT in the status word. force_timeout = 1 makes one
+ * role of the next launches wait on a barrier that nothing arrives at, so the
+ * bounded wait runs out on purpose (the kernel then drains and exits).
+ * Errors: INVALID_ARG (NULL plan, zero limit, force_timeout not 0/1). */
+int swin_attn_plan_set_debug(swin_attn_plan_t plan, uint64_t wait_limit_ns, int force_timeout);
+
 /* Synchronise `stream`, read and clear the plan's device status word.
  * Returns SWIN_OK, SWIN_ERR_TIMEOUT, SWIN_ERR_DEVICE or SWIN_ERR_CUDA. */
 int swin_attn_status(swin_attn_plan_t plan, swin_stream_t stream);

@@ -29,6 +29,8 @@ struct swin_attn_plan_s {
   int *d_status;
   int *d_slot_base;        // [bwd_ctas]
   int *d_head_slot_begin;  // [heads + 1]
+  uint64_t wait_limit_ns;  // bound of every in-kernel wait
+  int debug_force_timeout;
 };
 
 namespace {
@@ -169,6 +171,8 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
   std::memset(p, 0, sizeof(*p));
   p->d = *desc;
   p->g = make_geo(desc);
+  p->wait_limit_ns = 1000000000ull;
+  p->debug_force_timeout = 0;
   const Geo &g = p->g;
   if (cudaGetDevice(&p->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
@@ -290,6 +294,8 @@ int swin_attn_fwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.items = p->items;
   a.ctas = p->fwd_ctas;
   a.scale = 1.0f / sqrtf((float)p->g.hd);
+  a.wait_limit_ns = p->wait_limit_ns;
+  a.debug_force_timeout = p->debug_force_timeout;
   if (p->impl == SWIN_IMPL_TC) return launch_fwd_tc(a, stream);
   return launch_fwd_simt(a, p->d.dtype, stream);
 }
@@ -329,6 +335,8 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.items = p->items;
   a.ctas = p->bwd_ctas;
   a.scale = 1.0f / sqrtf((float)p->g.hd);
+  a.wait_limit_ns = p->wait_limit_ns;
+  a.debug_force_timeout = p->debug_force_timeout;
   rc = p->impl == SWIN_IMPL_TC ? launch_bwd_tc(a, stream) : launch_bwd_simt(a, p->d.dtype, stream);
   if (rc || !dbias) return rc;
   FoldArgs f;
@@ -340,6 +348,13 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   const int total = f.T * f.heads;
   fold_kernel<<<(total + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(f);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
+}
+
+int swin_attn_plan_set_debug(swin_attn_plan_t p, uint64_t wait_limit_ns, int force_timeout) {
+  if (!p || wait_limit_ns == 0 || (force_timeout != 0 && force_timeout != 1)) return SWIN_ERR_INVALID_ARG;
+  p->wait_limit_ns = wait_limit_ns;
+  p->debug_force_timeout = force_timeout;
+  return SWIN_OK;
 }
 
 int swin_attn_status(swin_attn_plan_t p, swin_stream_t stream) {

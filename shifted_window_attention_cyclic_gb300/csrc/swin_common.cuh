@@ -106,6 +106,8 @@ struct FwdArgs {
   int64_t items;
   int ctas;
   float scale;  // hd^-1/2
+  uint64_t wait_limit_ns;   // bound of every in-kernel wait
+  int debug_force_timeout;  // testing hook: one role waits on a barrier nothing arrives at
 };
 
 struct BwdArgs {
@@ -120,6 +122,8 @@ struct BwdArgs {
   int64_t items;
   int ctas;
   float scale;
+  uint64_t wait_limit_ns;
+  int debug_force_timeout;
 };
 
 struct FoldArgs {

@@ -1,14 +1,356 @@
-// swin_tc.cu -- tcgen05/TMEM kernels of SW-MSA (bf16, head_dim 32).
+// swin_tc.cu -- tcgen05/TMEM kernels of SW-MSA for bf16, head_dim 32,
+// windows of up to 128 slots (sm_103a).
+//
+// Forward, per work item (head h, image b, window omega), one item at a time
+// per CTA stage, persistent CTAs over TERRA Eq. (4) contiguous item ranges:
+//  * gather warps (4): route every slot (cyclic shift, ragged edge, pads) and
+//    cp.async its Q, K, V rows (64 B each) straight from the [B, grid, C]
+//    tensors into 64B-swizzled smem tiles; pads are zero-filled. They also
+//    write two K=16 mask tiles: Qm (one-hot of the query's region bits) and
+//    Km (0 where the key is a live key of that region, -2^100 elsewhere), so
+//    that one extra MMA step adds the region/land/pad mask to QK^T.
+//  * MMA warp (1 elected thread): S = Q K^T + Qm Km^T into TMEM (fp32),
+//    then O = P V with P read from TMEM (bf16).
+//  * softmax warpgroups (2, ping-pong on alternate items): one thread per
+//    TMEM lane (query slot). Logits x = S * scale*log2e + bias*log2e, where the
+//    per-head bias tile [slot_i][slot_j] stays resident in TMEM; row max, exp2,
+//    row sum, P written back over S as bf16; after PV the thread normalises
+//    its O row and stores it at the slot's grid token (the reverse route),
+//    plus the log-sum-exp.
+// Masked keys get exactly zero probability: exp2 of about -3e29 is +0.
+//
+// Every wait is bounded (globaltimer); on timeout the CTA raises an abort
+// flag, every role leaves its loop, copies and MMAs in flight are drained,
+// TMEM is freed and the device status word reports a timeout.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "swin_tc.cuh"
+#include "tc_ptx.cuh"
 
 namespace swin {
+namespace {
 
-bool tc_supported(const Geo &, int) { return false; }
+using namespace ptx;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint16_t kBf16One = 0x3F80;   // 1.0
+constexpr uint16_t kBf16NegBig = 0xF180;  // -2^100
+
+// Swizzled byte offsets inside a tile (16-byte chunk c of row r).
+__device__ __forceinline__ uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
+__device__ __forceinline__ uint32_t sw32(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
+
+__device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
+
+// ---------------------------------------------------------------- forward ---
+namespace fwd {
+
+constexpr int kStages = 4;
+constexpr int kTileBytes = 128 * 64;  // 128 slot rows x 32 bf16
+constexpr int kMaskBytes = 128 * 32;  // 128 rows x 16 bf16
+constexpr int kQ = 0, kK = kTileBytes, kV = 2 * kTileBytes, kQm = 3 * kTileBytes, kKm = kQm + kMaskBytes;
+constexpr int kMeta = kKm + kMaskBytes;  // int32 src[128], uint8 live[128]
+constexpr int kStageBytes = kMeta + 1024;
+constexpr int kBarOff = kStages * kStageBytes;
+// barrier indices
+constexpr int bFull = 0, bEmpty = kStages, bSFull = 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
+              bTFree = bOFull + 2, bHcArrive = bTFree + 2, bHcDone = bHcArrive + 1, bNever = bHcDone + 1,
+              bDrain = bNever + 1, kNumBars = bDrain + 1;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+
+constexpr int kSoftmaxWarps = 8, kProducerWarps = 4;
+constexpr int kProducerWarp0 = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + kProducerWarps;
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+// TMEM columns
+constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256, kColBias = 384;
+
+__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kBarOff;
+  auto bar = [&](int idx) { return bars + 8u * idx; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kMiscOff + 4);
+
+  const Geo &g = a.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = g.n, N = round16(n), NG = N >> 4;
+  int64_t L, R;
+  eq4_range(a.items, a.ctas, blockIdx.x, L, R);
+  const int64_t count = R - L;
+  WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(bFull + s), kProducerWarps * 32);
+      mbar_init(bar(bEmpty + s), 1);
+    }
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bar(bSFull + w), 1);
+      mbar_init(bar(bPFull + w), 128);
+      mbar_init(bar(bOFull + w), 1);
+      mbar_init(bar(bTFree + w), 128);
+    }
+    mbar_init(bar(bHcArrive), kSoftmaxWarps * 32);
+    mbar_init(bar(bHcDone), kSoftmaxWarps * 32);
+    mbar_init(bar(bNever), 1);
+    mbar_init(bar(bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= kProducerWarp0 && warp < kMmaWarp) {
+    // ------------------------------------------------------------ gather ---
+    const int pt = threadIdx.x - kProducerWarp0 * 32;  // slot row 0..127
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
+    int64_t issued = 0;
+    for (int64_t it = 0; it < count; ++it) {
+      const int s = (int)(it % kStages);
+      if (it >= kStages && !mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      const Item x = decode_item(g, L + it);
+      int wc[3];
+      window_coords(g, x.omega, wc);
+      SlotRoute r = {-1, 0, 0, 0};
+      if (pt < n) r = slot_route(g, wc, pt);
+      const bool valid = r.src >= 0;
+      const int64_t tok = (int64_t)x.b * g.tokens + (valid ? r.src : 0);
+      const bool live = valid && !(g.has_land && a.land[tok]);
+      const int64_t off = tok * g.C + (int64_t)x.h * 32;
+      const uint32_t nb = valid ? 16u : 0u;
+      const uint32_t st = sbase + s * kStageBytes;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        cp_async16(st + kQ + sw64(pt, c), q + off + 8 * c, nb);
+        cp_async16(st + kK + sw64(pt, c), k + off + 8 * c, nb);
+        cp_async16(st + kV + sw64(pt, c), v + off + 8 * c, nb);
+      }
+      uint32_t qm[8], km[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const uint32_t lo = (live && r.reg == 2 * w) ? 0u : kBf16NegBig;
+        const uint32_t hi = (live && r.reg == 2 * w + 1) ? 0u : kBf16NegBig;
+        km[w] = lo | (hi << 16);
+        const uint32_t qlo = (live && r.reg == 2 * w) ? kBf16One : 0u;
+        const uint32_t qhi = (live && r.reg == 2 * w + 1) ? kBf16One : 0u;
+        qm[w] = qlo | (qhi << 16);
+      }
+      uint8_t *sp = smem + s * kStageBytes;
+      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
+      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
+      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
+      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
+      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? r.src : -1;
+      (sp + kMeta + 512)[pt] = live ? 1 : 0;
+      cp_async_commit();
+      if (it > 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(bar(bFull + (int)((it - 1) % kStages)));
+      }
+      issued = it + 1;
+    }
+    cp_async_wait_all();
+    if (issued > 0 && !*abort_flag) {
+      fence_proxy_async_smem();
+      mbar_arrive(bar(bFull + (int)((issued - 1) % kStages)));
+    }
+  } else if (warp == kMmaWarp) {
+    // --------------------------------------------------------------- MMA ---
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16(128, N, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16(128, 32, 0, 1);
+      auto issue_s = [&](int64_t it) -> bool {
+        const int s = (int)(it % kStages), wb = (int)(it & 1);
+        if (!mbar_wait(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) return false;
+        if (it >= 2 && !mbar_wait(bar(bTFree + wb), (uint32_t)((it >> 1) - 1) & 1u, ctl)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + s * kStageBytes;
+        const uint32_t d = tmem + kColS + 128u * wb;
+        mma_ss(d, smem_desc(st + kQ, 16, 512, kSwizzle64B), smem_desc(st + kK, 16, 512, kSwizzle64B), idesc_qk, 0);
+        mma_ss(d, smem_desc(st + kQ + 32, 16, 512, kSwizzle64B), smem_desc(st + kK + 32, 16, 512, kSwizzle64B),
+               idesc_qk, 1);
+        mma_ss(d, smem_desc(st + kQm, 16, 256, kSwizzle32B), smem_desc(st + kKm, 16, 256, kSwizzle32B), idesc_qk, 1);
+        mma_commit(bar(bSFull + wb));
+        return true;
+      };
+      auto issue_pv = [&](int64_t it) -> bool {
+        const int s = (int)(it % kStages), wb = (int)(it & 1);
+        if (!mbar_wait(bar(bPFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + s * kStageBytes;
+        const uint32_t d = tmem + kColO + 32u * wb, p = tmem + kColS + 128u * wb;
+        for (int kk = 0; kk < NG; ++kk)
+          mma_ts(d, p + 8u * kk, smem_desc(st + kV + 1024u * kk, kTileBytes, 512, kSwizzle64B), idesc_pv,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(bar(bOFull + wb));
+        mma_commit(bar(bEmpty + s));
+        return true;
+      };
+      if (count > 0 && issue_s(0)) {
+        for (int64_t it = 0; it < count; ++it) {
+          if (it + 1 < count && !issue_s(it + 1)) break;
+          if (!issue_pv(it)) break;
+        }
+      }
+      // drain every MMA this thread issued before TMEM is released
+      mma_commit(bar(bDrain));
+      volatile int no_abort = 0;
+      WaitCtl drain_ctl{&no_abort, a.status, a.wait_limit_ns};
+      mbar_wait(bar(bDrain), 0, drain_ctl);
+    }
+    __syncwarp();
+  } else {
+    // ----------------------------------------------------------- softmax ---
+    const int grp = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + kColS + 128u * grp;
+    const uint32_t tO = tmem + lane_addr + kColO + 32u * grp;
+    const uint32_t tB = tmem + lane_addr + kColBias;
+    const float cs = a.scale * kLog2e;
+    const float2 cs2 = make_float2(cs, cs);
+    int cur_h = -1;
+    uint32_t hc = 0;
+    bool ok = true;
+    if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
+    for (int64_t it = 0; ok && it < count; ++it) {
+      const Item x = decode_item(g, L + it);
+      if (x.h != cur_h) {
+        // head change: both warpgroups finished the previous head's items;
+        // each writes half of the bias tile (columns 64*grp .. +63) of its lane.
+        mbar_arrive(bar(bHcArrive));
+        if (!mbar_wait_warp(bar(bHcArrive), hc & 1u, ctl)) break;
+        tc_fence_after();
+        int wc0[3] = {0, 0, 0};
+        const int rb = (i < n) ? slot_route(g, wc0, i).rbase : 0;
+#pragma unroll 1
+        for (int jg = 0; jg < 4; ++jg) {
+          uint32_t vals[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int j = 64 * grp + 16 * jg + e;
+            float b = 0.f;
+            if (i < n && j < n && a.bias) b = a.bias[(int64_t)(rb - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
+            vals[e] = __float_as_uint(b);
+          }
+          tmem_st16(tB + 64u * grp + 16u * jg, vals);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar(bHcDone));
+        if (!mbar_wait_warp(bar(bHcDone), hc & 1u, ctl)) break;
+        tc_fence_after();
+        ++hc;
+        cur_h = x.h;
+      }
+      if ((int)(it & 1) != grp) continue;
+      const uint32_t kk = (uint32_t)(it >> 1);
+      const int s = (int)(it % kStages);
+      if (!mbar_wait_warp(bar(bSFull + grp), kk & 1u, ctl)) break;
+      tc_fence_after();
+      if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
+      const uint8_t *sp = smem + s * kStageBytes;
+      const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
+      const bool live = (sp + kMeta + 512)[i] != 0;
+      // pass 1: row max of x = S*cs + bias
+      float m = -INFINITY;
+      for (int gi = 0; gi < NG; ++gi) {
+        uint32_t sv[16], bv[16];
+        tmem_ld16(tS + 16u * gi, sv);
+        tmem_ld16(tB + 16u * gi, bv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
+                                       make_float2(__uint_as_float(bv[e]), __uint_as_float(bv[e + 1])));
+          m = max3(m, xs.x, xs.y);
+        }
+      }
+      // pass 2: p = exp2(x - m), row sum, P (bf16) written over S
+      const float2 negm = make_float2(-m, -m);
+      float2 sum2 = make_float2(0.f, 0.f);
+      for (int gi = 0; gi < NG; ++gi) {
+        uint32_t sv[16], bv[16], pv[8];
+        tmem_ld16(tS + 16u * gi, sv);
+        tmem_ld16(tB + 16u * gi, bv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
+                                 make_float2(__uint_as_float(bv[e]), __uint_as_float(bv[e + 1])));
+          xs = __fadd2_rn(xs, negm);
+          const float2 p = make_float2(ex2(xs.x), ex2(xs.y));
+          sum2 = __fadd2_rn(sum2, p);
+          pv[e >> 1] = pack_bf16(p.x, p.y);
+        }
+        tmem_st8(tS + 8u * gi, pv);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(bPFull + grp));
+      if (!mbar_wait_warp(bar(bOFull + grp), kk & 1u, ctl)) break;
+      tc_fence_after();
+      uint32_t ov[32];
+      tmem_ld16(tO, *reinterpret_cast<uint32_t(*)[16]>(ov));
+      tmem_ld16(tO + 16, *reinterpret_cast<uint32_t(*)[16]>(ov + 16));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(bTFree + grp));
+      if (i < n && src >= 0) {
+        const int64_t tok = (int64_t)x.b * g.tokens + src;
+        uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)x.h * 32);
+        const float sum = sum2.x + sum2.y;
+        const float inv = live ? 1.0f / sum : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(ov[8 * c + 2 * e]) * inv, __uint_as_float(ov[8 * c + 2 * e + 1]) * inv);
+          op[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (a.lse)
+          a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m + __log2f(sum)) * kLn2 : -INFINITY;
+      }
+    }
+    tmem_wait_st();
+    tmem_wait_ld();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace fwd
+}  // namespace
+
+bool tc_supported(const Geo &g, int dtype) { return dtype == SWIN_BF16 && g.hd == 32 && g.n <= 128; }
 int tc_fwd_ctas_per_sm(const Geo &) { return 1; }
 int tc_bwd_ctas_per_sm(const Geo &) { return 1; }
-int launch_fwd_tc(const FwdArgs &, void *) { return SWIN_ERR_UNSUPPORTED; }
-int launch_bwd_tc(const BwdArgs &, void *) { return SWIN_ERR_UNSUPPORTED; }
+
+int launch_fwd_tc(const FwdArgs &a, void *stream) {
+  auto kern = fwd::fwd_tc_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmemBytes) != cudaSuccess)
+    return SWIN_ERR_CUDA;
+  kern<<<a.ctas, fwd::kThreads, fwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
+}
+
+int launch_bwd_tc(const BwdArgs &a, void *stream) { return launch_bwd_simt(a, SWIN_BF16, stream); }
 
 }  // namespace swin

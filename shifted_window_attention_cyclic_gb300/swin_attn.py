@@ -82,6 +82,8 @@ def load_library():
     lib.swin_attn_fwd.restype = ctypes.c_int
     lib.swin_attn_bwd.argtypes = [vp] * 13 + [sz, vp]
     lib.swin_attn_bwd.restype = ctypes.c_int
+    lib.swin_attn_plan_set_debug.argtypes = [vp, ctypes.c_uint64, ctypes.c_int]
+    lib.swin_attn_plan_set_debug.restype = ctypes.c_int
     lib.swin_attn_status.argtypes = [vp, vp]
     lib.swin_attn_status.restype = ctypes.c_int
     lib.swin_attn_plan_destroy.argtypes = [vp]
@@ -211,6 +213,11 @@ def swin_attn_bwd(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv, dbias,
 
 def swin_attn_status(plan: Plan, stream=None) -> int:
     return int(load_library().swin_attn_status(plan.handle, _stream(stream)))
+
+
+def swin_attn_plan_set_debug(plan: Plan, wait_limit_ns: int, force_timeout: int) -> None:
+    _check(load_library().swin_attn_plan_set_debug(plan.handle, int(wait_limit_ns), int(force_timeout)),
+           "swin_attn_plan_set_debug")
 
 
 def swin_attn_plan_destroy(plan: Plan) -> None:

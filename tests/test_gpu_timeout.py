@@ -1,0 +1,47 @@
+"""Failure path of the tensor-core kernels, without any GPU fault.
+
+The plan's testing hook makes one role of the next launch wait on an mbarrier
+that nothing arrives at. The bounded wait gives up after a short limit, the
+CTA drains its copies and MMAs, frees TMEM and exits; the host reads
+SWIN_ERR_TIMEOUT from the device status word. The same plan then runs
+normally again and matches the oracle, so the context stayed usable."""
+import numpy as np
+import pytest
+
+import oracle
+from shifted_window_attention_cyclic_gb300 import workloads
+from tests.parity_util import assert_close, host, problem_of, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def test_forced_wait_timeout_is_reported_and_recoverable():
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    wl = workloads.custom((13, 27), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3), seed_index=91)
+    x = workloads.generate(wl)
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch,
+                               wl.dtype, wl.has_land, "tc")
+    assert attn.info.impl == C.SWIN_IMPL_TC
+    t = to_device(x, wl, torch.device("cuda", 0))
+    C.swin_attn_plan_set_debug(attn.plan, 5_000_000, 1)  # 5 ms limit, forced wait
+    attn.forward(t["q"], t["k"], t["v"], t["bias"], t["land"])
+    assert C.swin_attn_status(attn.plan) == C.SWIN_ERR_TIMEOUT
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK  # status word was cleared
+    C.swin_attn_plan_set_debug(attn.plan, 1_000_000_000, 0)
+    o, _ = attn.forward(t["q"], t["k"], t["v"], t["bias"], t["land"])
+    torch.cuda.synchronize()
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK
+    o_ref, _ = oracle.fwd(problem_of(wl), x["q"], x["k"], x["v"], x["bias"], x["land"])
+    assert_close("O", host(o), o_ref, wl.dtype)
+
+
+def test_debug_hook_rejects_bad_arguments():
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    attn = SwinWindowAttention((8, 16), (4, 8), (2, 4), (0, 1), 2, 32)
+    lib = C.load_library()
+    assert lib.swin_attn_plan_set_debug(attn.plan.handle, 0, 0) == C.SWIN_ERR_INVALID_ARG
+    assert lib.swin_attn_plan_set_debug(attn.plan.handle, 10, 2) == C.SWIN_ERR_INVALID_ARG
+    assert lib.swin_attn_plan_set_debug(None, 10, 0) == C.SWIN_ERR_INVALID_ARG
