@@ -337,6 +337,394 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
 }
 
 }  // namespace fwd
+
+// --------------------------------------------------------------- backward ---
+// Per work item: S = Q K^T + mask and dP = dO V^T into TMEM; one thread per
+// query row recomputes P = exp2(S*cs + bias2 - lse2) (pass 1: delta_i =
+// sum_j P_ij dP_ij, P to smem for dV), then dS = P (dP - delta) (pass 2: dS to
+// smem for dK and dQ, added into the per-head dBias slot-pair accumulator kept
+// in TMEM). dV = P^T dO, dK = dS^T Q and dQ = dS K run on the tensor cores;
+// the epilogue warps store them at the slots' grid tokens (the inverse route).
+// The bias tile of the current head lives in smem (row i is only read by
+// thread i); at a head change the TMEM accumulator is folded into bias rows
+// in a fixed order and written to the CTA's workspace slot.
+namespace bwd {
+
+constexpr int kStages = 2;
+constexpr int kTile = 128 * 64, kMask = 128 * 32;
+constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kdO = 3 * kTile, kQm = 4 * kTile, kKm = kQm + kMask;
+constexpr int kMeta = kKm + kMask;  // int32 src[128] @0, float lse2[128] @512, uint8 live[128] @1024
+constexpr int kStageBytes = kMeta + 2048;
+constexpr int kP = kStages * kStageBytes;  // P tile, bf16, [j-atom][i][64 j], 128B swizzle
+constexpr int kdS = kP + 32768;            // dS tile, same layout
+constexpr int kBias = kdS + 32768;         // fp32 [128][kBiasStride]: bias*log2e, or the dBias fold buffer
+constexpr int kBiasStride = 132;
+constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
+constexpr int bFull = 0, bEmpty = kStages, bSpFull = 2 * kStages, bPFull = bSpFull + 1, bDsFull = bPFull + 1,
+              bAccFull = bDsFull + 1, bAccFree = bAccFull + 1, bDsFree = bAccFree + 1, bWsync = bDsFree + 1,
+              bNever = bWsync + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+
+constexpr int kEpilogueWarp0 = 4, kProducerWarp0 = 8, kMmaWarp = 12;  // softmax warps 0-3
+constexpr int kThreads = (kMmaWarp + 1) * 32;
+constexpr uint32_t kTmemCols = 512, kColS = 0, kColdP = 128, kColdV = 256, kColdK = 288, kColdQ = 320,
+                   kColAcc = 384;
+
+// byte offset of the 16-byte chunk holding j = 8c..8c+7 of row i in a P/dS tile
+__device__ __forceinline__ uint32_t pds_chunk(int i, int c) {
+  return (c >> 3) * 16384 + (i >> 3) * 1024 + (i & 7) * 128 + (((c & 7) ^ (i & 7)) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kBarOff;
+  auto bar = [&](int idx) { return bars + 8u * idx; };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kMiscOff);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kMiscOff + 4);
+
+  const Geo &g = a.g;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = g.n, N = round16(n), NG = N >> 4;
+  int64_t L, R;
+  eq4_range(a.items, a.ctas, blockIdx.x, L, R);
+  const int64_t count = R - L;
+  WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(bFull + s), 128);
+      mbar_init(bar(bEmpty + s), 1 + 128);
+    }
+    mbar_init(bar(bSpFull), 1);
+    mbar_init(bar(bPFull), 128);
+    mbar_init(bar(bDsFull), 128);
+    mbar_init(bar(bAccFull), 1);
+    mbar_init(bar(bAccFree), 128);
+    mbar_init(bar(bDsFree), 1);
+    mbar_init(bar(bWsync), 128);
+    mbar_init(bar(bNever), 1);
+    mbar_init(bar(bDrain), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= kProducerWarp0 && warp < kMmaWarp) {
+    // ------------------------------------------------------------ gather ---
+    const int pt = threadIdx.x - kProducerWarp0 * 32;
+    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
+    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
+    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
+    const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
+    int64_t issued = 0;
+    for (int64_t it = 0; it < count; ++it) {
+      const int s = (int)(it % kStages);
+      if (it >= kStages && !mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      const Item x = decode_item(g, L + it);
+      int wc[3];
+      window_coords(g, x.omega, wc);
+      SlotRoute r = {-1, 0, 0, 0};
+      if (pt < n) r = slot_route(g, wc, pt);
+      const bool valid = r.src >= 0;
+      const int64_t tok = (int64_t)x.b * g.tokens + (valid ? r.src : 0);
+      const bool live = valid && !(g.has_land && a.land[tok]);
+      const int64_t off = tok * g.C + (int64_t)x.h * 32;
+      const uint32_t nb = valid ? 16u : 0u;
+      const uint32_t st = sbase + s * kStageBytes;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        cp_async16(st + kQ + sw64(pt, c), q + off + 8 * c, nb);
+        cp_async16(st + kK + sw64(pt, c), k + off + 8 * c, nb);
+        cp_async16(st + kV + sw64(pt, c), v + off + 8 * c, nb);
+        cp_async16(st + kdO + sw64(pt, c), dout + off + 8 * c, nb);
+      }
+      uint32_t qm[8], km[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const uint32_t lo = (live && r.reg == 2 * w) ? 0u : kBf16NegBig;
+        const uint32_t hi = (live && r.reg == 2 * w + 1) ? 0u : kBf16NegBig;
+        km[w] = lo | (hi << 16);
+        const uint32_t qlo = (live && r.reg == 2 * w) ? kBf16One : 0u;
+        const uint32_t qhi = (live && r.reg == 2 * w + 1) ? kBf16One : 0u;
+        qm[w] = qlo | (qhi << 16);
+      }
+      uint8_t *sp = smem + s * kStageBytes;
+      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
+      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
+      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
+      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
+      const float lse = live ? a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + r.src] : 0.f;
+      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? r.src : -1;
+      reinterpret_cast<float *>(sp + kMeta + 512)[pt] = lse * kLog2e;
+      (sp + kMeta + 1024)[pt] = live ? 1 : 0;
+      cp_async_commit();
+      if (it > 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(bar(bFull + (int)((it - 1) % kStages)));
+      }
+      issued = it + 1;
+    }
+    cp_async_wait_all();
+    if (issued > 0 && !*abort_flag) {
+      fence_proxy_async_smem();
+      mbar_arrive(bar(bFull + (int)((issued - 1) % kStages)));
+    }
+  } else if (warp == kMmaWarp) {
+    // --------------------------------------------------------------- MMA ---
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16(128, N, 0, 0);
+      const uint32_t idesc_mn = idesc_bf16(128, 32, 1, 1);
+      const uint32_t idesc_dq = idesc_bf16(128, 32, 0, 1);
+      const uint32_t tS = tmem + kColS, tdP = tmem + kColdP;
+      auto issue_sdp = [&](int64_t it) -> bool {
+        const int s = (int)(it % kStages);
+        if (!mbar_wait(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) return false;
+        tc_fence_after();
+        const uint32_t st = sbase + s * kStageBytes;
+        mma_ss(tS, smem_desc(st + kQ, 16, 512, kSwizzle64B), smem_desc(st + kK, 16, 512, kSwizzle64B), idesc_s, 0);
+        mma_ss(tS, smem_desc(st + kQ + 32, 16, 512, kSwizzle64B), smem_desc(st + kK + 32, 16, 512, kSwizzle64B),
+               idesc_s, 1);
+        mma_ss(tS, smem_desc(st + kQm, 16, 256, kSwizzle32B), smem_desc(st + kKm, 16, 256, kSwizzle32B), idesc_s, 1);
+        mma_ss(tdP, smem_desc(st + kdO, 16, 512, kSwizzle64B), smem_desc(st + kV, 16, 512, kSwizzle64B), idesc_s, 0);
+        mma_ss(tdP, smem_desc(st + kdO + 32, 16, 512, kSwizzle64B), smem_desc(st + kV + 32, 16, 512, kSwizzle64B),
+               idesc_s, 1);
+        mma_commit(bar(bSpFull));
+        return true;
+      };
+      bool ok = count > 0 && issue_sdp(0);
+      for (int64_t it = 0; ok && it < count; ++it) {
+        const int s = (int)(it % kStages);
+        const uint32_t st = sbase + s * kStageBytes;
+        if (!mbar_wait(bar(bPFull), (uint32_t)it & 1u, ctl)) break;
+        if (it >= 1 && !mbar_wait(bar(bAccFree), (uint32_t)(it - 1) & 1u, ctl)) break;
+        tc_fence_after();
+        for (int kk = 0; kk < 8; ++kk)  // dV = P^T dO: M = keys, K = queries
+          mma_ss(tmem + kColdV, smem_desc(sbase + kP + 2048u * kk, 16384, 1024, kSwizzle128B),
+                 smem_desc(st + kdO + 1024u * kk, kTile, 512, kSwizzle64B), idesc_mn, kk > 0 ? 1u : 0u);
+        if (!mbar_wait(bar(bDsFull), (uint32_t)it & 1u, ctl)) break;
+        tc_fence_after();
+        if (it + 1 < count && !issue_sdp(it + 1)) break;
+        for (int kk = 0; kk < 8; ++kk)  // dK = dS^T Q
+          mma_ss(tmem + kColdK, smem_desc(sbase + kdS + 2048u * kk, 16384, 1024, kSwizzle128B),
+                 smem_desc(st + kQ + 1024u * kk, kTile, 512, kSwizzle64B), idesc_mn, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < NG; ++kk)  // dQ = dS K: M = queries, K = keys
+          mma_ss(tmem + kColdQ, smem_desc(sbase + kdS + 16384u * (kk >> 2) + 32u * (kk & 3), 16, 1024, kSwizzle128B),
+                 smem_desc(st + kK + 1024u * kk, kTile, 512, kSwizzle64B), idesc_dq, kk > 0 ? 1u : 0u);
+        mma_commit(bar(bAccFull));
+        mma_commit(bar(bDsFree));
+        mma_commit(bar(bEmpty + s));
+      }
+      mma_commit(bar(bDrain));
+      volatile int no_abort = 0;
+      WaitCtl drain_ctl{&no_abort, a.status, a.wait_limit_ns};
+      mbar_wait(bar(bDrain), 0, drain_ctl);
+    }
+    __syncwarp();
+  } else if (warp >= kEpilogueWarp0) {
+    // ---------------------------------------------------------- epilogue ---
+    const int q4 = warp & 3, e = q4 * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    for (int64_t it = 0; it < count; ++it) {
+      const int s = (int)(it % kStages);
+      if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
+      const int src = reinterpret_cast<const int *>(smem + s * kStageBytes + kMeta)[e];
+      mbar_arrive(bar(bEmpty + s));
+      if (!mbar_wait_warp(bar(bAccFull), (uint32_t)it & 1u, ctl)) break;
+      tc_fence_after();
+      uint32_t dv[32], dk[32], dq[32];
+      tmem_ld16(tmem + lane_addr + kColdV, *reinterpret_cast<uint32_t(*)[16]>(dv));
+      tmem_ld16(tmem + lane_addr + kColdV + 16, *reinterpret_cast<uint32_t(*)[16]>(dv + 16));
+      tmem_ld16(tmem + lane_addr + kColdK, *reinterpret_cast<uint32_t(*)[16]>(dk));
+      tmem_ld16(tmem + lane_addr + kColdK + 16, *reinterpret_cast<uint32_t(*)[16]>(dk + 16));
+      tmem_ld16(tmem + lane_addr + kColdQ, *reinterpret_cast<uint32_t(*)[16]>(dq));
+      tmem_ld16(tmem + lane_addr + kColdQ + 16, *reinterpret_cast<uint32_t(*)[16]>(dq + 16));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(bAccFree));
+      if (e < n && src >= 0) {
+        const Item x = decode_item(g, L + it);
+        const int64_t off = ((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * 32;
+        uint4 *pv = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) + off);
+        uint4 *pk = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dk) + off);
+        uint4 *pq = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) + off);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t wv[4], wk[4], wq[4];
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int j = 8 * c + 2 * t;
+            wv[t] = pack_bf16(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1]));
+            wk[t] = pack_bf16(__uint_as_float(dk[j]) * a.scale, __uint_as_float(dk[j + 1]) * a.scale);
+            wq[t] = pack_bf16(__uint_as_float(dq[j]) * a.scale, __uint_as_float(dq[j + 1]) * a.scale);
+          }
+          pv[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          pk[c] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
+          pq[c] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+        }
+      }
+    }
+    tmem_wait_ld();
+  } else {
+    // ----------------------------------------------------------- softmax ---
+    const int q4 = warp & 3, i = q4 * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + kColS, tdP = tmem + lane_addr + kColdP, tAcc = tmem + lane_addr + kColAcc;
+    float *brow = reinterpret_cast<float *>(smem + kBias) + i * kBiasStride;
+    const float cs = a.scale * kLog2e;
+    const float2 cs2 = make_float2(cs, cs);
+    const bool want_db = a.ws != nullptr;
+    int wc0[3] = {0, 0, 0};
+    const SlotRoute ri = slot_route(g, wc0, i < n ? i : 0);
+    int cur_h = -1, h_first = -1;
+    uint32_t wsync_phase = 0;
+    bool ok = true;
+    if (a.debug_force_timeout) ok = mbar_wait_warp(bar(bNever), 0, ctl);
+    // Fold the slot-pair dBias accumulator into bias rows (fixed order) and
+    // write workspace slot `slot`.
+    auto flush = [&](int slot) -> bool {
+      for (int gi = 0; gi < 8; ++gi) {
+        uint32_t av[16];
+        tmem_ld16(tAcc + 16u * gi, av);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) brow[16 * gi + e] = __uint_as_float(av[e]);
+      }
+      mbar_arrive(bar(bWsync));
+      if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) return false;
+      ++wsync_phase;
+      const float *acc = reinterpret_cast<const float *>(smem + kBias);
+      for (int t = i; t < g.T; t += 128) {
+        int dlt[3], rem = t;
+        for (int d = 0; d < 3; ++d) {
+          dlt[d] = rem / g.rstride[d] - (g.w[d] - 1);
+          rem %= g.rstride[d];
+        }
+        float sum = 0.f;
+        for (int i0 = max(0, dlt[0]); i0 < min(g.w[0], g.w[0] + dlt[0]); ++i0)
+          for (int i1 = max(0, dlt[1]); i1 < min(g.w[1], g.w[1] + dlt[1]); ++i1)
+            for (int i2 = max(0, dlt[2]); i2 < min(g.w[2], g.w[2] + dlt[2]); ++i2) {
+              const int qi = (i0 * g.w[1] + i1) * g.w[2] + i2;
+              const int kj = ((i0 - dlt[0]) * g.w[1] + (i1 - dlt[1])) * g.w[2] + (i2 - dlt[2]);
+              sum += acc[qi * kBiasStride + kj];
+            }
+        a.ws[(int64_t)slot * g.T + t] = sum;
+      }
+      mbar_arrive(bar(bWsync));
+      if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) return false;
+      ++wsync_phase;
+      return true;
+    };
+    for (int64_t it = 0; ok && it < count; ++it) {
+      const Item x = decode_item(g, L + it);
+      if (x.h != cur_h) {
+        if (cur_h >= 0 && want_db && !flush(a.slot_base[blockIdx.x] + (cur_h - h_first))) break;
+        for (int j = 0; j < 128; ++j) {
+          float b = 0.f;
+          if (i < n && j < n && a.bias)
+            b = a.bias[(int64_t)(ri.rbase - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
+          brow[j] = b;
+        }
+        if (want_db) {
+          uint32_t z[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) z[e] = 0u;
+          for (int gi = 0; gi < 8; ++gi) tmem_st16(tAcc + 16u * gi, z);
+          tmem_wait_st();
+        }
+        if (h_first < 0) h_first = x.h;
+        cur_h = x.h;
+      }
+      const int s = (int)(it % kStages);
+      if (!mbar_wait_warp(bar(bSpFull), (uint32_t)it & 1u, ctl)) break;
+      tc_fence_after();
+      if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
+      const uint8_t *sp = smem + s * kStageBytes;
+      const float lse2 = reinterpret_cast<const float *>(sp + kMeta + 512)[i];
+      const bool live = (sp + kMeta + 1024)[i] != 0;
+      // pass 1: P = exp2(S*cs + bias2 - lse2); delta = sum_j P dP; P (fp32) back to TMEM, P (bf16) to smem
+      float delta = 0.f;
+      const float2 nl2 = make_float2(-lse2, -lse2);
+      for (int gi = 0; gi < NG; ++gi) {
+        uint32_t sv[16], dpv[16], pv[16], pb[8];
+        tmem_ld16(tS + 16u * gi, sv);
+        tmem_ld16(tdP + 16u * gi, dpv);
+        float bv[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4 *>(bv + e) = *reinterpret_cast<const float4 *>(brow + 16 * gi + e);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
+                                 make_float2(bv[e], bv[e + 1]));
+          xs = __fadd2_rn(xs, nl2);
+          float p0 = live ? ex2(xs.x) : 0.f, p1 = live ? ex2(xs.y) : 0.f;
+          delta = fmaf(p0, __uint_as_float(dpv[e]), delta);
+          delta = fmaf(p1, __uint_as_float(dpv[e + 1]), delta);
+          pv[e] = __float_as_uint(p0);
+          pv[e + 1] = __float_as_uint(p1);
+          pb[e >> 1] = pack_bf16(p0, p1);
+        }
+        tmem_st16(tS + 16u * gi, pv);
+        *reinterpret_cast<uint4 *>(smem + kP + pds_chunk(i, 2 * gi)) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+        *reinterpret_cast<uint4 *>(smem + kP + pds_chunk(i, 2 * gi + 1)) = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(bPFull));
+      if (it >= 1 && !mbar_wait_warp(bar(bDsFree), (uint32_t)(it - 1) & 1u, ctl)) break;
+      // pass 2: dS = P (dP - delta); dS (bf16) to smem; dBias accumulator += dS
+      const float2 nd2 = make_float2(-delta, -delta);
+      for (int gi = 0; gi < NG; ++gi) {
+        uint32_t pv[16], dpv[16], av[16], db[8];
+        tmem_ld16(tS + 16u * gi, pv);
+        tmem_ld16(tdP + 16u * gi, dpv);
+        if (want_db) tmem_ld16(tAcc + 16u * gi, av);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const float2 p = make_float2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1]));
+          const float2 d = __fadd2_rn(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd2);
+          const float2 ds = __fmul2_rn(p, d);
+          db[e >> 1] = pack_bf16(ds.x, ds.y);
+          if (want_db) {
+            const float2 acc = __fadd2_rn(make_float2(__uint_as_float(av[e]), __uint_as_float(av[e + 1])), ds);
+            av[e] = __float_as_uint(acc.x);
+            av[e + 1] = __float_as_uint(acc.y);
+          }
+        }
+        if (want_db) tmem_st16(tAcc + 16u * gi, av);
+        *reinterpret_cast<uint4 *>(smem + kdS + pds_chunk(i, 2 * gi)) = make_uint4(db[0], db[1], db[2], db[3]);
+        *reinterpret_cast<uint4 *>(smem + kdS + pds_chunk(i, 2 * gi + 1)) = make_uint4(db[4], db[5], db[6], db[7]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(bDsFull));
+    }
+    if (ok && !*abort_flag && cur_h >= 0 && want_db) flush(a.slot_base[blockIdx.x] + (cur_h - h_first));
+    tmem_wait_st();
+    tmem_wait_ld();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace bwd
 }  // namespace
 
 bool tc_supported(const Geo &g, int dtype) { return dtype == SWIN_BF16 && g.hd == 32 && g.n <= 128; }
@@ -351,6 +739,12 @@ int launch_fwd_tc(const FwdArgs &a, void *stream) {
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
 }
 
-int launch_bwd_tc(const BwdArgs &a, void *stream) { return launch_bwd_simt(a, SWIN_BF16, stream); }
+int launch_bwd_tc(const BwdArgs &a, void *stream) {
+  auto kern = bwd::bwd_tc_kernel;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmemBytes) != cudaSuccess)
+    return SWIN_ERR_CUDA;
+  kern<<<a.ctas, bwd::kThreads, bwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
+  return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
+}
 
 }  // namespace swin
