@@ -117,10 +117,21 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    int64_t issued = 0;
+    // Copies of `pending` are in flight but not yet announced on full[]; they
+    // are announced after the next item is issued (two items in flight), or
+    // before this thread blocks on an empty stage (so no wait cycle forms).
+    int64_t pending = -1;
     for (int64_t it = 0; it < count; ++it) {
       const int s = (int)(it % kStages);
-      if (it >= kStages && !mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      if (it >= kStages) {
+        if (pending >= 0) {
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          mbar_arrive(bar(bFull + (int)(pending % kStages)));
+          pending = -1;
+        }
+        if (!mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      }
       const Item x = decode_item(g, L + it);
       int wc[3];
       window_coords(g, x.omega, wc);
@@ -156,17 +167,17 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? r.src : -1;
       (sp + kMeta + 512)[pt] = live ? 1 : 0;
       cp_async_commit();
-      if (it > 0) {
+      if (pending >= 0) {
         cp_async_wait<1>();
         fence_proxy_async_smem();
-        mbar_arrive(bar(bFull + (int)((it - 1) % kStages)));
+        mbar_arrive(bar(bFull + (int)(pending % kStages)));
       }
-      issued = it + 1;
+      pending = it;
     }
     cp_async_wait_all();
-    if (issued > 0 && !*abort_flag) {
+    if (pending >= 0 && !*abort_flag) {
       fence_proxy_async_smem();
-      mbar_arrive(bar(bFull + (int)((issued - 1) % kStages)));
+      mbar_arrive(bar(bFull + (int)(pending % kStages)));
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
@@ -426,10 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
     const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
-    int64_t issued = 0;
+    // Copies of `pending` are in flight but not yet announced on full[]; they
+    // are announced after the next item is issued (two items in flight), or
+    // before this thread blocks on an empty stage (so no wait cycle forms).
+    int64_t pending = -1;
     for (int64_t it = 0; it < count; ++it) {
       const int s = (int)(it % kStages);
-      if (it >= kStages && !mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      if (it >= kStages) {
+        if (pending >= 0) {
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          mbar_arrive(bar(bFull + (int)(pending % kStages)));
+          pending = -1;
+        }
+        if (!mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      }
       const Item x = decode_item(g, L + it);
       int wc[3];
       window_coords(g, x.omega, wc);
@@ -468,17 +490,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       reinterpret_cast<float *>(sp + kMeta + 512)[pt] = lse * kLog2e;
       (sp + kMeta + 1024)[pt] = live ? 1 : 0;
       cp_async_commit();
-      if (it > 0) {
+      if (pending >= 0) {
         cp_async_wait<1>();
         fence_proxy_async_smem();
-        mbar_arrive(bar(bFull + (int)((it - 1) % kStages)));
+        mbar_arrive(bar(bFull + (int)(pending % kStages)));
       }
-      issued = it + 1;
+      pending = it;
     }
     cp_async_wait_all();
-    if (issued > 0 && !*abort_flag) {
+    if (pending >= 0 && !*abort_flag) {
       fence_proxy_async_smem();
-      mbar_arrive(bar(bFull + (int)((issued - 1) % kStages)));
+      mbar_arrive(bar(bFull + (int)(pending % kStages)));
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
