@@ -145,6 +145,28 @@ int swin_attn_bwd(swin_attn_plan_t plan, const void *q, const void *k, const voi
                   const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,
                   void *workspace, size_t workspace_bytes, swin_stream_t stream);
 
+/* Backward for callers that cannot allocate device memory. No counterpart on
+ * the pages: it exists for callers whose host code has no device allocator
+ * of its own (for example a C or Fortran model that only receives tensors),
+ * or whose device memory all belongs to a pool they may not touch while
+ * stepping, and who therefore cannot provide swin_attn_bwd's workspace.
+ * Same arguments, results and errors as swin_attn_bwd without the
+ * workspace: the partial dBias tables go to a fixed device array inside this
+ * library (SWIN_NOALLOC_MAX_WORKSPACE_BYTES, held on every GPU that loads the
+ * library until the process exits). Nothing is allocated by any call.
+ *  - Plans whose swin_attn_workspace_bytes() exceeds the array are rejected
+ *    with SWIN_ERR_WORKSPACE (nothing is launched).
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the one array: calls that can overlap on the GPU (other
+ *    streams, other threads) race on it; serialise them.
+ * Errors: those of swin_attn_bwd, WORKSPACE as above, CUDA. */
+#define SWIN_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)4 << 20)
+int swin_attn_bwd_noalloc(swin_attn_plan_t plan, const void *q, const void *k, const void *v,
+                          const void *dout, const float *lse, const float *bias,
+                          const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,
+                          swin_stream_t stream);
+
 /* Testing hook for the failure path of the tensor-core kernels. Every wait
  * inside those kernels gives up after `wait_limit_ns` (default 1 s) and then
  * records SWIN_ERR_TIMEOUT in the status word. force_timeout = 1 makes one

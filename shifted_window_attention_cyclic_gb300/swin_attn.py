@@ -82,6 +82,8 @@ def load_library():
     lib.swin_attn_fwd.restype = ctypes.c_int
     lib.swin_attn_bwd.argtypes = [vp] * 13 + [sz, vp]
     lib.swin_attn_bwd.restype = ctypes.c_int
+    lib.swin_attn_bwd_noalloc.argtypes = [vp] * 13
+    lib.swin_attn_bwd_noalloc.restype = ctypes.c_int
     lib.swin_attn_plan_set_debug.argtypes = [vp, ctypes.c_uint64, ctypes.c_int]
     lib.swin_attn_plan_set_debug.restype = ctypes.c_int
     lib.swin_attn_status.argtypes = [vp, vp]
@@ -209,6 +211,14 @@ def swin_attn_bwd(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv, dbias,
     _check(load_library().swin_attn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(bias),
                                         _ptr(land), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
                                         ws_bytes, _stream(stream)), "swin_attn_bwd")
+
+
+def swin_attn_bwd_noalloc(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv, dbias, stream=None) -> None:
+    """Backward without a workspace argument: the partial dBias tables live in
+    a fixed array inside the library, so the call allocates nothing."""
+    _check(load_library().swin_attn_bwd_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse),
+                                                _ptr(bias), _ptr(land), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+                                                _stream(stream)), "swin_attn_bwd_noalloc")
 
 
 def swin_attn_status(plan: Plan, stream=None) -> int:
