@@ -69,6 +69,10 @@ WORKLOADS = {
     "eddy_ocean": Workload("eddy_ocean", 3, "bf16", 1, (256, 540), (8, 12), (4, 6), (0, 1), 16, 32, (0.3, 0.3), True),
     "depth3d": Workload("depth3d", 4, "bf16", 1, (16, 192, 384), (2, 8, 8), (1, 4, 4), (0, 0, 1), 8, 32,
                         (0.3, 0.6), True),
+    # half of depth3d (8 levels, same window/shift/land recipe): the profiling
+    # case for ncu captures, still larger than L2 (302 MB per tensor)
+    "depth3d_8lvl": Workload("depth3d_8lvl", 5, "bf16", 1, (8, 192, 384), (2, 8, 8), (1, 4, 4), (0, 0, 1), 8, 32,
+                             (0.3, 0.6), True),
 }
 
 
