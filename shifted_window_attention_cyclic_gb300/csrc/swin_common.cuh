@@ -86,6 +86,72 @@ __host__ __device__ __forceinline__ Item decode_item(const Geo &g, int64_t it) {
   return x;
 }
 
+// Sequential walk over work items in head-major order, one step per item,
+// without divisions (a CTA's items are a contiguous range).
+struct ItemCursor {
+  int h, b, omega, wc[3];
+  __host__ __device__ __forceinline__ void init(const Geo &g, int64_t it) {
+    const Item x = decode_item(g, it);
+    h = x.h;
+    b = x.b;
+    omega = x.omega;
+    window_coords(g, omega, wc);
+  }
+  __host__ __device__ __forceinline__ void next(const Geo &g) {
+    if (++wc[2] == g.nw[2]) {
+      wc[2] = 0;
+      if (++wc[1] == g.nw[1]) {
+        wc[1] = 0;
+        ++wc[0];
+      }
+    }
+    if (++omega == g.nwin) {
+      omega = 0;
+      wc[0] = wc[1] = wc[2] = 0;
+      if (++b == g.batch) {
+        b = 0;
+        ++h;
+      }
+    }
+  }
+};
+
+// In-window coordinates of one slot, computed once per thread.
+struct SlotCoord {
+  int sc[3];
+};
+
+__host__ __device__ __forceinline__ SlotCoord slot_coord(const Geo &g, int sigma) {
+  SlotCoord c;
+  c.sc[2] = sigma % g.w[2];
+  const int t = sigma / g.w[2];
+  c.sc[1] = t % g.w[1];
+  c.sc[0] = t / g.w[1];
+  return c;
+}
+
+// slot_route() for a slot whose coordinates are already known (no divisions).
+__host__ __device__ __forceinline__ SlotRoute route_slot(const Geo &g, const int wc[3], const SlotCoord &c) {
+  SlotRoute r;
+  r.rbase = 0;
+  r.roff = 0;
+  int src = 0, reg = 0;
+  bool pad = false;
+  for (int a = 0; a < 3; ++a) {
+    const int p = wc[a] * g.w[a] + c.sc[a];
+    pad |= p >= g.G[a];
+    int u = p + g.s[a];
+    if (u >= g.G[a]) u -= g.G[a];
+    src = src * g.G[a] + u;
+    if (!g.per[a] && g.s[a] > 0 && p >= g.G[a] - g.s[a]) reg |= 1 << (a - g.lead);
+    r.rbase += (c.sc[a] + g.w[a] - 1) * g.rstride[a];
+    r.roff += c.sc[a] * g.rstride[a];
+  }
+  r.src = pad ? -1 : src;
+  r.reg = pad ? 0 : reg;
+  return r;
+}
+
 // TERRA Eq. (4): contiguous range of CTA r among P over M items.
 __host__ __device__ __forceinline__ void eq4_range(int64_t M, int64_t P, int64_t r, int64_t &L, int64_t &R) {
   L = (r * M) / P;

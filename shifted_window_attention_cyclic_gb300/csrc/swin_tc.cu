@@ -44,6 +44,29 @@ __device__ __forceinline__ uint32_t sw32(int r, int c) { return r * 32 + ((c ^ (
 
 __device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
 
+// What a gather thread knows about its slot of one item before the copies.
+struct SlotPrep {
+  int h, src, reg;
+  int64_t tok;
+  uint8_t land;
+  float lse;
+};
+
+// Mask rows of one slot: Qm = one-hot of the query's region bits (live
+// queries only); Km = 0 in the column of the key's region if the key is live,
+// -2^100 everywhere else. Qm Km^T then adds -2^100 to every masked logit.
+__device__ __forceinline__ void build_mask_rows(bool live, int reg, uint32_t (&qm)[8], uint32_t (&km)[8]) {
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t lo = (live && reg == 2 * w) ? 0u : kBf16NegBig;
+    const uint32_t hi = (live && reg == 2 * w + 1) ? 0u : kBf16NegBig;
+    km[w] = lo | (hi << 16);
+    const uint32_t qlo = (live && reg == 2 * w) ? kBf16One : 0u;
+    const uint32_t qhi = (live && reg == 2 * w + 1) ? kBf16One : 0u;
+    qm[w] = qlo | (qhi << 16);
+  }
+}
+
 // ---------------------------------------------------------------- forward ---
 namespace fwd {
 
@@ -120,9 +143,28 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     // Copies of `pending` are in flight but not yet announced on full[]; they
     // are announced after the next item is issued (two items in flight), or
     // before this thread blocks on an empty stage (so no wait cycle forms).
+    // The per-slot land byte of the next item is loaded one item ahead.
+    const SlotCoord scoord = slot_coord(g, pt < n ? pt : 0);
+    auto prep = [&](const ItemCursor &c, SlotPrep &p) {
+      const SlotRoute r = (pt < n) ? route_slot(g, c.wc, scoord) : SlotRoute{-1, 0, 0, 0};
+      p.h = c.h;
+      p.src = r.src;
+      p.reg = r.reg;
+      p.tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
+      p.land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p.tok) : (uint8_t)0;
+    };
+    ItemCursor cur;
+    SlotPrep pc, pn;
+    if (count > 0) {
+      cur.init(g, L);
+      prep(cur, pc);
+    }
     int64_t pending = -1;
     for (int64_t it = 0; it < count; ++it) {
       const int s = (int)(it % kStages);
+      ItemCursor nx = cur;
+      nx.next(g);
+      if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         if (pending >= 0) {
           cp_async_wait<0>();
@@ -132,15 +174,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         }
         if (!mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
       }
-      const Item x = decode_item(g, L + it);
-      int wc[3];
-      window_coords(g, x.omega, wc);
-      SlotRoute r = {-1, 0, 0, 0};
-      if (pt < n) r = slot_route(g, wc, pt);
-      const bool valid = r.src >= 0;
-      const int64_t tok = (int64_t)x.b * g.tokens + (valid ? r.src : 0);
-      const bool live = valid && !(g.has_land && a.land[tok]);
-      const int64_t off = tok * g.C + (int64_t)x.h * 32;
+      const bool valid = pc.src >= 0;
+      const bool live = valid && !pc.land;
+      const int64_t off = pc.tok * g.C + (int64_t)pc.h * 32;
       const uint32_t nb = valid ? 16u : 0u;
       const uint32_t st = sbase + s * kStageBytes;
 #pragma unroll
@@ -150,21 +186,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         cp_async16(st + kV + sw64(pt, c), v + off + 8 * c, nb);
       }
       uint32_t qm[8], km[8];
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const uint32_t lo = (live && r.reg == 2 * w) ? 0u : kBf16NegBig;
-        const uint32_t hi = (live && r.reg == 2 * w + 1) ? 0u : kBf16NegBig;
-        km[w] = lo | (hi << 16);
-        const uint32_t qlo = (live && r.reg == 2 * w) ? kBf16One : 0u;
-        const uint32_t qhi = (live && r.reg == 2 * w + 1) ? kBf16One : 0u;
-        qm[w] = qlo | (qhi << 16);
-      }
+      build_mask_rows(live, pc.reg, qm, km);
       uint8_t *sp = smem + s * kStageBytes;
       *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
       *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
       *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
       *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
-      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? r.src : -1;
+      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? pc.src : -1;
       (sp + kMeta + 512)[pt] = live ? 1 : 0;
       cp_async_commit();
       if (pending >= 0) {
@@ -173,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         mbar_arrive(bar(bFull + (int)(pending % kStages)));
       }
       pending = it;
+      cur = nx;
+      pc = pn;
     }
     cp_async_wait_all();
     if (pending >= 0 && !*abort_flag) {
@@ -237,8 +267,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     uint32_t hc = 0;
     bool ok = true;
     if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
-    for (int64_t it = 0; ok && it < count; ++it) {
-      const Item x = decode_item(g, L + it);
+    ItemCursor x;
+    if (count > 0) x.init(g, L);
+    for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
       if (x.h != cur_h) {
         // head change: both warpgroups finished the previous head's items;
         // each writes half of the bias tile (columns 64*grp .. +63) of its lane.
@@ -437,12 +468,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
     const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
-    // Copies of `pending` are in flight but not yet announced on full[]; they
-    // are announced after the next item is issued (two items in flight), or
-    // before this thread blocks on an empty stage (so no wait cycle forms).
+    // Same gather as the forward plus dO rows and each slot's saved LSE;
+    // the land byte and the LSE of the next item are loaded one item ahead.
+    const SlotCoord scoord = slot_coord(g, pt < n ? pt : 0);
+    auto prep = [&](const ItemCursor &c, SlotPrep &p) {
+      const SlotRoute r = (pt < n) ? route_slot(g, c.wc, scoord) : SlotRoute{-1, 0, 0, 0};
+      p.h = c.h;
+      p.src = r.src;
+      p.reg = r.reg;
+      p.tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
+      p.land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p.tok) : (uint8_t)0;
+      p.lse = (r.src >= 0) ? __ldg(a.lse + ((int64_t)c.b * g.heads + c.h) * g.tokens + r.src) : 0.f;
+    };
+    ItemCursor cur;
+    SlotPrep pc, pn;
+    if (count > 0) {
+      cur.init(g, L);
+      prep(cur, pc);
+    }
     int64_t pending = -1;
     for (int64_t it = 0; it < count; ++it) {
       const int s = (int)(it % kStages);
+      ItemCursor nx = cur;
+      nx.next(g);
+      if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         if (pending >= 0) {
           cp_async_wait<0>();
@@ -452,15 +501,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
         }
         if (!mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
       }
-      const Item x = decode_item(g, L + it);
-      int wc[3];
-      window_coords(g, x.omega, wc);
-      SlotRoute r = {-1, 0, 0, 0};
-      if (pt < n) r = slot_route(g, wc, pt);
-      const bool valid = r.src >= 0;
-      const int64_t tok = (int64_t)x.b * g.tokens + (valid ? r.src : 0);
-      const bool live = valid && !(g.has_land && a.land[tok]);
-      const int64_t off = tok * g.C + (int64_t)x.h * 32;
+      const bool valid = pc.src >= 0;
+      const bool live = valid && !pc.land;
+      const int64_t off = pc.tok * g.C + (int64_t)pc.h * 32;
       const uint32_t nb = valid ? 16u : 0u;
       const uint32_t st = sbase + s * kStageBytes;
 #pragma unroll
@@ -471,23 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
         cp_async16(st + kdO + sw64(pt, c), dout + off + 8 * c, nb);
       }
       uint32_t qm[8], km[8];
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        const uint32_t lo = (live && r.reg == 2 * w) ? 0u : kBf16NegBig;
-        const uint32_t hi = (live && r.reg == 2 * w + 1) ? 0u : kBf16NegBig;
-        km[w] = lo | (hi << 16);
-        const uint32_t qlo = (live && r.reg == 2 * w) ? kBf16One : 0u;
-        const uint32_t qhi = (live && r.reg == 2 * w + 1) ? kBf16One : 0u;
-        qm[w] = qlo | (qhi << 16);
-      }
+      build_mask_rows(live, pc.reg, qm, km);
       uint8_t *sp = smem + s * kStageBytes;
       *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
       *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
       *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
       *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
-      const float lse = live ? a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + r.src] : 0.f;
-      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? r.src : -1;
-      reinterpret_cast<float *>(sp + kMeta + 512)[pt] = lse * kLog2e;
+      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? pc.src : -1;
+      reinterpret_cast<float *>(sp + kMeta + 512)[pt] = live ? pc.lse * kLog2e : 0.f;
       (sp + kMeta + 1024)[pt] = live ? 1 : 0;
       cp_async_commit();
       if (pending >= 0) {
@@ -496,6 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
         mbar_arrive(bar(bFull + (int)(pending % kStages)));
       }
       pending = it;
+      cur = nx;
+      pc = pn;
     }
     cp_async_wait_all();
     if (pending >= 0 && !*abort_flag) {
@@ -557,7 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     // ---------------------------------------------------------- epilogue ---
     const int q4 = warp & 3, e = q4 * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-    for (int64_t it = 0; it < count; ++it) {
+    ItemCursor x;
+    if (count > 0) x.init(g, L);
+    for (int64_t it = 0; it < count; ++it, x.next(g)) {
       const int s = (int)(it % kStages);
       if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
       const int src = reinterpret_cast<const int *>(smem + s * kStageBytes + kMeta)[e];
@@ -575,7 +613,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       tc_fence_before();
       mbar_arrive(bar(bAccFree));
       if (e < n && src >= 0) {
-        const Item x = decode_item(g, L + it);
         const int64_t off = ((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * 32;
         uint4 *pv = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) + off);
         uint4 *pk = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dk) + off);
@@ -647,8 +684,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       ++wsync_phase;
       return true;
     };
-    for (int64_t it = 0; ok && it < count; ++it) {
-      const Item x = decode_item(g, L + it);
+    ItemCursor x;
+    if (count > 0) x.init(g, L);
+    for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
       if (x.h != cur_h) {
         if (cur_h >= 0 && want_db && !flush(a.slot_base[blockIdx.x] + (cur_h - h_first))) break;
         for (int j = 0; j < 128; ++j) {
