@@ -71,6 +71,7 @@ __device__ __forceinline__ void build_mask_rows(bool live, int reg, uint32_t (&q
 namespace fwd {
 
 constexpr int kStages = 4;
+constexpr int kAhead = kStages - 2;  // items whose copies stay in flight unannounced
 constexpr int kTileBytes = 128 * 64;  // 128 slot rows x 32 bf16
 constexpr int kMaskBytes = 128 * 32;  // 128 rows x 16 bf16
 constexpr int kQ = 0, kK = kTileBytes, kV = 2 * kTileBytes, kQm = 3 * kTileBytes, kKm = kQm + kMaskBytes;
@@ -166,13 +167,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       nx.next(g);
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
-        if (pending >= 0) {
+        const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
+        if (!mbar_try_wait(bar(bEmpty + s), par)) {
+          // about to block: announce everything still pending first
           cp_async_wait<0>();
           fence_proxy_async_smem();
-          mbar_arrive(bar(bFull + (int)(pending % kStages)));
+          for (; pending >= 0 && pending < it; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
           pending = -1;
+          if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
         }
-        if (!mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
       }
       const bool valid = pc.src >= 0;
       const bool live = valid && !pc.land;
@@ -195,19 +198,20 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? pc.src : -1;
       (sp + kMeta + 512)[pt] = live ? 1 : 0;
       cp_async_commit();
-      if (pending >= 0) {
-        cp_async_wait<1>();
+      if (pending < 0) pending = it;
+      if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
+        cp_async_wait<kAhead>();
         fence_proxy_async_smem();
         mbar_arrive(bar(bFull + (int)(pending % kStages)));
+        ++pending;
       }
-      pending = it;
       cur = nx;
       pc = pn;
     }
     cp_async_wait_all();
     if (pending >= 0 && !*abort_flag) {
       fence_proxy_async_smem();
-      mbar_arrive(bar(bFull + (int)(pending % kStages)));
+      for (; pending < count; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
@@ -307,28 +311,44 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       const uint8_t *sp = smem + s * kStageBytes;
       const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
       const bool live = (sp + kMeta + 512)[i] != 0;
-      // pass 1: row max of x = S*cs + bias
+      // pass 1: row max of x = S*cs + bias. TMEM loads of group gi+1 are in
+      // flight while group gi is computed (two register buffers).
       float m = -INFINITY;
-      for (int gi = 0; gi < NG; ++gi) {
-        uint32_t sv[16], bv[16];
-        tmem_ld16(tS + 16u * gi, sv);
-        tmem_ld16(tB + 16u * gi, bv);
-        tmem_wait_ld();
+      auto max_group = [&](uint32_t (&sv)[16], uint32_t (&bv)[16]) {
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           const float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
                                        make_float2(__uint_as_float(bv[e]), __uint_as_float(bv[e + 1])));
           m = max3(m, xs.x, xs.y);
         }
+      };
+      uint32_t s0[16], b0[16], s1[16], b1[16];
+      tmem_ld16(tS, s0);
+      tmem_ld16(tB, b0);
+#pragma unroll
+      for (int gi = 0; gi < 8; gi += 2) {
+        if (gi < NG) {
+          tmem_wait_ld_tied(s0, b0);
+          if (gi + 1 < NG) {
+            tmem_ld16(tS + 16u * (gi + 1), s1);
+            tmem_ld16(tB + 16u * (gi + 1), b1);
+          }
+          max_group(s0, b0);
+        }
+        if (gi + 1 < NG) {
+          tmem_wait_ld_tied(s1, b1);
+          if (gi + 2 < NG) {
+            tmem_ld16(tS + 16u * (gi + 2), s0);
+            tmem_ld16(tB + 16u * (gi + 2), b0);
+          }
+          max_group(s1, b1);
+        }
       }
       // pass 2: p = exp2(x - m), row sum, P (bf16) written over S
       const float2 negm = make_float2(-m, -m);
       float2 sum2 = make_float2(0.f, 0.f);
-      for (int gi = 0; gi < NG; ++gi) {
-        uint32_t sv[16], bv[16], pv[8];
-        tmem_ld16(tS + 16u * gi, sv);
-        tmem_ld16(tB + 16u * gi, bv);
-        tmem_wait_ld();
+      auto exp_group = [&](int gi, uint32_t (&sv)[16], uint32_t (&bv)[16]) {
+        uint32_t pv[8];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
           float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
@@ -339,6 +359,27 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
           pv[e >> 1] = pack_bf16(p.x, p.y);
         }
         tmem_st8(tS + 8u * gi, pv);
+      };
+      tmem_ld16(tS, s0);
+      tmem_ld16(tB, b0);
+#pragma unroll
+      for (int gi = 0; gi < 8; gi += 2) {
+        if (gi < NG) {
+          tmem_wait_ld_tied(s0, b0);
+          if (gi + 1 < NG) {
+            tmem_ld16(tS + 16u * (gi + 1), s1);
+            tmem_ld16(tB + 16u * (gi + 1), b1);
+          }
+          exp_group(gi, s0, b0);
+        }
+        if (gi + 1 < NG) {
+          tmem_wait_ld_tied(s1, b1);
+          if (gi + 2 < NG) {
+            tmem_ld16(tS + 16u * (gi + 2), s0);
+            tmem_ld16(tB + 16u * (gi + 2), b0);
+          }
+          exp_group(gi + 1, s1, b1);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -393,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
 namespace bwd {
 
 constexpr int kStages = 2;
+constexpr int kAhead = 1;
 constexpr int kTile = 128 * 64, kMask = 128 * 32;
 constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kdO = 3 * kTile, kQm = 4 * kTile, kKm = kQm + kMask;
 constexpr int kMeta = kKm + kMask;  // int32 src[128] @0, float lse2[128] @512, uint8 live[128] @1024
@@ -404,11 +446,15 @@ constexpr int kBiasStride = 132;
 constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
 constexpr int bFull = 0, bEmpty = kStages, bSpFull = 2 * kStages, bPFull = bSpFull + 1, bDsFull = bPFull + 1,
               bAccFull = bDsFull + 1, bAccFree = bAccFull + 1, bDsFree = bAccFree + 1, bWsync = bDsFree + 1,
-              bNever = bWsync + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+              bDsync = bWsync + 1, bNever = bDsync + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
+constexpr int kDeltaOff = kMiscOff + 16;         // float [2][128]: the two halves of delta_i
+constexpr int kSmemBytes = kDeltaOff + 1024 + 1024;
 
-constexpr int kEpilogueWarp0 = 4, kProducerWarp0 = 8, kMmaWarp = 12;  // softmax warps 0-3
+// softmax warps 0-7: two warpgroups, each owning half of every row's columns
+// gather warps 12-14: 96 threads cover the 128 slot rows (threads 0-31 take two)
+constexpr int kSoftmaxThreads = 256, kEpilogueWarp0 = 8, kProducerWarp0 = 12, kMmaWarp = 15;
+constexpr int kProducerThreads = (kMmaWarp - kProducerWarp0) * 32;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColdP = 128, kColdV = 256, kColdK = 288, kColdQ = 320,
                    kColAcc = 384;
@@ -437,16 +483,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bFull + s), 128);
+      mbar_init(bar(bFull + s), kProducerThreads);
       mbar_init(bar(bEmpty + s), 1 + 128);
     }
     mbar_init(bar(bSpFull), 1);
-    mbar_init(bar(bPFull), 128);
-    mbar_init(bar(bDsFull), 128);
+    mbar_init(bar(bPFull), kSoftmaxThreads);
+    mbar_init(bar(bDsFull), kSoftmaxThreads);
     mbar_init(bar(bAccFull), 1);
     mbar_init(bar(bAccFree), 128);
     mbar_init(bar(bDsFree), 1);
-    mbar_init(bar(bWsync), 128);
+    mbar_init(bar(bWsync), kSoftmaxThreads);
+    mbar_init(bar(bDsync), kSoftmaxThreads);
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
@@ -470,18 +517,29 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
     // Same gather as the forward plus dO rows and each slot's saved LSE;
     // the land byte and the LSE of the next item are loaded one item ahead.
-    const SlotCoord scoord = slot_coord(g, pt < n ? pt : 0);
-    auto prep = [&](const ItemCursor &c, SlotPrep &p) {
-      const SlotRoute r = (pt < n) ? route_slot(g, c.wc, scoord) : SlotRoute{-1, 0, 0, 0};
-      p.h = c.h;
-      p.src = r.src;
-      p.reg = r.reg;
-      p.tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
-      p.land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p.tok) : (uint8_t)0;
-      p.lse = (r.src >= 0) ? __ldg(a.lse + ((int64_t)c.b * g.heads + c.h) * g.tokens + r.src) : 0.f;
+    constexpr int kRows = (128 + kProducerThreads - 1) / kProducerThreads;  // slot rows per thread
+    int rows[kRows];
+    SlotCoord scoord[kRows];
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) {
+      rows[rr] = pt + rr * kProducerThreads;
+      scoord[rr] = slot_coord(g, rows[rr] < n ? rows[rr] : 0);
+    }
+    auto prep = [&](const ItemCursor &c, SlotPrep (&p)[kRows]) {
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        const int row = rows[rr];
+        const SlotRoute r = (row < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
+        p[rr].h = c.h;
+        p[rr].src = r.src;
+        p[rr].reg = r.reg;
+        p[rr].tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
+        p[rr].land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p[rr].tok) : (uint8_t)0;
+        p[rr].lse = (r.src >= 0) ? __ldg(a.lse + ((int64_t)c.b * g.heads + c.h) * g.tokens + r.src) : 0.f;
+      }
     };
     ItemCursor cur;
-    SlotPrep pc, pn;
+    SlotPrep pc[kRows], pn[kRows];
     if (count > 0) {
       cur.init(g, L);
       prep(cur, pc);
@@ -493,50 +551,60 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       nx.next(g);
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
-        if (pending >= 0) {
+        const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
+        if (!mbar_try_wait(bar(bEmpty + s), par)) {
+          // about to block: announce everything still pending first
           cp_async_wait<0>();
           fence_proxy_async_smem();
-          mbar_arrive(bar(bFull + (int)(pending % kStages)));
+          for (; pending >= 0 && pending < it; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
           pending = -1;
+          if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
         }
-        if (!mbar_wait(bar(bEmpty + s), (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
       }
-      const bool valid = pc.src >= 0;
-      const bool live = valid && !pc.land;
-      const int64_t off = pc.tok * g.C + (int64_t)pc.h * 32;
-      const uint32_t nb = valid ? 16u : 0u;
       const uint32_t st = sbase + s * kStageBytes;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        cp_async16(st + kQ + sw64(pt, c), q + off + 8 * c, nb);
-        cp_async16(st + kK + sw64(pt, c), k + off + 8 * c, nb);
-        cp_async16(st + kV + sw64(pt, c), v + off + 8 * c, nb);
-        cp_async16(st + kdO + sw64(pt, c), dout + off + 8 * c, nb);
-      }
-      uint32_t qm[8], km[8];
-      build_mask_rows(live, pc.reg, qm, km);
       uint8_t *sp = smem + s * kStageBytes;
-      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
-      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
-      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
-      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
-      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? pc.src : -1;
-      reinterpret_cast<float *>(sp + kMeta + 512)[pt] = live ? pc.lse * kLog2e : 0.f;
-      (sp + kMeta + 1024)[pt] = live ? 1 : 0;
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        const int row = rows[rr];
+        if (row >= 128) continue;
+        const SlotPrep &q0 = pc[rr];
+        const bool valid = q0.src >= 0;
+        const bool live = valid && !q0.land;
+        const int64_t off = q0.tok * g.C + (int64_t)q0.h * 32;
+        const uint32_t nb = valid ? 16u : 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          cp_async16(st + kQ + sw64(row, c), q + off + 8 * c, nb);
+          cp_async16(st + kK + sw64(row, c), k + off + 8 * c, nb);
+          cp_async16(st + kV + sw64(row, c), v + off + 8 * c, nb);
+          cp_async16(st + kdO + sw64(row, c), dout + off + 8 * c, nb);
+        }
+        uint32_t qm[8], km[8];
+        build_mask_rows(live, q0.reg, qm, km);
+        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
+        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
+        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
+        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
+        reinterpret_cast<int *>(sp + kMeta)[row] = valid ? q0.src : -1;
+        reinterpret_cast<float *>(sp + kMeta + 512)[row] = live ? q0.lse * kLog2e : 0.f;
+        (sp + kMeta + 1024)[row] = live ? 1 : 0;
+      }
       cp_async_commit();
-      if (pending >= 0) {
-        cp_async_wait<1>();
+      if (pending < 0) pending = it;
+      if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
+        cp_async_wait<kAhead>();
         fence_proxy_async_smem();
         mbar_arrive(bar(bFull + (int)(pending % kStages)));
+        ++pending;
       }
-      pending = it;
       cur = nx;
-      pc = pn;
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) pc[rr] = pn[rr];
     }
     cp_async_wait_all();
     if (pending >= 0 && !*abort_flag) {
       fence_proxy_async_smem();
-      mbar_arrive(bar(bFull + (int)(pending % kStages)));
+      for (; pending < count; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
@@ -602,44 +670,43 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       mbar_arrive(bar(bEmpty + s));
       if (!mbar_wait_warp(bar(bAccFull), (uint32_t)it & 1u, ctl)) break;
       tc_fence_after();
-      uint32_t dv[32], dk[32], dq[32];
-      tmem_ld16(tmem + lane_addr + kColdV, *reinterpret_cast<uint32_t(*)[16]>(dv));
-      tmem_ld16(tmem + lane_addr + kColdV + 16, *reinterpret_cast<uint32_t(*)[16]>(dv + 16));
-      tmem_ld16(tmem + lane_addr + kColdK, *reinterpret_cast<uint32_t(*)[16]>(dk));
-      tmem_ld16(tmem + lane_addr + kColdK + 16, *reinterpret_cast<uint32_t(*)[16]>(dk + 16));
-      tmem_ld16(tmem + lane_addr + kColdQ, *reinterpret_cast<uint32_t(*)[16]>(dq));
-      tmem_ld16(tmem + lane_addr + kColdQ + 16, *reinterpret_cast<uint32_t(*)[16]>(dq + 16));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(bAccFree));
-      if (e < n && src >= 0) {
-        const int64_t off = ((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * 32;
-        uint4 *pv = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dv) + off);
-        uint4 *pk = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dk) + off);
-        uint4 *pq = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.dq) + off);
+      // one 32-column accumulator at a time: TMEM -> registers -> bf16 -> grid
+      const bool store = e < n && src >= 0;
+      const int64_t off = ((int64_t)x.b * g.tokens + (store ? src : 0)) * g.C + (int64_t)x.h * 32;
+      auto drain = [&](uint32_t col, void *base, float mul) {
+        uint32_t lo[16], hi[16];
+        tmem_ld16(tmem + lane_addr + col, lo);
+        tmem_ld16(tmem + lane_addr + col + 16, hi);
+        tmem_wait_ld_tied(lo, hi);
+        if (!store) return;
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(base) + off);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t wv[4], wk[4], wq[4];
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const int j = 8 * c + 2 * t;
-            wv[t] = pack_bf16(__uint_as_float(dv[j]), __uint_as_float(dv[j + 1]));
-            wk[t] = pack_bf16(__uint_as_float(dk[j]) * a.scale, __uint_as_float(dk[j + 1]) * a.scale);
-            wq[t] = pack_bf16(__uint_as_float(dq[j]) * a.scale, __uint_as_float(dq[j + 1]) * a.scale);
-          }
-          pv[c] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-          pk[c] = make_uint4(wk[0], wk[1], wk[2], wk[3]);
-          pq[c] = make_uint4(wq[0], wq[1], wq[2], wq[3]);
+          const uint32_t *src16 = c < 2 ? lo : hi;
+          const int o = (c & 1) * 8;
+          dst[c] = make_uint4(pack_bf16(__uint_as_float(src16[o + 0]) * mul, __uint_as_float(src16[o + 1]) * mul),
+                              pack_bf16(__uint_as_float(src16[o + 2]) * mul, __uint_as_float(src16[o + 3]) * mul),
+                              pack_bf16(__uint_as_float(src16[o + 4]) * mul, __uint_as_float(src16[o + 5]) * mul),
+                              pack_bf16(__uint_as_float(src16[o + 6]) * mul, __uint_as_float(src16[o + 7]) * mul));
         }
-      }
+      };
+      drain(kColdV, a.dv, 1.f);
+      drain(kColdK, a.dk, a.scale);
+      drain(kColdQ, a.dq, a.scale);
+      tc_fence_before();
+      mbar_arrive(bar(bAccFree));
     }
     tmem_wait_ld();
   } else {
     // ----------------------------------------------------------- softmax ---
-    const int q4 = warp & 3, i = q4 * 32 + lane;
+    // Warpgroup grp owns the 16-column groups [gb, ge) of every row; lane i
+    // of TMEM is query slot i. delta_i is the sum of the two halves (fixed order).
+    const int grp = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane, tid = grp * 128 + i;
+    const int ng0 = (NG + 1) >> 1, gb = grp ? ng0 : 0, ge = grp ? NG : ng0;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_addr + kColS, tdP = tmem + lane_addr + kColdP, tAcc = tmem + lane_addr + kColAcc;
     float *brow = reinterpret_cast<float *>(smem + kBias) + i * kBiasStride;
+    float *dpart = reinterpret_cast<float *>(smem + kDeltaOff);
     const float cs = a.scale * kLog2e;
     const float2 cs2 = make_float2(cs, cs);
     const bool want_db = a.ws != nullptr;
@@ -652,10 +719,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     // Fold the slot-pair dBias accumulator into bias rows (fixed order) and
     // write workspace slot `slot`.
     auto flush = [&](int slot) -> bool {
-      for (int gi = 0; gi < 8; ++gi) {
+      for (int gi = gb; gi < ge; ++gi) {
         uint32_t av[16];
         tmem_ld16(tAcc + 16u * gi, av);
-        tmem_wait_ld();
+        tmem_wait_ld_tied(av);
 #pragma unroll
         for (int e = 0; e < 16; ++e) brow[16 * gi + e] = __uint_as_float(av[e]);
       }
@@ -663,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) return false;
       ++wsync_phase;
       const float *acc = reinterpret_cast<const float *>(smem + kBias);
-      for (int t = i; t < g.T; t += 128) {
+      for (int t = tid; t < g.T; t += kSoftmaxThreads) {
         int dlt[3], rem = t;
         for (int d = 0; d < 3; ++d) {
           dlt[d] = rem / g.rstride[d] - (g.w[d] - 1);
@@ -689,7 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
       if (x.h != cur_h) {
         if (cur_h >= 0 && want_db && !flush(a.slot_base[blockIdx.x] + (cur_h - h_first))) break;
-        for (int j = 0; j < 128; ++j) {
+        for (int j = 16 * gb; j < 16 * ge; ++j) {
           float b = 0.f;
           if (i < n && j < n && a.bias)
             b = a.bias[(int64_t)(ri.rbase - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
@@ -699,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
           uint32_t z[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) z[e] = 0u;
-          for (int gi = 0; gi < 8; ++gi) tmem_st16(tAcc + 16u * gi, z);
+          for (int gi = gb; gi < ge; ++gi) tmem_st16(tAcc + 16u * gi, z);
           tmem_wait_st();
         }
         if (h_first < 0) h_first = x.h;
@@ -712,61 +779,116 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       const uint8_t *sp = smem + s * kStageBytes;
       const float lse2 = reinterpret_cast<const float *>(sp + kMeta + 512)[i];
       const bool live = (sp + kMeta + 1024)[i] != 0;
-      // pass 1: P = exp2(S*cs + bias2 - lse2); delta = sum_j P dP; P (fp32) back to TMEM, P (bf16) to smem
+      // pass 1: P = exp2(S*cs + bias2 - lse2); partial delta = sum_j P dP over
+      // this half; P (fp32) back over S in TMEM, P (bf16) to the smem tile.
       float delta = 0.f;
       const float2 nl2 = make_float2(-lse2, -lse2);
-      for (int gi = 0; gi < NG; ++gi) {
-        uint32_t sv[16], dpv[16], pv[16], pb[8];
-        tmem_ld16(tS + 16u * gi, sv);
-        tmem_ld16(tdP + 16u * gi, dpv);
-        float bv[16];
+      auto p_group = [&](int gi, uint32_t (&sv)[16], uint32_t (&dpv)[16]) {
+        uint32_t pb[8];
 #pragma unroll
-        for (int e = 0; e < 16; e += 4) *reinterpret_cast<float4 *>(bv + e) = *reinterpret_cast<const float4 *>(brow + 16 * gi + e);
-        tmem_wait_ld();
+        for (int e4 = 0; e4 < 16; e4 += 4) {
+          const float4 b4 = *reinterpret_cast<const float4 *>(brow + 16 * gi + e4);
+          const float bb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
-                                 make_float2(bv[e], bv[e + 1]));
-          xs = __fadd2_rn(xs, nl2);
-          float p0 = live ? ex2(xs.x) : 0.f, p1 = live ? ex2(xs.y) : 0.f;
-          delta = fmaf(p0, __uint_as_float(dpv[e]), delta);
-          delta = fmaf(p1, __uint_as_float(dpv[e + 1]), delta);
-          pv[e] = __float_as_uint(p0);
-          pv[e + 1] = __float_as_uint(p1);
-          pb[e >> 1] = pack_bf16(p0, p1);
+          for (int e = e4; e < e4 + 4; e += 2) {
+            float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
+                                   make_float2(bb[e - e4], bb[e - e4 + 1]));
+            xs = __fadd2_rn(xs, nl2);
+            const float p0 = live ? ex2(xs.x) : 0.f, p1 = live ? ex2(xs.y) : 0.f;
+            delta = fmaf(p0, __uint_as_float(dpv[e]), delta);
+            delta = fmaf(p1, __uint_as_float(dpv[e + 1]), delta);
+            sv[e] = __float_as_uint(p0);  // P (fp32) overwrites S in the register buffer
+            sv[e + 1] = __float_as_uint(p1);
+            pb[e >> 1] = pack_bf16(p0, p1);
+          }
         }
-        tmem_st16(tS + 16u * gi, pv);
+        tmem_st16(tS + 16u * gi, sv);
         *reinterpret_cast<uint4 *>(smem + kP + pds_chunk(i, 2 * gi)) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
         *reinterpret_cast<uint4 *>(smem + kP + pds_chunk(i, 2 * gi + 1)) = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+      };
+      {
+        uint32_t s0[16], d0[16], s1[16], d1[16];
+        tmem_ld16(tS + 16u * gb, s0);
+        tmem_ld16(tdP + 16u * gb, d0);
+#pragma unroll
+        for (int k2 = 0; k2 < 4; k2 += 2) {
+          const int g0 = gb + k2, g1 = gb + k2 + 1;
+          if (g0 < ge) {
+            tmem_wait_ld_tied(s0, d0);
+            if (g1 < ge) {
+              tmem_ld16(tS + 16u * g1, s1);
+              tmem_ld16(tdP + 16u * g1, d1);
+            }
+            p_group(g0, s0, d0);
+          }
+          if (g1 < ge) {
+            tmem_wait_ld_tied(s1, d1);
+            if (g1 + 1 < ge) {
+              tmem_ld16(tS + 16u * (g1 + 1), s0);
+              tmem_ld16(tdP + 16u * (g1 + 1), d0);
+            }
+            p_group(g1, s1, d1);
+          }
+        }
       }
+      dpart[grp * 128 + i] = delta;
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(bPFull));
+      mbar_arrive(bar(bDsync));
+      if (!mbar_wait_warp(bar(bDsync), (uint32_t)it & 1u, ctl)) break;
+      delta = dpart[i] + dpart[128 + i];
       if (it >= 1 && !mbar_wait_warp(bar(bDsFree), (uint32_t)(it - 1) & 1u, ctl)) break;
-      // pass 2: dS = P (dP - delta); dS (bf16) to smem; dBias accumulator += dS
+      tc_fence_after();
+      // pass 2: dS = P (dP - delta); dS (bf16) to the smem tile; dBias
+      // slot-pair accumulator += dS.
       const float2 nd2 = make_float2(-delta, -delta);
-      for (int gi = 0; gi < NG; ++gi) {
-        uint32_t pv[16], dpv[16], av[16], db[8];
-        tmem_ld16(tS + 16u * gi, pv);
-        tmem_ld16(tdP + 16u * gi, dpv);
-        if (want_db) tmem_ld16(tAcc + 16u * gi, av);
-        tmem_wait_ld();
+      // 8-column sub-groups (one 16-byte dS chunk each) keep the double
+      // buffers of P, dP and the accumulator within the register budget.
+      auto ds_sub = [&](int sg, uint32_t (&pv)[8], uint32_t (&dpv)[8], uint32_t (&av)[8]) {
+        uint32_t db[4];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
+        for (int e = 0; e < 8; e += 2) {
           const float2 p = make_float2(__uint_as_float(pv[e]), __uint_as_float(pv[e + 1]));
           const float2 d = __fadd2_rn(make_float2(__uint_as_float(dpv[e]), __uint_as_float(dpv[e + 1])), nd2);
           const float2 ds = __fmul2_rn(p, d);
           db[e >> 1] = pack_bf16(ds.x, ds.y);
+          const float2 acc = __fadd2_rn(make_float2(__uint_as_float(av[e]), __uint_as_float(av[e + 1])), ds);
+          av[e] = __float_as_uint(acc.x);
+          av[e + 1] = __float_as_uint(acc.y);
+        }
+        if (want_db) tmem_st8(tAcc + 8u * sg, av);
+        *reinterpret_cast<uint4 *>(smem + kdS + pds_chunk(i, sg)) = make_uint4(db[0], db[1], db[2], db[3]);
+      };
+      {
+        uint32_t p0[8], d0[8], a0[8], p1[8], d1[8], a1[8];
+        auto load3 = [&](int sg, uint32_t (&pv)[8], uint32_t (&dpv)[8], uint32_t (&av)[8]) {
+          tmem_ld8(tS + 8u * sg, pv);
+          tmem_ld8(tdP + 8u * sg, dpv);
           if (want_db) {
-            const float2 acc = __fadd2_rn(make_float2(__uint_as_float(av[e]), __uint_as_float(av[e + 1])), ds);
-            av[e] = __float_as_uint(acc.x);
-            av[e + 1] = __float_as_uint(acc.y);
+            tmem_ld8(tAcc + 8u * sg, av);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) av[e] = 0u;
+          }
+        };
+        const int sb = 2 * gb, se = 2 * ge;
+        load3(sb, p0, d0, a0);
+#pragma unroll
+        for (int k2 = 0; k2 < 8; k2 += 2) {
+          const int s0 = sb + k2, s1 = sb + k2 + 1;
+          if (s0 < se) {
+            tmem_wait_ld_tied(p0, d0, a0);
+            if (s1 < se) load3(s1, p1, d1, a1);
+            ds_sub(s0, p0, d0, a0);
+          }
+          if (s1 < se) {
+            tmem_wait_ld_tied(p1, d1, a1);
+            if (s1 + 1 < se) load3(s1 + 1, p0, d0, a0);
+            ds_sub(s1, p1, d1, a1);
           }
         }
-        if (want_db) tmem_st16(tAcc + 16u * gi, av);
-        *reinterpret_cast<uint4 *>(smem + kdS + pds_chunk(i, 2 * gi)) = make_uint4(db[0], db[1], db[2], db[3]);
-        *reinterpret_cast<uint4 *>(smem + kdS + pds_chunk(i, 2 * gi + 1)) = make_uint4(db[4], db[5], db[6], db[7]);
       }
       tmem_wait_st();
       fence_proxy_async_smem();
