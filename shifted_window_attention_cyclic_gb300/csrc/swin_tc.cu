@@ -72,24 +72,33 @@ namespace fwd {
 
 constexpr int kStages = 4;
 constexpr int kAhead = kStages - 2;  // items whose copies stay in flight unannounced
+// The MMA thread issues S(k) only after PV(k-2), so freeing stage s(it) (PV
+// of item it - kStages) needs items up to it - kStages + 2 announced; with
+// kAhead <= kStages - 2 the gather warps may block on empty[] while still
+// holding kAhead unannounced items.
+constexpr bool kFlushBeforeBlock = kAhead > kStages - 2;
 constexpr int kTileBytes = 128 * 64;  // 128 slot rows x 32 bf16
 constexpr int kMaskBytes = 128 * 32;  // 128 rows x 16 bf16
 constexpr int kQ = 0, kK = kTileBytes, kV = 2 * kTileBytes, kQm = 3 * kTileBytes, kKm = kQm + kMaskBytes;
 constexpr int kMeta = kKm + kMaskBytes;  // int32 src[128], uint8 live[128]
 constexpr int kStageBytes = kMeta + 1024;
-constexpr int kBarOff = kStages * kStageBytes;
+constexpr int kBias = kStages * kStageBytes;  // fp32 [128][kBiasStride]: bias*log2e of the current head
+constexpr int kBiasStride = 132;
+constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
 // barrier indices
 constexpr int bFull = 0, bEmpty = kStages, bSFull = 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
-              bTFree = bOFull + 2, bHcArrive = bTFree + 2, bHcDone = bHcArrive + 1, bNever = bHcDone + 1,
-              bDrain = bNever + 1, kNumBars = bDrain + 1;
+              bTFree = bOFull + 2, bMax = bTFree + 2, bNever = bMax + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
+constexpr int kXchg = kMiscOff + 16;  // float max[2 items][2 halves][128], sum[2 items][2 halves][128]
+constexpr int kSmemBytes = kXchg + 4096 + 1024;  // + alignment slack
 
-constexpr int kSoftmaxWarps = 8, kProducerWarps = 4;
-constexpr int kProducerWarp0 = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + kProducerWarps;
+// warps 0-7: two softmax warpgroups, each owning half of every row's columns;
+// 8-10: gather; 11: MMA
+constexpr int kSoftmaxWarps = 8, kProducerWarp0 = 8, kMmaWarp = 11;
+constexpr int kProducerThreads = (kMmaWarp - kProducerWarp0) * 32;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
-// TMEM columns
-constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256, kColBias = 384;
+// TMEM columns: S/P of warpgroup w at 128*w, O of warpgroup w at 256 + 32*w
+constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
 __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -110,17 +119,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bFull + s), kProducerWarps * 32);
+      mbar_init(bar(bFull + s), kProducerThreads);
       mbar_init(bar(bEmpty + s), 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(bSFull + w), 1);
-      mbar_init(bar(bPFull + w), 128);
+      mbar_init(bar(bPFull + w), kSoftmaxWarps * 32);
       mbar_init(bar(bOFull + w), 1);
-      mbar_init(bar(bTFree + w), 128);
+      mbar_init(bar(bTFree + w), kSoftmaxWarps * 32);
     }
-    mbar_init(bar(bHcArrive), kSoftmaxWarps * 32);
-    mbar_init(bar(bHcDone), kSoftmaxWarps * 32);
+    mbar_init(bar(bMax), kSoftmaxWarps * 32);
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
@@ -137,25 +145,35 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
 
   if (warp >= kProducerWarp0 && warp < kMmaWarp) {
     // ------------------------------------------------------------ gather ---
-    const int pt = threadIdx.x - kProducerWarp0 * 32;  // slot row 0..127
+    // Route every slot of the item (roll, ragged pad, region) and cp.async its
+    // Q, K, V rows into the stage; the land byte of the next item is loaded
+    // one item ahead. Copies of items [pending, it] are in flight unannounced.
+    const int pt = threadIdx.x - kProducerWarp0 * 32;
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    // Copies of `pending` are in flight but not yet announced on full[]; they
-    // are announced after the next item is issued (two items in flight), or
-    // before this thread blocks on an empty stage (so no wait cycle forms).
-    // The per-slot land byte of the next item is loaded one item ahead.
-    const SlotCoord scoord = slot_coord(g, pt < n ? pt : 0);
-    auto prep = [&](const ItemCursor &c, SlotPrep &p) {
-      const SlotRoute r = (pt < n) ? route_slot(g, c.wc, scoord) : SlotRoute{-1, 0, 0, 0};
-      p.h = c.h;
-      p.src = r.src;
-      p.reg = r.reg;
-      p.tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
-      p.land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p.tok) : (uint8_t)0;
+    constexpr int kRows = (128 + kProducerThreads - 1) / kProducerThreads;  // slot rows per thread
+    int rows[kRows];
+    SlotCoord scoord[kRows];
+#pragma unroll
+    for (int rr = 0; rr < kRows; ++rr) {
+      rows[rr] = pt + rr * kProducerThreads;
+      scoord[rr] = slot_coord(g, rows[rr] < n ? rows[rr] : 0);
+    }
+    auto prep = [&](const ItemCursor &c, SlotPrep (&p)[kRows]) {
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        const SlotRoute r = (rows[rr] < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
+        p[rr].h = c.h;
+        p[rr].src = r.src;
+        p[rr].reg = r.reg;
+        p[rr].tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
+        p[rr].land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p[rr].tok) : (uint8_t)0;
+        p[rr].lse = 0.f;
+      }
     };
     ItemCursor cur;
-    SlotPrep pc, pn;
+    SlotPrep pc[kRows], pn[kRows];
     if (count > 0) {
       cur.init(g, L);
       prep(cur, pc);
@@ -168,45 +186,51 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (!mbar_try_wait(bar(bEmpty + s), par)) {
-          // about to block: announce everything still pending first
+        if (kFlushBeforeBlock && !mbar_try_wait(bar(bEmpty + s), par)) {
           cp_async_wait<0>();
           fence_proxy_async_smem();
           for (; pending >= 0 && pending < it; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
           pending = -1;
-          if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
         }
+        if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
       }
-      const bool valid = pc.src >= 0;
-      const bool live = valid && !pc.land;
-      const int64_t off = pc.tok * g.C + (int64_t)pc.h * 32;
-      const uint32_t nb = valid ? 16u : 0u;
       const uint32_t st = sbase + s * kStageBytes;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        cp_async16(st + kQ + sw64(pt, c), q + off + 8 * c, nb);
-        cp_async16(st + kK + sw64(pt, c), k + off + 8 * c, nb);
-        cp_async16(st + kV + sw64(pt, c), v + off + 8 * c, nb);
-      }
-      uint32_t qm[8], km[8];
-      build_mask_rows(live, pc.reg, qm, km);
       uint8_t *sp = smem + s * kStageBytes;
-      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
-      *reinterpret_cast<uint4 *>(sp + kQm + sw32(pt, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
-      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
-      *reinterpret_cast<uint4 *>(sp + kKm + sw32(pt, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
-      reinterpret_cast<int *>(sp + kMeta)[pt] = valid ? pc.src : -1;
-      (sp + kMeta + 512)[pt] = live ? 1 : 0;
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        const int row = rows[rr];
+        if (row >= 128) continue;
+        const SlotPrep &q0 = pc[rr];
+        const bool valid = q0.src >= 0;
+        const bool live = valid && !q0.land;
+        const int64_t off = q0.tok * g.C + (int64_t)q0.h * 32;
+        const uint32_t nb = valid ? 16u : 0u;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          cp_async16(st + kQ + sw64(row, c), q + off + 8 * c, nb);
+          cp_async16(st + kK + sw64(row, c), k + off + 8 * c, nb);
+          cp_async16(st + kV + sw64(row, c), v + off + 8 * c, nb);
+        }
+        uint32_t qm[8], km[8];
+        build_mask_rows(live, q0.reg, qm, km);
+        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
+        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
+        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
+        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
+        reinterpret_cast<int *>(sp + kMeta)[row] = valid ? q0.src : -1;
+        (sp + kMeta + 512)[row] = live ? 1 : 0;
+      }
       cp_async_commit();
       if (pending < 0) pending = it;
-      if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
+      if (it - pending >= kAhead) {
         cp_async_wait<kAhead>();
         fence_proxy_async_smem();
         mbar_arrive(bar(bFull + (int)(pending % kStages)));
         ++pending;
       }
       cur = nx;
-      pc = pn;
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) pc[rr] = pn[rr];
     }
     cp_async_wait_all();
     if (pending >= 0 && !*abort_flag) {
@@ -215,40 +239,65 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
+    // Event loop: S(k) is issued as soon as its data has landed and PV(k-2)
+    // (same TMEM buffer) has been issued; PV(k) as soon as P(k) is written and
+    // the epilogue has read O(k-2). Neither waits behind the other.
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16(128, N, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(128, 32, 0, 1);
-      auto issue_s = [&](int64_t it) -> bool {
-        const int s = (int)(it % kStages), wb = (int)(it & 1);
-        if (!mbar_wait(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) return false;
-        if (it >= 2 && !mbar_wait(bar(bTFree + wb), (uint32_t)((it >> 1) - 1) & 1u, ctl)) return false;
-        tc_fence_after();
-        const uint32_t st = sbase + s * kStageBytes;
-        const uint32_t d = tmem + kColS + 128u * wb;
-        mma_ss(d, smem_desc(st + kQ, 16, 512, kSwizzle64B), smem_desc(st + kK, 16, 512, kSwizzle64B), idesc_qk, 0);
-        mma_ss(d, smem_desc(st + kQ + 32, 16, 512, kSwizzle64B), smem_desc(st + kK + 32, 16, 512, kSwizzle64B),
-               idesc_qk, 1);
-        mma_ss(d, smem_desc(st + kQm, 16, 256, kSwizzle32B), smem_desc(st + kKm, 16, 256, kSwizzle32B), idesc_qk, 1);
-        mma_commit(bar(bSFull + wb));
-        return true;
-      };
-      auto issue_pv = [&](int64_t it) -> bool {
-        const int s = (int)(it % kStages), wb = (int)(it & 1);
-        if (!mbar_wait(bar(bPFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) return false;
-        tc_fence_after();
-        const uint32_t st = sbase + s * kStageBytes;
-        const uint32_t d = tmem + kColO + 32u * wb, p = tmem + kColS + 128u * wb;
-        for (int kk = 0; kk < NG; ++kk)
-          mma_ts(d, p + 8u * kk, smem_desc(st + kV + 1024u * kk, kTileBytes, 512, kSwizzle64B), idesc_pv,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(bar(bOFull + wb));
-        mma_commit(bar(bEmpty + s));
-        return true;
-      };
-      if (count > 0 && issue_s(0)) {
-        for (int64_t it = 0; it < count; ++it) {
-          if (it + 1 < count && !issue_s(it + 1)) break;
-          if (!issue_pv(it)) break;
+      int64_t ns = 0, npv = 0;
+      uint64_t idle_since = 0;
+      uint32_t spins = 0;
+      while (npv < count) {
+        bool progress = false;
+        if (ns < count && ns <= npv + 1) {
+          const int s = (int)(ns % kStages), wb = (int)(ns & 1);
+          if (mbar_try_wait(bar(bFull + s), (uint32_t)(ns / kStages) & 1u)) {
+            tc_fence_after();
+            const uint32_t st = sbase + s * kStageBytes;
+            const uint32_t d = tmem + kColS + 128u * wb;
+            mma_ss(d, smem_desc(st + kQ, 16, 512, kSwizzle64B), smem_desc(st + kK, 16, 512, kSwizzle64B), idesc_qk,
+                   0);
+            mma_ss(d, smem_desc(st + kQ + 32, 16, 512, kSwizzle64B), smem_desc(st + kK + 32, 16, 512, kSwizzle64B),
+                   idesc_qk, 1);
+            mma_ss(d, smem_desc(st + kQm, 16, 256, kSwizzle32B), smem_desc(st + kKm, 16, 256, kSwizzle32B),
+                   idesc_qk, 1);
+            mma_commit(bar(bSFull + wb));
+            ++ns;
+            progress = true;
+          }
+        }
+        if (npv < ns) {
+          const int s = (int)(npv % kStages), wb = (int)(npv & 1);
+          if (mbar_try_wait(bar(bPFull + wb), (uint32_t)(npv >> 1) & 1u) &&
+              (npv < 2 || mbar_try_wait(bar(bTFree + wb), (uint32_t)((npv >> 1) - 1) & 1u))) {
+            tc_fence_after();
+            const uint32_t st = sbase + s * kStageBytes;
+            const uint32_t d = tmem + kColO + 32u * wb, p = tmem + kColS + 128u * wb;
+            for (int kk = 0; kk < NG; ++kk)
+              mma_ts(d, p + 8u * kk, smem_desc(st + kV + 1024u * kk, kTileBytes, 512, kSwizzle64B), idesc_pv,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(bar(bOFull + wb));
+            mma_commit(bar(bEmpty + s));
+            ++npv;
+            progress = true;
+          }
+        }
+        if (progress) {
+          spins = 0;
+          idle_since = 0;
+          continue;
+        }
+        if ((++spins & 63u) == 0) {
+          if (*abort_flag) break;
+          const uint64_t now = globaltimer();
+          if (idle_since == 0) {
+            idle_since = now;
+          } else if (now - idle_since > a.wait_limit_ns) {
+            *abort_flag = 1;
+            atomicCAS(a.status, 0, kStatusTimeout);
+            break;
+          }
         }
       }
       // drain every MMA this thread issued before TMEM is released
@@ -260,153 +309,159 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     __syncwarp();
   } else {
     // ----------------------------------------------------------- softmax ---
+    // Thread (grp, i): TMEM lane i (query slot i), columns of 16-column groups
+    // [gb, ge) of the item's S row, loaded into registers with one wait.
+    // x = S*scale*log2e + bias*log2e (this half of bias row i, in smem), half
+    // row max -> exchanged -> row max m; p = exp2(x - m) -> P (bf16) over S;
+    // half row sums are exchanged for the epilogue. The epilogue of the
+    // previous item (its O row half normalised and stored at the grid token;
+    // the log-sum-exp) runs after this item's P is written, so the PV of the
+    // previous item is hidden behind this item's softmax.
     const int grp = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane;
+    const int ng0 = (NG + 1) >> 1, gb = grp ? ng0 : 0, ge = grp ? NG : ng0;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-    const uint32_t tS = tmem + lane_addr + kColS + 128u * grp;
-    const uint32_t tO = tmem + lane_addr + kColO + 32u * grp;
-    const uint32_t tB = tmem + lane_addr + kColBias;
+    float *brow = reinterpret_cast<float *>(smem + kBias) + i * kBiasStride;
+    // exchange slots, double-buffered by item parity: a warpgroup can only
+    // rewrite a slot after the other one passed the next max barrier
+    float *xmax = reinterpret_cast<float *>(smem + kXchg);         // [2][2][128]
+    float *xsum = reinterpret_cast<float *>(smem + kXchg + 2048);  // [2][2][128]
     const float cs = a.scale * kLog2e;
     const float2 cs2 = make_float2(cs, cs);
     int cur_h = -1;
-    uint32_t hc = 0;
     bool ok = true;
-    if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
-    ItemCursor x;
-    if (count > 0) x.init(g, L);
-    for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
-      if (x.h != cur_h) {
-        // head change: both warpgroups finished the previous head's items;
-        // each writes half of the bias tile (columns 64*grp .. +63) of its lane.
-        mbar_arrive(bar(bHcArrive));
-        if (!mbar_wait_warp(bar(bHcArrive), hc & 1u, ctl)) break;
-        tc_fence_after();
-        int wc0[3] = {0, 0, 0};
-        const int rb = (i < n) ? slot_route(g, wc0, i).rbase : 0;
-#pragma unroll 1
-        for (int jg = 0; jg < 4; ++jg) {
-          uint32_t vals[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int j = 64 * grp + 16 * jg + e;
-            float b = 0.f;
-            if (i < n && j < n && a.bias) b = a.bias[(int64_t)(rb - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
-            vals[e] = __float_as_uint(b);
-          }
-          tmem_st16(tB + 64u * grp + 16u * jg, vals);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(bHcDone));
-        if (!mbar_wait_warp(bar(bHcDone), hc & 1u, ctl)) break;
-        tc_fence_after();
-        ++hc;
-        cur_h = x.h;
-      }
-      if ((int)(it & 1) != grp) continue;
-      const uint32_t kk = (uint32_t)(it >> 1);
-      const int s = (int)(it % kStages);
-      if (!mbar_wait_warp(bar(bSFull + grp), kk & 1u, ctl)) break;
+    // deferred epilogue state of the previous item
+    bool have_prev = false, prev_live = false;
+    int prev_src = -1, prev_b = 0, prev_h = 0;
+    int64_t prev_it = 0;
+    float prev_m = 0.f;
+    auto load_o = [&](uint32_t (&ov)[16]) -> bool {
+      const int wb = (int)(prev_it & 1);
+      if (!mbar_wait_warp(bar(bOFull + wb), (uint32_t)(prev_it >> 1) & 1u, ctl)) return false;
       tc_fence_after();
-      if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
-      const uint8_t *sp = smem + s * kStageBytes;
-      const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
-      const bool live = (sp + kMeta + 512)[i] != 0;
-      // pass 1: row max of x = S*cs + bias. TMEM loads of group gi+1 are in
-      // flight while group gi is computed (two register buffers).
-      float m = -INFINITY;
-      auto max_group = [&](uint32_t (&sv)[16], uint32_t (&bv)[16]) {
+      tmem_ld16(tmem + lane_addr + kColO + 32u * wb + 16u * grp, ov);
+      tmem_wait_ld_tied(ov);
+      return true;
+    };
+    auto store_o = [&](const uint32_t (&ov)[16]) {
+      if (i < n && prev_src >= 0) {
+        const int pb = (int)(prev_it & 1);
+        const float sum = xsum[(pb * 2 + 0) * 128 + i] + xsum[(pb * 2 + 1) * 128 + i];
+        const int64_t tok = (int64_t)prev_b * g.tokens + prev_src;
+        uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)prev_h * 32 +
+                                              16 * grp);
+        const float inv = prev_live ? 1.0f / sum : 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          const float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
-                                       make_float2(__uint_as_float(bv[e]), __uint_as_float(bv[e + 1])));
-          m = max3(m, xs.x, xs.y);
-        }
-      };
-      uint32_t s0[16], b0[16], s1[16], b1[16];
-      tmem_ld16(tS, s0);
-      tmem_ld16(tB, b0);
-#pragma unroll
-      for (int gi = 0; gi < 8; gi += 2) {
-        if (gi < NG) {
-          tmem_wait_ld_tied(s0, b0);
-          if (gi + 1 < NG) {
-            tmem_ld16(tS + 16u * (gi + 1), s1);
-            tmem_ld16(tB + 16u * (gi + 1), b1);
-          }
-          max_group(s0, b0);
-        }
-        if (gi + 1 < NG) {
-          tmem_wait_ld_tied(s1, b1);
-          if (gi + 2 < NG) {
-            tmem_ld16(tS + 16u * (gi + 2), s0);
-            tmem_ld16(tB + 16u * (gi + 2), b0);
-          }
-          max_group(s1, b1);
-        }
-      }
-      // pass 2: p = exp2(x - m), row sum, P (bf16) written over S
-      const float2 negm = make_float2(-m, -m);
-      float2 sum2 = make_float2(0.f, 0.f);
-      auto exp_group = [&](int gi, uint32_t (&sv)[16], uint32_t (&bv)[16]) {
-        uint32_t pv[8];
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float2 xs = __ffma2_rn(make_float2(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), cs2,
-                                 make_float2(__uint_as_float(bv[e]), __uint_as_float(bv[e + 1])));
-          xs = __fadd2_rn(xs, negm);
-          const float2 p = make_float2(ex2(xs.x), ex2(xs.y));
-          sum2 = __fadd2_rn(sum2, p);
-          pv[e >> 1] = pack_bf16(p.x, p.y);
-        }
-        tmem_st8(tS + 8u * gi, pv);
-      };
-      tmem_ld16(tS, s0);
-      tmem_ld16(tB, b0);
-#pragma unroll
-      for (int gi = 0; gi < 8; gi += 2) {
-        if (gi < NG) {
-          tmem_wait_ld_tied(s0, b0);
-          if (gi + 1 < NG) {
-            tmem_ld16(tS + 16u * (gi + 1), s1);
-            tmem_ld16(tB + 16u * (gi + 1), b1);
-          }
-          exp_group(gi, s0, b0);
-        }
-        if (gi + 1 < NG) {
-          tmem_wait_ld_tied(s1, b1);
-          if (gi + 2 < NG) {
-            tmem_ld16(tS + 16u * (gi + 2), s0);
-            tmem_ld16(tB + 16u * (gi + 2), b0);
-          }
-          exp_group(gi + 1, s1, b1);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar(bPFull + grp));
-      if (!mbar_wait_warp(bar(bOFull + grp), kk & 1u, ctl)) break;
-      tc_fence_after();
-      uint32_t ov[32];
-      tmem_ld16(tO, *reinterpret_cast<uint32_t(*)[16]>(ov));
-      tmem_ld16(tO + 16, *reinterpret_cast<uint32_t(*)[16]>(ov + 16));
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(bTFree + grp));
-      if (i < n && src >= 0) {
-        const int64_t tok = (int64_t)x.b * g.tokens + src;
-        uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)x.h * 32);
-        const float sum = sum2.x + sum2.y;
-        const float inv = live ? 1.0f / sum : 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             w[e] = pack_bf16(__uint_as_float(ov[8 * c + 2 * e]) * inv, __uint_as_float(ov[8 * c + 2 * e + 1]) * inv);
           op[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        if (a.lse)
-          a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m + __log2f(sum)) * kLn2 : -INFINITY;
+        if (grp == 0 && a.lse)
+          a.lse[((int64_t)prev_b * g.heads + prev_h) * g.tokens + prev_src] =
+              prev_live ? (prev_m + __log2f(sum)) * kLn2 : -INFINITY;
+      }
+    };
+    if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
+    ItemCursor x;
+    if (count > 0) x.init(g, L);
+    for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
+      if (x.h != cur_h) {
+        // head change: this thread alone reads this half of bias row i
+        int wc0[3] = {0, 0, 0};
+        const int rb = (i < n) ? slot_route(g, wc0, i).rbase : 0;
+        for (int j = 16 * gb; j < 16 * ge; ++j) {
+          float b = 0.f;
+          if (i < n && j < n && a.bias) b = a.bias[(int64_t)(rb - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
+          brow[j] = b;
+        }
+        cur_h = x.h;
+      }
+      const int wb = (int)(it & 1), s = (int)(it % kStages);
+      const uint32_t tS = tmem + lane_addr + kColS + 128u * wb;
+      if (!mbar_wait_warp(bar(bSFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) break;
+      tc_fence_after();
+      uint32_t sv[4][16];
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4)
+        if (gb + k4 < ge) tmem_ld16(tS + 16u * (gb + k4), sv[k4]);
+      if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
+      const uint8_t *sp = smem + s * kStageBytes;
+      const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
+      const bool live = (sp + kMeta + 512)[i] != 0;
+      tmem_wait_ld_tied(sv[0], sv[1]);
+      tmem_wait_ld_tied(sv[2], sv[3]);
+      // x = S*cs + bias2 (kept in sv), half row max
+      float m = -INFINITY;
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        if (gb + k4 < ge) {
+#pragma unroll
+          for (int e4 = 0; e4 < 16; e4 += 4) {
+            const float4 b4 = *reinterpret_cast<const float4 *>(brow + 16 * (gb + k4) + e4);
+            const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e4]), __uint_as_float(sv[k4][e4 + 1])),
+                                         cs2, make_float2(b4.x, b4.y));
+            const float2 x1 = __ffma2_rn(
+                make_float2(__uint_as_float(sv[k4][e4 + 2]), __uint_as_float(sv[k4][e4 + 3])), cs2,
+                make_float2(b4.z, b4.w));
+            sv[k4][e4] = __float_as_uint(x0.x);
+            sv[k4][e4 + 1] = __float_as_uint(x0.y);
+            sv[k4][e4 + 2] = __float_as_uint(x1.x);
+            sv[k4][e4 + 3] = __float_as_uint(x1.y);
+            m = max3(m, max3(x0.x, x0.y, x1.x), x1.y);
+          }
+        }
+      }
+      const int xb = (int)(it & 1) * 256;
+      xmax[xb + grp * 128 + i] = m;
+      mbar_arrive(bar(bMax));
+      if (!mbar_wait_warp(bar(bMax), (uint32_t)it & 1u, ctl)) break;
+      m = fmaxf(xmax[xb + i], xmax[xb + 128 + i]);
+      // p = exp2(x - m), half row sum, P (bf16) over S
+      const float2 negm = make_float2(-m, -m);
+      float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k4 = 0; k4 < 4; ++k4) {
+        if (gb + k4 < ge) {
+          uint32_t pv[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float2 xs =
+                __fadd2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), negm);
+            const float2 p = make_float2(ex2(xs.x), ex2(xs.y));
+            sum2 = __fadd2_rn(sum2, p);
+            pv[e >> 1] = pack_bf16(p.x, p.y);
+          }
+          tmem_st8(tS + 8u * (gb + k4), pv);
+        }
+      }
+      tmem_wait_st();
+      // epilogue of the previous item: its PV finished during this softmax;
+      // both halves' sums of it were exchanged before this item's max barrier.
+      uint32_t ov[16];
+      if (have_prev && !load_o(ov)) break;
+      xsum[((int)(it & 1) * 2 + grp) * 128 + i] = sum2.x + sum2.y;
+      tc_fence_before();
+      if (have_prev) mbar_arrive(bar(bTFree + (int)(prev_it & 1)));
+      mbar_arrive(bar(bPFull + wb));
+      if (have_prev) store_o(ov);
+      have_prev = true;
+      prev_live = live;
+      prev_src = src;
+      prev_b = x.b;
+      prev_h = x.h;
+      prev_it = it;
+      prev_m = m;
+    }
+    if (have_prev && !*abort_flag) {
+      // the other half's sum of the last item: both warpgroups meet once more
+      mbar_arrive(bar(bMax));
+      uint32_t ov[16];
+      if (mbar_wait_warp(bar(bMax), (uint32_t)(prev_it + 1) & 1u, ctl) && load_o(ov)) {
+        tc_fence_before();
+        mbar_arrive(bar(bTFree + (int)(prev_it & 1)));
+        store_o(ov);
       }
     }
     tmem_wait_st();
@@ -435,6 +490,9 @@ namespace bwd {
 
 constexpr int kStages = 2;
 constexpr int kAhead = 1;
+// dK/dQ(it-2), which frees stage s(it), are issued after S(it-1): item it-1
+// must be announced before the gather warps block on empty[].
+constexpr bool kFlushBeforeBlock = true;
 constexpr int kTile = 128 * 64, kMask = 128 * 32;
 constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kdO = 3 * kTile, kQm = 4 * kTile, kKm = kQm + kMask;
 constexpr int kMeta = kKm + kMask;  // int32 src[128] @0, float lse2[128] @512, uint8 live[128] @1024
@@ -552,14 +610,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (!mbar_try_wait(bar(bEmpty + s), par)) {
+        if (kFlushBeforeBlock && !mbar_try_wait(bar(bEmpty + s), par)) {
           // about to block: announce everything still pending first
           cp_async_wait<0>();
           fence_proxy_async_smem();
           for (; pending >= 0 && pending < it; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
           pending = -1;
-          if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
         }
+        if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
       }
       const uint32_t st = sbase + s * kStageBytes;
       uint8_t *sp = smem + s * kStageBytes;
