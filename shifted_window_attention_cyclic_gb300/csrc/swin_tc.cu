@@ -52,26 +52,31 @@ struct SlotPrep {
   float lse;
 };
 
+// One 16-byte chunk (columns 8*half .. 8*half+7) of a slot's mask row:
+// key = false gives the Qm row, key = true the Km row (see below).
+__device__ __forceinline__ uint4 mask_chunk(bool live, int reg, bool key, int half) {
+  uint32_t r[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int c0 = 8 * half + 2 * t;
+    const bool h0 = live && reg == c0, h1 = live && reg == c0 + 1;
+    const uint32_t lo = key ? (h0 ? 0u : kBf16NegBig) : (h0 ? kBf16One : 0u);
+    const uint32_t hi = key ? (h1 ? 0u : kBf16NegBig) : (h1 ? kBf16One : 0u);
+    r[t] = lo | (hi << 16);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 // Mask rows of one slot: Qm = one-hot of the query's region bits (live
 // queries only); Km = 0 in the column of the key's region if the key is live,
 // -2^100 everywhere else. Qm Km^T then adds -2^100 to every masked logit.
-__device__ __forceinline__ void build_mask_rows(bool live, int reg, uint32_t (&qm)[8], uint32_t (&km)[8]) {
-#pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const uint32_t lo = (live && reg == 2 * w) ? 0u : kBf16NegBig;
-    const uint32_t hi = (live && reg == 2 * w + 1) ? 0u : kBf16NegBig;
-    km[w] = lo | (hi << 16);
-    const uint32_t qlo = (live && reg == 2 * w) ? kBf16One : 0u;
-    const uint32_t qhi = (live && reg == 2 * w + 1) ? kBf16One : 0u;
-    qm[w] = qlo | (qhi << 16);
-  }
 }
 
 // ---------------------------------------------------------------- forward ---
 namespace fwd {
 
 constexpr int kStages = 4;
-constexpr int kAhead = kStages - 2;  // items whose copies stay in flight unannounced
+constexpr int kAhead = 1;  // items whose copies stay in flight unannounced
 // The MMA thread issues S(k) only after PV(k-2), so freeing stage s(it) (PV
 // of item it - kStages) needs items up to it - kStages + 2 announced; with
 // kAhead <= kStages - 2 the gather warps may block on empty[] while still
@@ -145,35 +150,42 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
 
   if (warp >= kProducerWarp0 && warp < kMmaWarp) {
     // ------------------------------------------------------------ gather ---
-    // Route every slot of the item (roll, ragged pad, region) and cp.async its
-    // Q, K, V rows into the stage; the land byte of the next item is loaded
-    // one item ahead. Copies of items [pending, it] are in flight unannounced.
+    // Four consecutive threads gather one slot row: thread quad rq takes rows
+    // rq, rq + 24, rq + 48, ...; lane cq copies 16-byte chunk cq of the row's
+    // 64 bytes (one request of two full sectors per row and tensor). The
+    // route and land byte of the next item are prepared one item ahead.
     const int pt = threadIdx.x - kProducerWarp0 * 32;
+    const int cq = pt & 3, rq = pt >> 2;
+    constexpr int kRowStep = kProducerThreads / 4;
+    constexpr int kRows = (128 + kRowStep - 1) / kRowStep;
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    constexpr int kRows = (128 + kProducerThreads - 1) / kProducerThreads;  // slot rows per thread
-    int rows[kRows];
     SlotCoord scoord[kRows];
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) {
-      rows[rr] = pt + rr * kProducerThreads;
-      scoord[rr] = slot_coord(g, rows[rr] < n ? rows[rr] : 0);
+      const int row = rq + rr * kRowStep;
+      scoord[rr] = slot_coord(g, row < n ? row : 0);
     }
-    auto prep = [&](const ItemCursor &c, SlotPrep (&p)[kRows]) {
+    struct Prep {
+      int h, b;
+      int src[kRows], reg[kRows];
+      uint8_t land[kRows];
+    };
+    auto prep = [&](const ItemCursor &c, Prep &p) {
+      p.h = c.h;
+      p.b = c.b;
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
-        const SlotRoute r = (rows[rr] < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
-        p[rr].h = c.h;
-        p[rr].src = r.src;
-        p[rr].reg = r.reg;
-        p[rr].tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
-        p[rr].land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p[rr].tok) : (uint8_t)0;
-        p[rr].lse = 0.f;
+        const int row = rq + rr * kRowStep;
+        const SlotRoute r = (row < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
+        p.src[rr] = r.src;
+        p.reg[rr] = r.reg;
+        p.land[rr] = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : (uint8_t)0;
       }
     };
     ItemCursor cur;
-    SlotPrep pc[kRows], pn[kRows];
+    Prep pc, pn;
     if (count > 0) {
       cur.init(g, L);
       prep(cur, pc);
@@ -186,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (kFlushBeforeBlock && !mbar_try_wait(bar(bEmpty + s), par)) {
+        if (kFlushBeforeBlock && !mbar_test(bar(bEmpty + s), par)) {
+          // about to block: announce everything still pending first
           cp_async_wait<0>();
           fence_proxy_async_smem();
           for (; pending >= 0 && pending < it; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
@@ -196,41 +209,36 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       }
       const uint32_t st = sbase + s * kStageBytes;
       uint8_t *sp = smem + s * kStageBytes;
+      const Prep &p = pc;
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
-        const int row = rows[rr];
-        if (row >= 128) continue;
-        const SlotPrep &q0 = pc[rr];
-        const bool valid = q0.src >= 0;
-        const bool live = valid && !q0.land;
-        const int64_t off = q0.tok * g.C + (int64_t)q0.h * 32;
-        const uint32_t nb = valid ? 16u : 0u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          cp_async16(st + kQ + sw64(row, c), q + off + 8 * c, nb);
-          cp_async16(st + kK + sw64(row, c), k + off + 8 * c, nb);
-          cp_async16(st + kV + sw64(row, c), v + off + 8 * c, nb);
+        const int row = rq + rr * kRowStep;
+        if (row < 128) {
+          const bool valid = p.src[rr] >= 0;
+          const bool live = valid && !p.land[rr];
+          const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
+          const uint32_t nb = valid ? 16u : 0u;
+          cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
+          cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
+          cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
+          *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
+              mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
+          if (cq == 0) {
+            reinterpret_cast<int *>(sp + kMeta)[row] = valid ? p.src[rr] : -1;
+            (sp + kMeta + 512)[row] = live ? 1 : 0;
+          }
         }
-        uint32_t qm[8], km[8];
-        build_mask_rows(live, q0.reg, qm, km);
-        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
-        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
-        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
-        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
-        reinterpret_cast<int *>(sp + kMeta)[row] = valid ? q0.src : -1;
-        (sp + kMeta + 512)[row] = live ? 1 : 0;
       }
       cp_async_commit();
       if (pending < 0) pending = it;
-      if (it - pending >= kAhead) {
+      if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
         cp_async_wait<kAhead>();
         fence_proxy_async_smem();
         mbar_arrive(bar(bFull + (int)(pending % kStages)));
         ++pending;
       }
       cur = nx;
-#pragma unroll
-      for (int rr = 0; rr < kRows; ++rr) pc[rr] = pn[rr];
+      pc = pn;
     }
     cp_async_wait_all();
     if (pending >= 0 && !*abort_flag) {
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         bool progress = false;
         if (ns < count && ns <= npv + 1) {
           const int s = (int)(ns % kStages), wb = (int)(ns & 1);
-          if (mbar_try_wait(bar(bFull + s), (uint32_t)(ns / kStages) & 1u)) {
+          if (mbar_test(bar(bFull + s), (uint32_t)(ns / kStages) & 1u)) {
             tc_fence_after();
             const uint32_t st = sbase + s * kStageBytes;
             const uint32_t d = tmem + kColS + 128u * wb;
@@ -269,8 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         }
         if (npv < ns) {
           const int s = (int)(npv % kStages), wb = (int)(npv & 1);
-          if (mbar_try_wait(bar(bPFull + wb), (uint32_t)(npv >> 1) & 1u) &&
-              (npv < 2 || mbar_try_wait(bar(bTFree + wb), (uint32_t)((npv >> 1) - 1) & 1u))) {
+          if (mbar_test(bar(bPFull + wb), (uint32_t)(npv >> 1) & 1u) &&
+              (npv < 2 || mbar_test(bar(bTFree + wb), (uint32_t)((npv >> 1) - 1) & 1u))) {
             tc_fence_after();
             const uint32_t st = sbase + s * kStageBytes;
             const uint32_t d = tmem + kColO + 32u * wb, p = tmem + kColS + 128u * wb;
@@ -568,36 +576,45 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
 
   if (warp >= kProducerWarp0 && warp < kMmaWarp) {
     // ------------------------------------------------------------ gather ---
+    // Four consecutive threads gather one slot row: thread quad rq takes rows
+    // rq, rq + 24, rq + 48, ...; lane cq copies 16-byte chunk cq of the row's
+    // 64 bytes (one request of two full sectors per row and tensor). The
+    // route and land byte of the next item are prepared one item ahead.
     const int pt = threadIdx.x - kProducerWarp0 * 32;
+    const int cq = pt & 3, rq = pt >> 2;
+    constexpr int kRowStep = kProducerThreads / 4;
+    constexpr int kRows = (128 + kRowStep - 1) / kRowStep;
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
     const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
-    // Same gather as the forward plus dO rows and each slot's saved LSE;
-    // the land byte and the LSE of the next item are loaded one item ahead.
-    constexpr int kRows = (128 + kProducerThreads - 1) / kProducerThreads;  // slot rows per thread
-    int rows[kRows];
     SlotCoord scoord[kRows];
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) {
-      rows[rr] = pt + rr * kProducerThreads;
-      scoord[rr] = slot_coord(g, rows[rr] < n ? rows[rr] : 0);
+      const int row = rq + rr * kRowStep;
+      scoord[rr] = slot_coord(g, row < n ? row : 0);
     }
-    auto prep = [&](const ItemCursor &c, SlotPrep (&p)[kRows]) {
+    struct Prep {
+      int h, b;
+      int src[kRows], reg[kRows];
+      uint8_t land[kRows];
+      float lse[kRows];
+    };
+    auto prep = [&](const ItemCursor &c, Prep &p) {
+      p.h = c.h;
+      p.b = c.b;
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
-        const int row = rows[rr];
+        const int row = rq + rr * kRowStep;
         const SlotRoute r = (row < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
-        p[rr].h = c.h;
-        p[rr].src = r.src;
-        p[rr].reg = r.reg;
-        p[rr].tok = (int64_t)c.b * g.tokens + (r.src >= 0 ? r.src : 0);
-        p[rr].land = (r.src >= 0 && g.has_land) ? __ldg(a.land + p[rr].tok) : (uint8_t)0;
-        p[rr].lse = (r.src >= 0) ? __ldg(a.lse + ((int64_t)c.b * g.heads + c.h) * g.tokens + r.src) : 0.f;
+        p.src[rr] = r.src;
+        p.reg[rr] = r.reg;
+        p.land[rr] = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : (uint8_t)0;
+        p.lse[rr] = (r.src >= 0) ? __ldg(a.lse + ((int64_t)c.b * g.heads + c.h) * g.tokens + r.src) : 0.f;
       }
     };
     ItemCursor cur;
-    SlotPrep pc[kRows], pn[kRows];
+    Prep pc, pn;
     if (count > 0) {
       cur.init(g, L);
       prep(cur, pc);
@@ -610,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (kFlushBeforeBlock && !mbar_try_wait(bar(bEmpty + s), par)) {
+        if (kFlushBeforeBlock && !mbar_test(bar(bEmpty + s), par)) {
           // about to block: announce everything still pending first
           cp_async_wait<0>();
           fence_proxy_async_smem();
@@ -621,31 +638,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       }
       const uint32_t st = sbase + s * kStageBytes;
       uint8_t *sp = smem + s * kStageBytes;
+      const Prep &p = pc;
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
-        const int row = rows[rr];
-        if (row >= 128) continue;
-        const SlotPrep &q0 = pc[rr];
-        const bool valid = q0.src >= 0;
-        const bool live = valid && !q0.land;
-        const int64_t off = q0.tok * g.C + (int64_t)q0.h * 32;
-        const uint32_t nb = valid ? 16u : 0u;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          cp_async16(st + kQ + sw64(row, c), q + off + 8 * c, nb);
-          cp_async16(st + kK + sw64(row, c), k + off + 8 * c, nb);
-          cp_async16(st + kV + sw64(row, c), v + off + 8 * c, nb);
-          cp_async16(st + kdO + sw64(row, c), dout + off + 8 * c, nb);
+        const int row = rq + rr * kRowStep;
+        if (row < 128) {
+          const bool valid = p.src[rr] >= 0;
+          const bool live = valid && !p.land[rr];
+          const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
+          const uint32_t nb = valid ? 16u : 0u;
+          cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
+          cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
+          cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
+          cp_async16(st + kdO + sw64(row, cq), dout + off + 8 * cq, nb);
+          *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
+              mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
+          if (cq == 0) {
+            reinterpret_cast<int *>(sp + kMeta)[row] = valid ? p.src[rr] : -1;
+            reinterpret_cast<float *>(sp + kMeta + 512)[row] = live ? p.lse[rr] * kLog2e : 0.f;
+            (sp + kMeta + 1024)[row] = live ? 1 : 0;
+          }
         }
-        uint32_t qm[8], km[8];
-        build_mask_rows(live, q0.reg, qm, km);
-        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 0)) = make_uint4(qm[0], qm[1], qm[2], qm[3]);
-        *reinterpret_cast<uint4 *>(sp + kQm + sw32(row, 1)) = make_uint4(qm[4], qm[5], qm[6], qm[7]);
-        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 0)) = make_uint4(km[0], km[1], km[2], km[3]);
-        *reinterpret_cast<uint4 *>(sp + kKm + sw32(row, 1)) = make_uint4(km[4], km[5], km[6], km[7]);
-        reinterpret_cast<int *>(sp + kMeta)[row] = valid ? q0.src : -1;
-        reinterpret_cast<float *>(sp + kMeta + 512)[row] = live ? q0.lse * kLog2e : 0.f;
-        (sp + kMeta + 1024)[row] = live ? 1 : 0;
       }
       cp_async_commit();
       if (pending < 0) pending = it;
@@ -656,8 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
         ++pending;
       }
       cur = nx;
-#pragma unroll
-      for (int rr = 0; rr < kRows; ++rr) pc[rr] = pn[rr];
+      pc = pn;
     }
     cp_async_wait_all();
     if (pending >= 0 && !*abort_flag) {
