@@ -70,7 +70,6 @@ __device__ __forceinline__ uint4 mask_chunk(bool live, int reg, bool key, int ha
 // Mask rows of one slot: Qm = one-hot of the query's region bits (live
 // queries only); Km = 0 in the column of the key's region if the key is live,
 // -2^100 everywhere else. Qm Km^T then adds -2^100 to every masked logit.
-}
 
 // ---------------------------------------------------------------- forward ---
 namespace fwd {
