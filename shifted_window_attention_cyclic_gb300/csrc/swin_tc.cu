@@ -123,16 +123,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bFull + s), kProducerThreads);
+      mbar_init(bar(bFull + s), kProducerThreads / 32);
       mbar_init(bar(bEmpty + s), 1);
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(bSFull + w), 1);
-      mbar_init(bar(bPFull + w), kSoftmaxWarps * 32);
+      mbar_init(bar(bPFull + w), kSoftmaxWarps);
       mbar_init(bar(bOFull + w), 1);
-      mbar_init(bar(bTFree + w), kSoftmaxWarps * 32);
+      mbar_init(bar(bTFree + w), kSoftmaxWarps);
     }
-    mbar_init(bar(bMax), kSoftmaxWarps * 32);
+    mbar_init(bar(bMax), kSoftmaxWarps);
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
@@ -197,14 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (kFlushBeforeBlock && !mbar_test(bar(bEmpty + s), par)) {
+        if (kFlushBeforeBlock && !__all_sync(0xffffffffu, mbar_test(bar(bEmpty + s), par))) {
           // about to block: announce everything still pending first
           cp_async_wait<0>();
           fence_proxy_async_smem();
-          for (; pending >= 0 && pending < it; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
+          for (; pending >= 0 && pending < it; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
           pending = -1;
         }
-        if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
+        if (!mbar_wait_warp(bar(bEmpty + s), par, ctl)) break;
       }
       const uint32_t st = sbase + s * kStageBytes;
       uint8_t *sp = smem + s * kStageBytes;
@@ -233,16 +233,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
         cp_async_wait<kAhead>();
         fence_proxy_async_smem();
-        mbar_arrive(bar(bFull + (int)(pending % kStages)));
+        mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
         ++pending;
       }
       cur = nx;
       pc = pn;
     }
     cp_async_wait_all();
-    if (pending >= 0 && !*abort_flag) {
+    if (pending >= 0 && !__any_sync(0xffffffffu, *abort_flag != 0)) {
       fence_proxy_async_smem();
-      for (; pending < count; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
+      for (; pending < count; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       }
       const int xb = (int)(it & 1) * 256;
       xmax[xb + grp * 128 + i] = m;
-      mbar_arrive(bar(bMax));
+      mbar_arrive_warp(bar(bMax));
       if (!mbar_wait_warp(bar(bMax), (uint32_t)it & 1u, ctl)) break;
       m = fmaxf(xmax[xb + i], xmax[xb + 128 + i]);
       // p = exp2(x - m), half row sum, P (bf16) over S
@@ -450,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       if (have_prev && !load_o(ov)) break;
       xsum[((int)(it & 1) * 2 + grp) * 128 + i] = sum2.x + sum2.y;
       tc_fence_before();
-      if (have_prev) mbar_arrive(bar(bTFree + (int)(prev_it & 1)));
-      mbar_arrive(bar(bPFull + wb));
+      if (have_prev) mbar_arrive_warp(bar(bTFree + (int)(prev_it & 1)));
+      mbar_arrive_warp(bar(bPFull + wb));
       if (have_prev) store_o(ov);
       have_prev = true;
       prev_live = live;
@@ -461,13 +461,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       prev_it = it;
       prev_m = m;
     }
-    if (have_prev && !*abort_flag) {
+    if (have_prev && !__any_sync(0xffffffffu, *abort_flag != 0)) {
       // the other half's sum of the last item: both warpgroups meet once more
-      mbar_arrive(bar(bMax));
+      mbar_arrive_warp(bar(bMax));
       uint32_t ov[16];
       if (mbar_wait_warp(bar(bMax), (uint32_t)(prev_it + 1) & 1u, ctl) && load_o(ov)) {
         tc_fence_before();
-        mbar_arrive(bar(bTFree + (int)(prev_it & 1)));
+        mbar_arrive_warp(bar(bTFree + (int)(prev_it & 1)));
         store_o(ov);
       }
     }
@@ -548,17 +548,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bFull + s), kProducerThreads);
-      mbar_init(bar(bEmpty + s), 1 + 128);
+      mbar_init(bar(bFull + s), kProducerThreads / 32);
+      mbar_init(bar(bEmpty + s), 1 + 4);  // MMA commit + epilogue warps
     }
     mbar_init(bar(bSpFull), 1);
-    mbar_init(bar(bPFull), kSoftmaxThreads);
-    mbar_init(bar(bDsFull), kSoftmaxThreads);
+    mbar_init(bar(bPFull), kSoftmaxThreads / 32);
+    mbar_init(bar(bDsFull), kSoftmaxThreads / 32);
     mbar_init(bar(bAccFull), 1);
-    mbar_init(bar(bAccFree), 128);
+    mbar_init(bar(bAccFree), 4);
     mbar_init(bar(bDsFree), 1);
-    mbar_init(bar(bWsync), kSoftmaxThreads);
-    mbar_init(bar(bDsync), kSoftmaxThreads);
+    mbar_init(bar(bWsync), kSoftmaxThreads / 32);
+    mbar_init(bar(bDsync), kSoftmaxThreads / 32);
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
@@ -626,14 +626,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       if (it + 1 < count) prep(nx, pn);
       if (it >= kStages) {
         const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (kFlushBeforeBlock && !mbar_test(bar(bEmpty + s), par)) {
+        if (kFlushBeforeBlock && !__all_sync(0xffffffffu, mbar_test(bar(bEmpty + s), par))) {
           // about to block: announce everything still pending first
           cp_async_wait<0>();
           fence_proxy_async_smem();
-          for (; pending >= 0 && pending < it; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
+          for (; pending >= 0 && pending < it; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
           pending = -1;
         }
-        if (!mbar_wait(bar(bEmpty + s), par, ctl)) break;
+        if (!mbar_wait_warp(bar(bEmpty + s), par, ctl)) break;
       }
       const uint32_t st = sbase + s * kStageBytes;
       uint8_t *sp = smem + s * kStageBytes;
@@ -664,16 +664,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
         cp_async_wait<kAhead>();
         fence_proxy_async_smem();
-        mbar_arrive(bar(bFull + (int)(pending % kStages)));
+        mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
         ++pending;
       }
       cur = nx;
       pc = pn;
     }
     cp_async_wait_all();
-    if (pending >= 0 && !*abort_flag) {
+    if (pending >= 0 && !__any_sync(0xffffffffu, *abort_flag != 0)) {
       fence_proxy_async_smem();
-      for (; pending < count; ++pending) mbar_arrive(bar(bFull + (int)(pending % kStages)));
+      for (; pending < count; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
     }
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       const int s = (int)(it % kStages);
       if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
       const int src = reinterpret_cast<const int *>(smem + s * kStageBytes + kMeta)[e];
-      mbar_arrive(bar(bEmpty + s));
+      mbar_arrive_warp(bar(bEmpty + s));
       if (!mbar_wait_warp(bar(bAccFull), (uint32_t)it & 1u, ctl)) break;
       tc_fence_after();
       // one 32-column accumulator at a time: TMEM -> registers -> bf16 -> grid
@@ -763,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       drain(kColdK, a.dk, a.scale);
       drain(kColdQ, a.dq, a.scale);
       tc_fence_before();
-      mbar_arrive(bar(bAccFree));
+      mbar_arrive_warp(bar(bAccFree));
     }
     tmem_wait_ld();
   } else {
@@ -795,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) brow[16 * gi + e] = __uint_as_float(av[e]);
       }
-      mbar_arrive(bar(bWsync));
+      mbar_arrive_warp(bar(bWsync));
       if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) return false;
       ++wsync_phase;
       const float *acc = reinterpret_cast<const float *>(smem + kBias);
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
             }
         a.ws[(int64_t)slot * g.T + t] = sum;
       }
-      mbar_arrive(bar(bWsync));
+      mbar_arrive_warp(bar(bWsync));
       if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) return false;
       ++wsync_phase;
       return true;
@@ -904,8 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(bPFull));
-      mbar_arrive(bar(bDsync));
+      mbar_arrive_warp(bar(bPFull));
+      mbar_arrive_warp(bar(bDsync));
       if (!mbar_wait_warp(bar(bDsync), (uint32_t)it & 1u, ctl)) break;
       delta = dpart[i] + dpart[128 + i];
       if (it >= 1 && !mbar_wait_warp(bar(bDsFree), (uint32_t)(it - 1) & 1u, ctl)) break;
@@ -962,9 +962,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(bar(bDsFull));
+      mbar_arrive_warp(bar(bDsFull));
     }
-    if (ok && !*abort_flag && cur_h >= 0 && want_db) flush(a.slot_base[blockIdx.x] + (cur_h - h_first));
+    if (ok && !__any_sync(0xffffffffu, *abort_flag != 0) && cur_h >= 0 && want_db) flush(a.slot_base[blockIdx.x] + (cur_h - h_first));
     tmem_wait_st();
     tmem_wait_ld();
   }

@@ -56,6 +56,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One arrival per warp: the lanes' prior writes (and fences) are ordered
+// before the elected lane's release-arrive by __syncwarp. Barriers that
+// count warps instead of threads avoid 32 contended atomics per warp.
+__device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Bounded-wait control: every spin ends either when the phase completes, when
 // another role of the CTA has raised the abort flag, or when `limit_ns` has
 // passed (then this thread raises the abort flag and the device status word).
