@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
           idle_since = 0;
           continue;
         }
+        __nanosleep(32);  // leave the issue slots to the softmax warps of this SMSP
         if ((++spins & 63u) == 0) {
           if (*abort_flag) break;
           const uint64_t now = globaltimer();
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       tmem_wait_ld_tied(sv[0], sv[1]);
       tmem_wait_ld_tied(sv[2], sv[3]);
       // x = S*cs + bias2 (kept in sv), half row max
-      float m = -INFINITY;
+      float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
         if (gb + k4 < ge) {
@@ -416,10 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
             sv[k4][e4 + 1] = __float_as_uint(x0.y);
             sv[k4][e4 + 2] = __float_as_uint(x1.x);
             sv[k4][e4 + 3] = __float_as_uint(x1.y);
-            m = max3(m, max3(x0.x, x0.y, x1.x), x1.y);
+            mp[e4 >> 2] = max3(mp[e4 >> 2], max3(x0.x, x0.y, x1.x), x1.y);
           }
         }
       }
+      float m = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
       const int xb = (int)(it & 1) * 256;
       xmax[xb + grp * 128 + i] = m;
       mbar_arrive_warp(bar(bMax));
@@ -427,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       m = fmaxf(xmax[xb + i], xmax[xb + 128 + i]);
       // p = exp2(x - m), half row sum, P (bf16) over S
       const float2 negm = make_float2(-m, -m);
-      float2 sum2 = make_float2(0.f, 0.f);
+      float2 sp2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
         if (gb + k4 < ge) {
@@ -437,12 +439,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
             const float2 xs =
                 __fadd2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), negm);
             const float2 p = make_float2(ex2(xs.x), ex2(xs.y));
-            sum2 = __fadd2_rn(sum2, p);
+            sp2[(e >> 1) & 3] = __fadd2_rn(sp2[(e >> 1) & 3], p);
             pv[e >> 1] = pack_bf16(p.x, p.y);
           }
           tmem_st8(tS + 8u * (gb + k4), pv);
         }
       }
+      const float2 sum2 = __fadd2_rn(__fadd2_rn(sp2[0], sp2[1]), __fadd2_rn(sp2[2], sp2[3]));
       tmem_wait_st();
       // epilogue of the previous item: its PV finished during this softmax;
       // both halves' sums of it were exchanged before this item's max barrier.
