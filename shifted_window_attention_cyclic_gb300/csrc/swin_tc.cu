@@ -93,14 +93,12 @@ constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
 constexpr int bFull = 0, bEmpty = kStages, bSFull = 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
               bTFree = bOFull + 2, bMax = bTFree + 2, bNever = bMax + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
-constexpr int kXchg = kMiscOff + 16;  // float max[2 items][4 parts][128], sum[2 items][4 parts][128]
-constexpr int kSmemBytes = kXchg + 8192 + 1024;  // + alignment slack
+constexpr int kXchg = kMiscOff + 16;  // float max[2 items][2 halves][128], sum[2 items][2 halves][128]
+constexpr int kSmemBytes = kXchg + 4096 + 1024;  // + alignment slack
 
-// warps 0-15: four softmax warpgroups, each owning a quarter of every row's
-// 16-column groups (groups g and g + 4); 16-18: gather; 19: MMA (640 threads
-// keep the 96-register budget)
-constexpr int kSoftmaxWGs = 4, kSoftmaxWarps = 4 * kSoftmaxWGs, kProducerWarp0 = kSoftmaxWarps,
-              kMmaWarp = kProducerWarp0 + 3;
+// warps 0-7: two softmax warpgroups, each owning half of every row's columns;
+// 8-10: gather; 11: MMA
+constexpr int kSoftmaxWarps = 8, kProducerWarp0 = 8, kMmaWarp = 11;
 constexpr int kProducerThreads = (kMmaWarp - kProducerWarp0) * 32;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 // TMEM columns: S/P of warpgroup w at 128*w, O of warpgroup w at 256 + 32*w
@@ -162,17 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    uint32_t scpack[kRows];  // in-window coordinates of each row, 8 bits per dim
+    SlotCoord scoord[kRows];
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) {
       const int row = rq + rr * kRowStep;
-      const SlotCoord c = slot_coord(g, row < n ? row : 0);
-      scpack[rr] = (uint32_t)c.sc[0] | ((uint32_t)c.sc[1] << 8) | ((uint32_t)c.sc[2] << 16);
+      scoord[rr] = slot_coord(g, row < n ? row : 0);
     }
     struct Prep {
       int h, b;
-      int src[kRows];
-      uint32_t flags[kRows];  // region bits | land << 8
+      int src[kRows], reg[kRows];
+      uint8_t land[kRows];
     };
     auto prep = [&](const ItemCursor &c, Prep &p) {
       p.h = c.h;
@@ -180,14 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
         const int row = rq + rr * kRowStep;
-        SlotCoord sc;
-        sc.sc[0] = scpack[rr] & 0xFF;
-        sc.sc[1] = (scpack[rr] >> 8) & 0xFF;
-        sc.sc[2] = scpack[rr] >> 16;
-        const SlotRoute r = (row < n) ? route_slot(g, c.wc, sc) : SlotRoute{-1, 0, 0, 0};
+        const SlotRoute r = (row < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
         p.src[rr] = r.src;
-        const uint32_t land = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : 0u;
-        p.flags[rr] = (uint32_t)r.reg | (land << 8);
+        p.reg[rr] = r.reg;
+        p.land[rr] = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : (uint8_t)0;
       }
     };
     ItemCursor cur;
@@ -221,14 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         const int row = rq + rr * kRowStep;
         if (row < 128) {
           const bool valid = p.src[rr] >= 0;
-          const bool live = valid && !(p.flags[rr] >> 8);
+          const bool live = valid && !p.land[rr];
           const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
           const uint32_t nb = valid ? 16u : 0u;
           cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
           cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
           cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
           *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
-              mask_chunk(live, (int)(p.flags[rr] & 0xFF), cq >= 2, cq & 1);
+              mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
           if (cq == 0) {
             reinterpret_cast<int *>(sp + kMeta)[row] = valid ? p.src[rr] : -1;
             (sp + kMeta + 512)[row] = live ? 1 : 0;
@@ -324,21 +317,22 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     __syncwarp();
   } else {
     // ----------------------------------------------------------- softmax ---
-    // Thread (grp, i): TMEM lane i (query slot i), 16-column groups grp and
-    // grp + 4 of the item's S row (loaded into registers with one wait).
-    // x = S*scale*log2e + bias*log2e (this part of bias row i, in smem), part
+    // Thread (grp, i): TMEM lane i (query slot i), columns of 16-column groups
+    // [gb, ge) of the item's S row, loaded into registers with one wait.
+    // x = S*scale*log2e + bias*log2e (this half of bias row i, in smem), half
     // row max -> exchanged -> row max m; p = exp2(x - m) -> P (bf16) over S;
-    // part sums are exchanged for the epilogue. The epilogue of the previous
-    // item (O columns 8*grp .. +7 of row i, normalised and stored at the grid
-    // token; the log-sum-exp) runs after this item's P is written, so the PV
-    // of the previous item is hidden behind this item's softmax.
+    // half row sums are exchanged for the epilogue. The epilogue of the
+    // previous item (its O row half normalised and stored at the grid token;
+    // the log-sum-exp) runs after this item's P is written, so the PV of the
+    // previous item is hidden behind this item's softmax.
     const int grp = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane;
+    const int ng0 = (NG + 1) >> 1, gb = grp ? ng0 : 0, ge = grp ? NG : ng0;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     float *brow = reinterpret_cast<float *>(smem + kBias) + i * kBiasStride;
     // exchange slots, double-buffered by item parity: a warpgroup can only
-    // rewrite a slot after all others passed the next max barrier
-    float *xmax = reinterpret_cast<float *>(smem + kXchg);         // [2][4][128]
-    float *xsum = reinterpret_cast<float *>(smem + kXchg + 4096);  // [2][4][128]
+    // rewrite a slot after the other one passed the next max barrier
+    float *xmax = reinterpret_cast<float *>(smem + kXchg);         // [2][2][128]
+    float *xsum = reinterpret_cast<float *>(smem + kXchg + 2048);  // [2][2][128]
     const float cs = a.scale * kLog2e;
     const float2 cs2 = make_float2(cs, cs);
     int cur_h = -1;
@@ -348,26 +342,30 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     int prev_src = -1, prev_b = 0, prev_h = 0;
     int64_t prev_it = 0;
     float prev_m = 0.f;
-    auto load_o = [&](uint32_t (&ov)[8]) -> bool {
+    auto load_o = [&](uint32_t (&ov)[16]) -> bool {
       const int wb = (int)(prev_it & 1);
       if (!mbar_wait_warp(bar(bOFull + wb), (uint32_t)(prev_it >> 1) & 1u, ctl)) return false;
       tc_fence_after();
-      tmem_ld8(tmem + lane_addr + kColO + 32u * wb + 8u * grp, ov);
-      tmem_wait_ld_tied8(ov);
+      tmem_ld16(tmem + lane_addr + kColO + 32u * wb + 16u * grp, ov);
+      tmem_wait_ld_tied(ov);
       return true;
     };
-    auto store_o = [&](const uint32_t (&ov)[8]) {
+    auto store_o = [&](const uint32_t (&ov)[16]) {
       if (i < n && prev_src >= 0) {
-        const int pb = (int)(prev_it & 1) * 512;
-        const float sum = (xsum[pb + i] + xsum[pb + 128 + i]) + (xsum[pb + 256 + i] + xsum[pb + 384 + i]);
+        const int pb = (int)(prev_it & 1);
+        const float sum = xsum[(pb * 2 + 0) * 128 + i] + xsum[(pb * 2 + 1) * 128 + i];
         const int64_t tok = (int64_t)prev_b * g.tokens + prev_src;
         uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)prev_h * 32 +
-                                              8 * grp);
+                                              16 * grp);
         const float inv = prev_live ? 1.0f / sum : 0.f;
-        *op = make_uint4(pack_bf16(__uint_as_float(ov[0]) * inv, __uint_as_float(ov[1]) * inv),
-                         pack_bf16(__uint_as_float(ov[2]) * inv, __uint_as_float(ov[3]) * inv),
-                         pack_bf16(__uint_as_float(ov[4]) * inv, __uint_as_float(ov[5]) * inv),
-                         pack_bf16(__uint_as_float(ov[6]) * inv, __uint_as_float(ov[7]) * inv));
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16(__uint_as_float(ov[8 * c + 2 * e]) * inv, __uint_as_float(ov[8 * c + 2 * e + 1]) * inv);
+          op[c] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
         if (grp == 0 && a.lse)
           a.lse[((int64_t)prev_b * g.heads + prev_h) * g.tokens + prev_src] =
               prev_live ? (prev_m + __log2f(sum)) * kLn2 : -INFINITY;
@@ -378,18 +376,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     if (count > 0) x.init(g, L);
     for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
       if (x.h != cur_h) {
-        // head change: this thread alone reads its part of bias row i
+        // head change: this thread alone reads this half of bias row i
         int wc0[3] = {0, 0, 0};
         const int rb = (i < n) ? slot_route(g, wc0, i).rbase : 0;
-        for (int k2 = 0; k2 < 2; ++k2) {
-          const int gi = grp + 4 * k2;
-          if (gi >= NG) continue;
-          for (int j = 16 * gi; j < 16 * gi + 16; ++j) {
-            float b = 0.f;
-            if (i < n && j < n && a.bias)
-              b = a.bias[(int64_t)(rb - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
-            brow[j] = b;
-          }
+        for (int j = 16 * gb; j < 16 * ge; ++j) {
+          float b = 0.f;
+          if (i < n && j < n && a.bias) b = a.bias[(int64_t)(rb - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
+          brow[j] = b;
         }
         cur_h = x.h;
       }
@@ -397,68 +390,68 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       const uint32_t tS = tmem + lane_addr + kColS + 128u * wb;
       if (!mbar_wait_warp(bar(bSFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) break;
       tc_fence_after();
-      uint32_t sv[2][16];
+      uint32_t sv[4][16];
 #pragma unroll
-      for (int k2 = 0; k2 < 2; ++k2)
-        if (grp + 4 * k2 < NG) tmem_ld16(tS + 16u * (grp + 4 * k2), sv[k2]);
+      for (int k4 = 0; k4 < 4; ++k4)
+        if (gb + k4 < ge) tmem_ld16(tS + 16u * (gb + k4), sv[k4]);
       if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
       const uint8_t *sp = smem + s * kStageBytes;
       const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
       const bool live = (sp + kMeta + 512)[i] != 0;
       tmem_wait_ld_tied(sv[0], sv[1]);
-      // x = S*cs + bias2 (kept in sv), part row max (independent chains)
-      float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      tmem_wait_ld_tied(sv[2], sv[3]);
+      // x = S*cs + bias2 (kept in sv), half row max
+      float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
 #pragma unroll
-      for (int k2 = 0; k2 < 2; ++k2) {
-        const int gi = grp + 4 * k2;
-        if (gi < NG) {
+      for (int k4 = 0; k4 < 4; ++k4) {
+        if (gb + k4 < ge) {
 #pragma unroll
           for (int e4 = 0; e4 < 16; e4 += 4) {
-            const float4 b4 = *reinterpret_cast<const float4 *>(brow + 16 * gi + e4);
-            const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[k2][e4]), __uint_as_float(sv[k2][e4 + 1])),
+            const float4 b4 = *reinterpret_cast<const float4 *>(brow + 16 * (gb + k4) + e4);
+            const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e4]), __uint_as_float(sv[k4][e4 + 1])),
                                          cs2, make_float2(b4.x, b4.y));
             const float2 x1 = __ffma2_rn(
-                make_float2(__uint_as_float(sv[k2][e4 + 2]), __uint_as_float(sv[k2][e4 + 3])), cs2,
+                make_float2(__uint_as_float(sv[k4][e4 + 2]), __uint_as_float(sv[k4][e4 + 3])), cs2,
                 make_float2(b4.z, b4.w));
-            sv[k2][e4] = __float_as_uint(x0.x);
-            sv[k2][e4 + 1] = __float_as_uint(x0.y);
-            sv[k2][e4 + 2] = __float_as_uint(x1.x);
-            sv[k2][e4 + 3] = __float_as_uint(x1.y);
+            sv[k4][e4] = __float_as_uint(x0.x);
+            sv[k4][e4 + 1] = __float_as_uint(x0.y);
+            sv[k4][e4 + 2] = __float_as_uint(x1.x);
+            sv[k4][e4 + 3] = __float_as_uint(x1.y);
             mp[e4 >> 2] = max3(mp[e4 >> 2], max3(x0.x, x0.y, x1.x), x1.y);
           }
         }
       }
-      const int xb = (int)(it & 1) * 512;
-      xmax[xb + grp * 128 + i] = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+      float m = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+      const int xb = (int)(it & 1) * 256;
+      xmax[xb + grp * 128 + i] = m;
       mbar_arrive_warp(bar(bMax));
       if (!mbar_wait_warp(bar(bMax), (uint32_t)it & 1u, ctl)) break;
-      const float m = fmaxf(fmaxf(xmax[xb + i], xmax[xb + 128 + i]), fmaxf(xmax[xb + 256 + i], xmax[xb + 384 + i]));
-      // p = exp2(x - m), part row sum, P (bf16) over S
+      m = fmaxf(xmax[xb + i], xmax[xb + 128 + i]);
+      // p = exp2(x - m), half row sum, P (bf16) over S
       const float2 negm = make_float2(-m, -m);
       float2 sp2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int k2 = 0; k2 < 2; ++k2) {
-        const int gi = grp + 4 * k2;
-        if (gi < NG) {
+      for (int k4 = 0; k4 < 4; ++k4) {
+        if (gb + k4 < ge) {
           uint32_t pv[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
             const float2 xs =
-                __fadd2_rn(make_float2(__uint_as_float(sv[k2][e]), __uint_as_float(sv[k2][e + 1])), negm);
+                __fadd2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), negm);
             const float2 p = make_float2(ex2(xs.x), ex2(xs.y));
             sp2[(e >> 1) & 3] = __fadd2_rn(sp2[(e >> 1) & 3], p);
             pv[e >> 1] = pack_bf16(p.x, p.y);
           }
-          tmem_st8(tS + 8u * gi, pv);
+          tmem_st8(tS + 8u * (gb + k4), pv);
         }
       }
       const float2 sum2 = __fadd2_rn(__fadd2_rn(sp2[0], sp2[1]), __fadd2_rn(sp2[2], sp2[3]));
       tmem_wait_st();
       // epilogue of the previous item: its PV finished during this softmax;
-      // all parts' sums of it were exchanged before this item's max barrier.
-      uint32_t ov[8];
+      // both halves' sums of it were exchanged before this item's max barrier.
+      uint32_t ov[16];
       if (have_prev && !load_o(ov)) break;
-      xsum[xb + grp * 128 + i] = sum2.x + sum2.y;
+      xsum[((int)(it & 1) * 2 + grp) * 128 + i] = sum2.x + sum2.y;
       tc_fence_before();
       if (have_prev) mbar_arrive_warp(bar(bTFree + (int)(prev_it & 1)));
       mbar_arrive_warp(bar(bPFull + wb));
@@ -472,9 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       prev_m = m;
     }
     if (have_prev && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      // the other parts' sums of the last item: all warpgroups meet once more
+      // the other half's sum of the last item: both warpgroups meet once more
       mbar_arrive_warp(bar(bMax));
-      uint32_t ov[8];
+      uint32_t ov[16];
       if (mbar_wait_warp(bar(bMax), (uint32_t)(prev_it + 1) & 1u, ctl) && load_o(ov)) {
         tc_fence_before();
         mbar_arrive_warp(bar(bTFree + (int)(prev_it & 1)));
@@ -597,17 +590,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
     const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
     const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
-    uint32_t scpack[kRows];  // in-window coordinates of each row, 8 bits per dim
+    SlotCoord scoord[kRows];
 #pragma unroll
     for (int rr = 0; rr < kRows; ++rr) {
       const int row = rq + rr * kRowStep;
-      const SlotCoord c = slot_coord(g, row < n ? row : 0);
-      scpack[rr] = (uint32_t)c.sc[0] | ((uint32_t)c.sc[1] << 8) | ((uint32_t)c.sc[2] << 16);
+      scoord[rr] = slot_coord(g, row < n ? row : 0);
     }
     struct Prep {
       int h, b;
-      int src[kRows];
-      uint32_t flags[kRows];  // region bits | land << 8
+      int src[kRows], reg[kRows];
+      uint8_t land[kRows];
       float lse[kRows];
     };
     auto prep = [&](const ItemCursor &c, Prep &p) {
@@ -616,14 +608,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
         const int row = rq + rr * kRowStep;
-        SlotCoord sc;
-        sc.sc[0] = scpack[rr] & 0xFF;
-        sc.sc[1] = (scpack[rr] >> 8) & 0xFF;
-        sc.sc[2] = scpack[rr] >> 16;
-        const SlotRoute r = (row < n) ? route_slot(g, c.wc, sc) : SlotRoute{-1, 0, 0, 0};
+        const SlotRoute r = (row < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
         p.src[rr] = r.src;
-        const uint32_t land = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : 0u;
-        p.flags[rr] = (uint32_t)r.reg | (land << 8);
+        p.reg[rr] = r.reg;
+        p.land[rr] = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : (uint8_t)0;
         p.lse[rr] = (r.src >= 0) ? __ldg(a.lse + ((int64_t)c.b * g.heads + c.h) * g.tokens + r.src) : 0.f;
       }
     };
@@ -658,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
         const int row = rq + rr * kRowStep;
         if (row < 128) {
           const bool valid = p.src[rr] >= 0;
-          const bool live = valid && !(p.flags[rr] >> 8);
+          const bool live = valid && !p.land[rr];
           const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
           const uint32_t nb = valid ? 16u : 0u;
           cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
@@ -666,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
           cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
           cp_async16(st + kdO + sw64(row, cq), dout + off + 8 * cq, nb);
           *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
-              mask_chunk(live, (int)(p.flags[rr] & 0xFF), cq >= 2, cq & 1);
+              mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
           if (cq == 0) {
             reinterpret_cast<int *>(sp + kMeta)[row] = valid ? p.src[rr] : -1;
             reinterpret_cast<float *>(sp + kMeta + 512)[row] = live ? p.lse[rr] * kLog2e : 0.f;

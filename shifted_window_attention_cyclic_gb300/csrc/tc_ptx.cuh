@@ -186,13 +186,6 @@ __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&a)[8], uint32_t (&b
                : "memory");
 }
 
-__device__ __forceinline__ void tmem_wait_ld_tied8(uint32_t (&a)[8]) {
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7])
-               :
-               : "memory");
-}
-
 // tcgen05.wait::ld that also names the destination registers of the loads it
 // waits for, so the compiler cannot move their first use above the wait.
 __device__ __forceinline__ void tmem_wait_ld_tied(uint32_t (&a)[16], uint32_t (&b)[16]) {
