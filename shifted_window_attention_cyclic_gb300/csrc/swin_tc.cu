@@ -93,12 +93,15 @@ constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
 constexpr int bFull = 0, bEmpty = kStages, bSFull = 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
               bTFree = bOFull + 2, bMax = bTFree + 2, bNever = bMax + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
-constexpr int kXchg = kMiscOff + 16;  // float max[2 items][2 halves][128], sum[2 items][2 halves][128]
-constexpr int kSmemBytes = kXchg + 4096 + 1024;  // + alignment slack
+// per-item exchange slots (double-buffered by item parity): float max[2][2][128],
+// float sum[2][2][128], int src[2][128], int live[2][128]; then int roff[128]
+constexpr int kXchg = kMiscOff + 16;
+constexpr int kRoff = kXchg + 6144;
+constexpr int kSmemBytes = kRoff + 512 + 1024;  // + alignment slack
 
 // warps 0-7: two softmax warpgroups, each owning half of every row's columns;
-// 8-10: gather; 11: MMA
-constexpr int kSoftmaxWarps = 8, kProducerWarp0 = 8, kMmaWarp = 11;
+// 8-11: epilogue; 12-14: gather; 15: MMA
+constexpr int kSoftmaxWarps = 8, kEpilogueWarp0 = 8, kProducerWarp0 = 12, kMmaWarp = 15;
 constexpr int kProducerThreads = (kMmaWarp - kProducerWarp0) * 32;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
 // TMEM columns: S/P of warpgroup w at 128*w, O of warpgroup w at 256 + 32*w
@@ -130,13 +133,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       mbar_init(bar(bSFull + w), 1);
       mbar_init(bar(bPFull + w), kSoftmaxWarps);
       mbar_init(bar(bOFull + w), 1);
-      mbar_init(bar(bTFree + w), kSoftmaxWarps);
+      mbar_init(bar(bTFree + w), 4);  // epilogue warps
     }
     mbar_init(bar(bMax), kSoftmaxWarps);
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  {
+    // key side of every slot's bias row offset, for the bias-row builds
+    int *roff = reinterpret_cast<int *>(smem + kRoff);
+    int wc0[3] = {0, 0, 0};
+    if (threadIdx.x < 128) roff[threadIdx.x] = threadIdx.x < n ? slot_route(g, wc0, threadIdx.x).roff : 0;
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -295,8 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
           idle_since = 0;
           continue;
         }
-        __nanosleep(32);  // leave the issue slots to the softmax warps of this SMSP
-        if ((++spins & 63u) == 0) {
+        // nothing ready: sleep on the barrier most likely to complete next
+        // (woken at its completion, or after a short hint)
+        if (npv < ns)
+          mbar_try_wait_hint(bar(bPFull + (int)(npv & 1)), (uint32_t)(npv >> 1) & 1u, 256);
+        else if (ns < count)
+          mbar_try_wait_hint(bar(bFull + (int)(ns % kStages)), (uint32_t)(ns / kStages) & 1u, 256);
+        if ((++spins & 15u) == 0) {
           if (*abort_flag) break;
           const uint64_t now = globaltimer();
           if (idle_since == 0) {
@@ -315,78 +329,91 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       mbar_wait(bar(bDrain), 0, drain_ctl);
     }
     __syncwarp();
+  } else if (warp >= kEpilogueWarp0) {
+    // ---------------------------------------------------------- epilogue ---
+    // Per item: O row i (32 fp32 columns of TMEM lane i) divided by the row
+    // sum, rounded to bf16 and stored at the slot's grid token (the reverse
+    // route); the log-sum-exp (m + log2 sum) * ln 2; land rows store zeros.
+    const int q4 = warp & 3, i = q4 * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    const float *xmax = reinterpret_cast<const float *>(smem + kXchg);
+    const float *xsum = xmax + 512;
+    const int *xsrc = reinterpret_cast<const int *>(xmax + 1024);
+    const int *xlive = xsrc + 256;
+    ItemCursor x;
+    if (count > 0) x.init(g, L);
+    for (int64_t it = 0; it < count; ++it, x.next(g)) {
+      const int wb = (int)(it & 1), xb = (int)(it & 1);
+      if (!mbar_wait_warp(bar(bOFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) break;
+      tc_fence_after();
+      uint32_t lo[16], hi[16];
+      tmem_ld16(tmem + lane_addr + kColO + 32u * wb, lo);
+      tmem_ld16(tmem + lane_addr + kColO + 32u * wb + 16, hi);
+      const float m = fmaxf(xmax[xb * 256 + i], xmax[xb * 256 + 128 + i]);
+      const float sum = xsum[xb * 256 + i] + xsum[xb * 256 + 128 + i];
+      const int src = xsrc[xb * 128 + i];
+      const bool live = xlive[xb * 128 + i] != 0;
+      tmem_wait_ld_tied(lo, hi);
+      tc_fence_before();
+      mbar_arrive_warp(bar(bTFree + wb));
+      if (i < n && src >= 0) {
+        const int64_t tok = (int64_t)x.b * g.tokens + src;
+        uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)x.h * 32);
+        const float inv = live ? __frcp_rn(sum) : 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t *v16 = c < 2 ? lo : hi;
+          const int o = (c & 1) * 8;
+          op[c] = make_uint4(pack_bf16(__uint_as_float(v16[o + 0]) * inv, __uint_as_float(v16[o + 1]) * inv),
+                             pack_bf16(__uint_as_float(v16[o + 2]) * inv, __uint_as_float(v16[o + 3]) * inv),
+                             pack_bf16(__uint_as_float(v16[o + 4]) * inv, __uint_as_float(v16[o + 5]) * inv),
+                             pack_bf16(__uint_as_float(v16[o + 6]) * inv, __uint_as_float(v16[o + 7]) * inv));
+        }
+        if (a.lse)
+          a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m + __log2f(sum)) * kLn2 : -INFINITY;
+      }
+    }
+    tmem_wait_ld();
   } else {
     // ----------------------------------------------------------- softmax ---
-    // Thread (grp, i): TMEM lane i (query slot i), columns of 16-column groups
-    // [gb, ge) of the item's S row, loaded into registers with one wait.
+    // Thread (grp, i): TMEM lane i (query slot i), 16-column groups [gb, ge)
+    // of the item's S row, loaded into registers with one wait.
     // x = S*scale*log2e + bias*log2e (this half of bias row i, in smem), half
     // row max -> exchanged -> row max m; p = exp2(x - m) -> P (bf16) over S;
-    // half row sums are exchanged for the epilogue. The epilogue of the
-    // previous item (its O row half normalised and stored at the grid token;
-    // the log-sum-exp) runs after this item's P is written, so the PV of the
-    // previous item is hidden behind this item's softmax.
+    // half row sums, the row max and the slot's token go to the item's
+    // exchange slot for the epilogue warps.
     const int grp = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane;
     const int ng0 = (NG + 1) >> 1, gb = grp ? ng0 : 0, ge = grp ? NG : ng0;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     float *brow = reinterpret_cast<float *>(smem + kBias) + i * kBiasStride;
-    // exchange slots, double-buffered by item parity: a warpgroup can only
-    // rewrite a slot after the other one passed the next max barrier
-    float *xmax = reinterpret_cast<float *>(smem + kXchg);         // [2][2][128]
-    float *xsum = reinterpret_cast<float *>(smem + kXchg + 2048);  // [2][2][128]
+    float *xmax = reinterpret_cast<float *>(smem + kXchg);  // [2][2][128]
+    float *xsum = xmax + 512;                                // [2][2][128]
+    int *xsrc = reinterpret_cast<int *>(xmax + 1024);        // [2][128]
+    int *xlive = xsrc + 256;                                 // [2][128]
+    const int *roff = reinterpret_cast<const int *>(smem + kRoff);
     const float cs = a.scale * kLog2e;
     const float2 cs2 = make_float2(cs, cs);
+    int wc0[3] = {0, 0, 0};
+    const int rbase = (i < n) ? slot_route(g, wc0, i).rbase : 0;
     int cur_h = -1;
     bool ok = true;
-    // deferred epilogue state of the previous item
-    bool have_prev = false, prev_live = false;
-    int prev_src = -1, prev_b = 0, prev_h = 0;
-    int64_t prev_it = 0;
-    float prev_m = 0.f;
-    auto load_o = [&](uint32_t (&ov)[16]) -> bool {
-      const int wb = (int)(prev_it & 1);
-      if (!mbar_wait_warp(bar(bOFull + wb), (uint32_t)(prev_it >> 1) & 1u, ctl)) return false;
-      tc_fence_after();
-      tmem_ld16(tmem + lane_addr + kColO + 32u * wb + 16u * grp, ov);
-      tmem_wait_ld_tied(ov);
-      return true;
-    };
-    auto store_o = [&](const uint32_t (&ov)[16]) {
-      if (i < n && prev_src >= 0) {
-        const int pb = (int)(prev_it & 1);
-        const float sum = xsum[(pb * 2 + 0) * 128 + i] + xsum[(pb * 2 + 1) * 128 + i];
-        const int64_t tok = (int64_t)prev_b * g.tokens + prev_src;
-        uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)prev_h * 32 +
-                                              16 * grp);
-        const float inv = prev_live ? 1.0f / sum : 0.f;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16(__uint_as_float(ov[8 * c + 2 * e]) * inv, __uint_as_float(ov[8 * c + 2 * e + 1]) * inv);
-          op[c] = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        if (grp == 0 && a.lse)
-          a.lse[((int64_t)prev_b * g.heads + prev_h) * g.tokens + prev_src] =
-              prev_live ? (prev_m + __log2f(sum)) * kLn2 : -INFINITY;
-      }
-    };
     if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
     ItemCursor x;
     if (count > 0) x.init(g, L);
     for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
       if (x.h != cur_h) {
-        // head change: this thread alone reads this half of bias row i
-        int wc0[3] = {0, 0, 0};
-        const int rb = (i < n) ? slot_route(g, wc0, i).rbase : 0;
-        for (int j = 16 * gb; j < 16 * ge; ++j) {
-          float b = 0.f;
-          if (i < n && j < n && a.bias) b = a.bias[(int64_t)(rb - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
-          brow[j] = b;
+        // head change: this thread alone reads this half of bias row i; the
+        // loads are independent so their latencies overlap
+        const float *bcol = a.bias ? a.bias + x.h : nullptr;
+#pragma unroll 16
+        for (int jj = 0; jj < 64; ++jj) {
+          const int j = 16 * gb + jj;
+          if (j < 16 * ge)
+            brow[j] = (bcol && i < n && j < n) ? __ldg(bcol + (int64_t)(rbase - roff[j]) * g.heads) * kLog2e : 0.f;
         }
         cur_h = x.h;
       }
-      const int wb = (int)(it & 1), s = (int)(it % kStages);
+      const int wb = (int)(it & 1), s = (int)(it % kStages), xb = (int)(it & 1);
       const uint32_t tS = tmem + lane_addr + kColS + 128u * wb;
       if (!mbar_wait_warp(bar(bSFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) break;
       tc_fence_after();
@@ -398,10 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       const uint8_t *sp = smem + s * kStageBytes;
       const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
       const bool live = (sp + kMeta + 512)[i] != 0;
+      // the epilogue warps are done with this exchange slot (item it - 2)
+      if (it >= 2 && !mbar_wait_warp(bar(bTFree + wb), (uint32_t)((it >> 1) - 1) & 1u, ctl)) break;
       tmem_wait_ld_tied(sv[0], sv[1]);
       tmem_wait_ld_tied(sv[2], sv[3]);
-      // x = S*cs + bias2 (kept in sv), half row max
-      float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // independent chains
+      // x = S*cs + bias2 (kept in sv), half row max (independent chains)
+      float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4) {
         if (gb + k4 < ge) {
@@ -421,12 +450,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
           }
         }
       }
-      float m = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
-      const int xb = (int)(it & 1) * 256;
-      xmax[xb + grp * 128 + i] = m;
+      xmax[xb * 256 + grp * 128 + i] = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
+      if (grp == 0) {
+        xsrc[xb * 128 + i] = src;
+        xlive[xb * 128 + i] = live ? 1 : 0;
+      }
       mbar_arrive_warp(bar(bMax));
       if (!mbar_wait_warp(bar(bMax), (uint32_t)it & 1u, ctl)) break;
-      m = fmaxf(xmax[xb + i], xmax[xb + 128 + i]);
+      const float m = fmaxf(xmax[xb * 256 + i], xmax[xb * 256 + 128 + i]);
       // p = exp2(x - m), half row sum, P (bf16) over S
       const float2 negm = make_float2(-m, -m);
       float2 sp2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -446,33 +477,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         }
       }
       const float2 sum2 = __fadd2_rn(__fadd2_rn(sp2[0], sp2[1]), __fadd2_rn(sp2[2], sp2[3]));
+      xsum[xb * 256 + grp * 128 + i] = sum2.x + sum2.y;
       tmem_wait_st();
-      // epilogue of the previous item: its PV finished during this softmax;
-      // both halves' sums of it were exchanged before this item's max barrier.
-      uint32_t ov[16];
-      if (have_prev && !load_o(ov)) break;
-      xsum[((int)(it & 1) * 2 + grp) * 128 + i] = sum2.x + sum2.y;
       tc_fence_before();
-      if (have_prev) mbar_arrive_warp(bar(bTFree + (int)(prev_it & 1)));
       mbar_arrive_warp(bar(bPFull + wb));
-      if (have_prev) store_o(ov);
-      have_prev = true;
-      prev_live = live;
-      prev_src = src;
-      prev_b = x.b;
-      prev_h = x.h;
-      prev_it = it;
-      prev_m = m;
-    }
-    if (have_prev && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      // the other half's sum of the last item: both warpgroups meet once more
-      mbar_arrive_warp(bar(bMax));
-      uint32_t ov[16];
-      if (mbar_wait_warp(bar(bMax), (uint32_t)(prev_it + 1) & 1u, ctl) && load_o(ov)) {
-        tc_fence_before();
-        mbar_arrive_warp(bar(bTFree + (int)(prev_it & 1)));
-        store_o(ov);
-      }
     }
     tmem_wait_st();
     tmem_wait_ld();

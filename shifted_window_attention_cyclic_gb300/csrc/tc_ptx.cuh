@@ -64,6 +64,20 @@ __device__ __forceinline__ void mbar_arrive_warp(uint32_t bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// Blocking probe with a suspend-time hint: the thread sleeps until the phase
+// completes (it is woken then) or about `hint_ns` passes.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded-wait control: every spin ends either when the phase completes, when
 // another role of the CTA has raised the abort flag, or when `limit_ns` has
 // passed (then this thread raises the abort flag and the device status word).
