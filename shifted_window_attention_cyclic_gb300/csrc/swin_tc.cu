@@ -22,8 +22,12 @@
 // Every wait is bounded (globaltimer); on timeout the CTA raises an abort
 // flag, every role leaves its loop, copies and MMAs in flight are drained,
 // TMEM is freed and the device status word reports a timeout.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "swin_tc.cuh"
 #include "tc_ptx.cuh"
@@ -107,7 +111,9 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;
 // TMEM columns: S/P of warpgroup w at 128*w, O of warpgroup w at 256 + 32*w
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
-__global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -147,6 +153,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
     int wc0[3] = {0, 0, 0};
     if (threadIdx.x < 128) roff[threadIdx.x] = threadIdx.x < n ? slot_route(g, wc0, threadIdx.x).roff : 0;
   }
+  // stage tiles start zeroed: box loads fill only the window's rows, and rows
+  // past the last slot must stay finite for the MMAs
+  for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
+    reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -218,6 +229,19 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
       const uint32_t st = sbase + s * kStageBytes;
       uint8_t *sp = smem + s * kStageBytes;
       const Prep &p = pc;
+      // A window that neither wraps nor has pads in any dim is one box of the
+      // grid tensor: one TMA load per tensor from an elected thread, counted
+      // as transaction bytes on full[s]; other windows take the row gather.
+      bool box = true;
+#pragma unroll
+      for (int d = 0; d < 3; ++d) box = box && cur.wc[d] * g.w[d] + g.w[d] + g.s[d] <= g.G[d];
+      if (box && pt == 0) {
+        mbar_expect_tx(bar(bFull + s), (uint32_t)(3 * n * 64));
+        const int c0 = cur.wc[0] * g.w[0] + g.s[0], c1 = cur.wc[1] * g.w[1] + g.s[1], c2 = cur.wc[2] * g.w[2] + g.s[2];
+        tma_load_5d(st + kQ, &tmq, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
+        tma_load_5d(st + kK, &tmk, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
+        tma_load_5d(st + kV, &tmv, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
+      }
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
         const int row = rq + rr * kRowStep;
@@ -226,9 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
           const bool live = valid && !p.land[rr];
           const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
           const uint32_t nb = valid ? 16u : 0u;
-          cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
-          cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
-          cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
+          if (!box) {
+            cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
+            cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
+            cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
+          }
           *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
               mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
           if (cq == 0) {
@@ -306,10 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_tc_kernel(const FwdArgs a) {
         }
         // nothing ready: sleep on the barrier most likely to complete next
         // (woken at its completion, or after a short hint)
-        if (npv < ns)
-          mbar_try_wait_hint(bar(bPFull + (int)(npv & 1)), (uint32_t)(npv >> 1) & 1u, 256);
-        else if (ns < count)
-          mbar_try_wait_hint(bar(bFull + (int)(ns % kStages)), (uint32_t)(ns / kStages) & 1u, 256);
+        if (ns < count && ns <= npv + 1)
+          mbar_try_wait_hint(bar(bFull + (int)(ns % kStages)), (uint32_t)(ns / kStages) & 1u, 64);
+        else if (npv < ns)
+          mbar_try_wait_hint(bar(bPFull + (int)(npv & 1)), (uint32_t)(npv >> 1) & 1u, 64);
         if ((++spins & 15u) == 0) {
           if (*abort_flag) break;
           const uint64_t now = globaltimer();
@@ -540,7 +566,9 @@ __device__ __forceinline__ uint32_t pds_chunk(int i, int c) {
   return (c >> 3) * 16384 + (i >> 3) * 1024 + (i & 7) * 128 + (((c & 7) ^ (i & 7)) << 4);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -575,6 +603,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
     *abort_flag = 0;
     fence_mbar_init();
   }
+  // stage tiles start zeroed: box loads fill only the window's rows, and rows
+  // past the last slot must stay finite for the MMAs
+  for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
+    reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -649,6 +682,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
       const uint32_t st = sbase + s * kStageBytes;
       uint8_t *sp = smem + s * kStageBytes;
       const Prep &p = pc;
+      // A window that neither wraps nor has pads in any dim is one box of the
+      // grid tensor: one TMA load per tensor from an elected thread, counted
+      // as transaction bytes on full[s]; other windows take the row gather.
+      bool box = true;
+#pragma unroll
+      for (int d = 0; d < 3; ++d) box = box && cur.wc[d] * g.w[d] + g.w[d] + g.s[d] <= g.G[d];
+      if (box && pt == 0) {
+        mbar_expect_tx(bar(bFull + s), (uint32_t)(4 * n * 64));
+        const int c0 = cur.wc[0] * g.w[0] + g.s[0], c1 = cur.wc[1] * g.w[1] + g.s[1], c2 = cur.wc[2] * g.w[2] + g.s[2];
+        tma_load_5d(st + kQ, &tmq, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
+        tma_load_5d(st + kK, &tmk, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
+        tma_load_5d(st + kV, &tmv, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
+        tma_load_5d(st + kdO, &tmdo, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
+      }
 #pragma unroll
       for (int rr = 0; rr < kRows; ++rr) {
         const int row = rq + rr * kRowStep;
@@ -657,10 +704,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_kernel(const BwdArgs a) {
           const bool live = valid && !p.land[rr];
           const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
           const uint32_t nb = valid ? 16u : 0u;
-          cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
-          cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
-          cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
-          cp_async16(st + kdO + sw64(row, cq), dout + off + 8 * cq, nb);
+          if (!box) {
+            cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
+            cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
+            cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
+            cp_async16(st + kdO + sw64(row, cq), dout + off + 8 * cq, nb);
+          }
           *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
               mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
           if (cq == 0) {
@@ -993,19 +1042,63 @@ bool tc_supported(const Geo &g, int dtype) { return dtype == SWIN_BF16 && g.hd =
 int tc_fwd_ctas_per_sm(const Geo &) { return 1; }
 int tc_bwd_ctas_per_sm(const Geo &) { return 1; }
 
+namespace {
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Tiled map of a [B, G0, G1, G2, C] bf16 tensor whose box is one window of
+// one head: (32 channels, w2, w1, w0, 1), 64-byte swizzle (the layout of the
+// kernels' operand tiles).
+bool window_tensor_map(CUtensorMap *m, const void *base, const Geo &g) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t e = 2;
+  cuuint64_t dims[5] = {(cuuint64_t)g.C, (cuuint64_t)g.G[2], (cuuint64_t)g.G[1], (cuuint64_t)g.G[0],
+                        (cuuint64_t)g.batch};
+  cuuint64_t strides[4] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e,
+                           dims[0] * dims[1] * dims[2] * dims[3] * e};
+  cuuint32_t box[5] = {32u, (cuuint32_t)g.w[2], (cuuint32_t)g.w[1], (cuuint32_t)g.w[0], 1u};
+  cuuint32_t es[5] = {1u, 1u, 1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 int launch_fwd_tc(const FwdArgs &a, void *stream) {
+  CUtensorMap mq, mk, mv;
+  if (!window_tensor_map(&mq, a.q, a.g) || !window_tensor_map(&mk, a.k, a.g) || !window_tensor_map(&mv, a.v, a.g))
+    return SWIN_ERR_CUDA;
   auto kern = fwd::fwd_tc_kernel;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmemBytes) != cudaSuccess)
     return SWIN_ERR_CUDA;
-  kern<<<a.ctas, fwd::kThreads, fwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
+  kern<<<a.ctas, fwd::kThreads, fwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mk, mv);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
 }
 
 int launch_bwd_tc(const BwdArgs &a, void *stream) {
+  CUtensorMap mq, mk, mv, mdo;
+  if (!window_tensor_map(&mq, a.q, a.g) || !window_tensor_map(&mk, a.k, a.g) || !window_tensor_map(&mv, a.v, a.g) ||
+      !window_tensor_map(&mdo, a.dout, a.g))
+    return SWIN_ERR_CUDA;
   auto kern = bwd::bwd_tc_kernel;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmemBytes) != cudaSuccess)
     return SWIN_ERR_CUDA;
-  kern<<<a.ctas, bwd::kThreads, bwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a);
+  kern<<<a.ctas, bwd::kThreads, bwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mk, mv, mdo);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
 }
 
