@@ -42,19 +42,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr uint16_t kBf16One = 0x3F80;   // 1.0
 constexpr uint16_t kBf16NegBig = 0xF180;  // -2^100
 
-// Swizzled byte offsets inside a tile (16-byte chunk c of row r).
-__device__ __forceinline__ uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
+// Swizzled byte offset of 16-byte chunk c of row r in a 32-byte-row mask tile.
 __device__ __forceinline__ uint32_t sw32(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
 
 __device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
-
-// What a gather thread knows about its slot of one item before the copies.
-struct SlotPrep {
-  int h, src, reg;
-  int64_t tok;
-  uint8_t land;
-  float lse;
-};
 
 // One 16-byte chunk (columns 8*half .. 8*half+7) of a slot's mask row:
 // key = false gives the Qm row, key = true the Km row (see below).
@@ -75,16 +66,156 @@ __device__ __forceinline__ uint4 mask_chunk(bool live, int reg, bool key, int ha
 // queries only); Km = 0 in the column of the key's region if the key is live,
 // -2^100 everywhere else. Qm Km^T then adds -2^100 to every masked logit.
 
+// Where one item's mask rows and slot metadata sit in a stage (the operand
+// tiles, 128 slot rows x 64 B with 64-byte swizzle, are passed per warp).
+struct StageLayout {
+  uint32_t bytes;            // stage stride
+  uint32_t qm, km;           // mask tiles: 128 rows x 32 B, 32-byte swizzle
+  uint32_t src, live, lse2;  // int src[128], uint8 live[128], float lse*log2e[128]
+};
+
+// The two TMA views of one [B, G0, G1, G2, C] bf16 tensor that the gather
+// warps load from (one head's 32 channels, 64-byte swizzle).
+struct TmaSet {
+  CUtensorMap box;   // a whole window: (32, w2, w1, w0, 1)
+  CUtensorMap rows;  // the [B*T, C] row view for gather4: (32, 1)
+};
+
+// Gather warps (three). Lane l of every warp routes slots 4l .. 4l+3 of the
+// next item one item ahead and loads their land bytes (and, for the warp that
+// writes them, their log-sum-exps), so that those loads are in flight while
+// the current item is issued.
+// Warp w brings in the tiles of tensors w and w + 3 (when there are four),
+// by TMA only. A window that neither wraps nor pads in any dim is one box
+// (lane 0 loads it); any other window is gathered by rows: lane l fetches
+// the rows of its own four slots with one gather4, pads reading token 0 of
+// the image, which the masks discard. Nothing here waits on a copy:
+// completion is counted in transaction bytes on the stage's full barrier. Warp 0 writes the slot metadata, warp 1 the query mask rows
+// (Qm) and warp 2 the key mask rows (Km).
+template <int kStages>
+__device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay, int ntiles, uint32_t tile_a,
+                                            uint32_t tile_b, const TmaSet *ma, const TmaSet *mb,
+                                            const uint8_t *land, const float *lse, uint8_t *smem, uint32_t sbase,
+                                            uint32_t full0, uint32_t empty0, const WaitCtl &ctl, int64_t L,
+                                            int64_t count, int pw, int lane) {
+  const int n = g.n, nq4 = (n + 3) >> 2;
+  SlotCoord sc[4];
+  int foff[4];  // token offset of slot 4l + j from the window's origin when the window is a box
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int slot = 4 * lane + j;
+    sc[j] = slot_coord(g, slot < n ? slot : 0);
+    foff[j] = (sc[j].sc[0] * g.G[1] + sc[j].sc[1]) * g.G[2] + sc[j].sc[2];
+  }
+  struct Prep {
+    int h, b, c[3];  // c: the window's first grid coordinate in each dim (a box's corner)
+    bool box;
+    int src[4];
+    uint32_t reg4;
+    uint32_t land[4];  // raw bytes: consumed one item later
+    float lse[4];
+  };
+  auto prep = [&](const ItemCursor &cu, Prep &p) {
+    p.h = cu.h;
+    p.b = cu.b;
+    p.box = true;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      p.c[d] = cu.wc[d] * g.w[d] + g.s[d];
+      p.box = p.box && p.c[d] + g.w[d] <= g.G[d];
+    }
+    const int org = (p.c[0] * g.G[1] + p.c[1]) * g.G[2] + p.c[2];
+    const int64_t tok0 = (int64_t)cu.b * g.tokens;
+    p.reg4 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int src = -1, reg = 0;
+      if (4 * lane + j < n) {
+        if (p.box) {
+          src = org + foff[j];
+        } else {
+          const SlotRoute r = route_slot(g, cu.wc, sc[j]);
+          src = r.src;
+          reg = r.reg;
+        }
+      }
+      p.src[j] = src;
+      p.reg4 |= (uint32_t)reg << (8 * j);
+      p.land[j] = (src >= 0 && land) ? __ldg(land + tok0 + src) : 0u;
+      if (lse) p.lse[j] = src >= 0 ? __ldg(lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens + src) : 0.f;
+    }
+  };
+  ItemCursor cur;
+  Prep pc, pn;
+  if (count > 0) {
+    cur.init(g, L);
+    prep(cur, pc);
+  }
+  int64_t it = 0;
+  for (; it < count; ++it) {
+    const int s = (int)(it % kStages);
+    ItemCursor nx = cur;
+    nx.next(g);
+    if (it + 1 < count) prep(nx, pn);
+    if (it >= kStages && !mbar_wait_warp(empty0 + 8u * s, (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+    const uint32_t st = sbase + s * lay.bytes, full = full0 + 8u * s;
+    uint8_t *sp = smem + s * lay.bytes;
+    const Prep &p = pc;
+    if (lane == 0) mbar_expect_tx(full, (uint32_t)(ntiles * (p.box ? n * 64 : nq4 * 256)));
+    __syncwarp();
+    const int x = p.h * 32;
+    if (p.box) {
+      if (lane == 0) {
+        tma_load_5d(st + tile_a, &ma->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
+        if (ntiles > 1) tma_load_5d(st + tile_b, &mb->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
+      }
+    } else if (lane < nq4) {
+      const int r0 = p.b * g.tokens;  // row of token 0 of the image in the [B*T, C] view
+      const int r[4] = {r0 + max(p.src[0], 0), r0 + max(p.src[1], 0), r0 + max(p.src[2], 0), r0 + max(p.src[3], 0)};
+      tma_gather4(st + tile_a + 256u * lane, &ma->rows, x, r[0], r[1], r[2], r[3], full);
+      if (ntiles > 1) tma_gather4(st + tile_b + 256u * lane, &mb->rows, x, r[0], r[1], r[2], r[3], full);
+    }
+    bool live[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) live[j] = p.src[j] >= 0 && p.land[j] == 0;
+    if (pw == 0) {
+      *reinterpret_cast<int4 *>(sp + lay.src + 16 * lane) = make_int4(p.src[0], p.src[1], p.src[2], p.src[3]);
+      *reinterpret_cast<uint32_t *>(sp + lay.live + 4 * lane) =
+          (live[0] ? 1u : 0u) | (live[1] ? 0x100u : 0u) | (live[2] ? 0x10000u : 0u) | (live[3] ? 0x1000000u : 0u);
+      if (lse)
+        *reinterpret_cast<float4 *>(sp + lay.lse2 + 16 * lane) =
+            make_float4(live[0] ? p.lse[0] * kLog2e : 0.f, live[1] ? p.lse[1] * kLog2e : 0.f,
+                        live[2] ? p.lse[2] * kLog2e : 0.f, live[3] ? p.lse[3] * kLog2e : 0.f);
+    } else {
+      const bool key = pw == 2;
+      const uint32_t mt = key ? lay.km : lay.qm;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int slot = 4 * lane + j;
+        if (slot < n) {
+          const int reg = (int)((p.reg4 >> (8 * j)) & 0xffu);
+          *reinterpret_cast<uint4 *>(sp + mt + sw32(slot, 0)) = mask_chunk(live[j], reg, key, 0);
+          *reinterpret_cast<uint4 *>(sp + mt + sw32(slot, 1)) = mask_chunk(live[j], reg, key, 1);
+        }
+      }
+    }
+    fence_proxy_async_smem();  // mask rows are read by the tensor cores
+    mbar_arrive_warp(full);
+    cur = nx;
+    pc = pn;
+  }
+  // Copies still in flight must land before the CTA exits. Unless a role gave
+  // up early these stages were consumed already and the waits return at once.
+  volatile int no_abort = 0;
+  const WaitCtl dctl{&no_abort, ctl.status, ctl.limit_ns < 50000000ull ? ctl.limit_ns : 50000000ull};
+  for (int64_t k = it > kStages ? it - kStages : 0; k < it; ++k)
+    mbar_wait_warp(full0 + 8u * (uint32_t)(k % kStages), (uint32_t)(k / kStages) & 1u, dctl);
+}
+
 // ---------------------------------------------------------------- forward ---
 namespace fwd {
 
 constexpr int kStages = 4;
-constexpr int kAhead = 1;  // items whose copies stay in flight unannounced
-// The MMA thread issues S(k) only after PV(k-2), so freeing stage s(it) (PV
-// of item it - kStages) needs items up to it - kStages + 2 announced; with
-// kAhead <= kStages - 2 the gather warps may block on empty[] while still
-// holding kAhead unannounced items.
-constexpr bool kFlushBeforeBlock = kAhead > kStages - 2;
 constexpr int kTileBytes = 128 * 64;  // 128 slot rows x 32 bf16
 constexpr int kMaskBytes = 128 * 32;  // 128 rows x 16 bf16
 constexpr int kQ = 0, kK = kTileBytes, kV = 2 * kTileBytes, kQm = 3 * kTileBytes, kKm = kQm + kMaskBytes;
@@ -112,8 +243,8 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
 __global__ void __launch_bounds__(kThreads, 1)
-    fwd_tc_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv) {
+    fwd_tc_kernel(const FwdArgs a, const __grid_constant__ TmaSet tmq, const __grid_constant__ TmaSet tmk,
+                  const __grid_constant__ TmaSet tmv) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -157,6 +288,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // past the last slot must stay finite for the MMAs
   for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
     reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  // slot rows past the window (n..127) are pads for every item: key mask
+  // -2^100 in every column, no token
+  for (int z = threadIdx.x; z < kStages * 128; z += blockDim.x) {
+    const int st = z / 128, row = z % 128;
+    if (row >= n) {
+      const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
+      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 0)) = make_uint4(nb2, nb2, nb2, nb2);
+      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
+      reinterpret_cast<int *>(smem + st * kStageBytes + kMeta)[row] = -1;
+    }
+  }
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -169,116 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kProducerWarp0 && warp < kMmaWarp) {
     // ------------------------------------------------------------ gather ---
-    // Four consecutive threads gather one slot row: thread quad rq takes rows
-    // rq, rq + 24, rq + 48, ...; lane cq copies 16-byte chunk cq of the row's
-    // 64 bytes (one request of two full sectors per row and tensor). The
-    // route and land byte of the next item are prepared one item ahead.
-    const int pt = threadIdx.x - kProducerWarp0 * 32;
-    const int cq = pt & 3, rq = pt >> 2;
-    constexpr int kRowStep = kProducerThreads / 4;
-    constexpr int kRows = (128 + kRowStep - 1) / kRowStep;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    SlotCoord scoord[kRows];
-#pragma unroll
-    for (int rr = 0; rr < kRows; ++rr) {
-      const int row = rq + rr * kRowStep;
-      scoord[rr] = slot_coord(g, row < n ? row : 0);
-    }
-    struct Prep {
-      int h, b;
-      int src[kRows], reg[kRows];
-      uint8_t land[kRows];
-    };
-    auto prep = [&](const ItemCursor &c, Prep &p) {
-      p.h = c.h;
-      p.b = c.b;
-#pragma unroll
-      for (int rr = 0; rr < kRows; ++rr) {
-        const int row = rq + rr * kRowStep;
-        const SlotRoute r = (row < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
-        p.src[rr] = r.src;
-        p.reg[rr] = r.reg;
-        p.land[rr] = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : (uint8_t)0;
-      }
-    };
-    ItemCursor cur;
-    Prep pc, pn;
-    if (count > 0) {
-      cur.init(g, L);
-      prep(cur, pc);
-    }
-    int64_t pending = -1;
-    for (int64_t it = 0; it < count; ++it) {
-      const int s = (int)(it % kStages);
-      ItemCursor nx = cur;
-      nx.next(g);
-      if (it + 1 < count) prep(nx, pn);
-      if (it >= kStages) {
-        const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (kFlushBeforeBlock && !__all_sync(0xffffffffu, mbar_test(bar(bEmpty + s), par))) {
-          // about to block: announce everything still pending first
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          for (; pending >= 0 && pending < it; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
-          pending = -1;
-        }
-        if (!mbar_wait_warp(bar(bEmpty + s), par, ctl)) break;
-      }
-      const uint32_t st = sbase + s * kStageBytes;
-      uint8_t *sp = smem + s * kStageBytes;
-      const Prep &p = pc;
-      // A window that neither wraps nor has pads in any dim is one box of the
-      // grid tensor: one TMA load per tensor from an elected thread, counted
-      // as transaction bytes on full[s]; other windows take the row gather.
-      bool box = true;
-#pragma unroll
-      for (int d = 0; d < 3; ++d) box = box && cur.wc[d] * g.w[d] + g.w[d] + g.s[d] <= g.G[d];
-      if (box && pt == 0) {
-        mbar_expect_tx(bar(bFull + s), (uint32_t)(3 * n * 64));
-        const int c0 = cur.wc[0] * g.w[0] + g.s[0], c1 = cur.wc[1] * g.w[1] + g.s[1], c2 = cur.wc[2] * g.w[2] + g.s[2];
-        tma_load_5d(st + kQ, &tmq, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
-        tma_load_5d(st + kK, &tmk, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
-        tma_load_5d(st + kV, &tmv, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
-      }
-#pragma unroll
-      for (int rr = 0; rr < kRows; ++rr) {
-        const int row = rq + rr * kRowStep;
-        if (row < 128) {
-          const bool valid = p.src[rr] >= 0;
-          const bool live = valid && !p.land[rr];
-          const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
-          const uint32_t nb = valid ? 16u : 0u;
-          if (!box) {
-            cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
-            cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
-            cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
-          }
-          *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
-              mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
-          if (cq == 0) {
-            reinterpret_cast<int *>(sp + kMeta)[row] = valid ? p.src[rr] : -1;
-            (sp + kMeta + 512)[row] = live ? 1 : 0;
-          }
-        }
-      }
-      cp_async_commit();
-      if (pending < 0) pending = it;
-      if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
-        cp_async_wait<kAhead>();
-        fence_proxy_async_smem();
-        mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
-        ++pending;
-      }
-      cur = nx;
-      pc = pn;
-    }
-    cp_async_wait_all();
-    if (pending >= 0 && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      fence_proxy_async_smem();
-      for (; pending < count; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
-    }
+    const int pw = warp - kProducerWarp0;
+    const StageLayout lay{kStageBytes, kQm, kKm, kMeta, kMeta + 512, 0};
+    gather_role<kStages>(g, lay, 1, pw == 0 ? kQ : pw == 1 ? kK : kV, 0, pw == 0 ? &tmq : pw == 1 ? &tmk : &tmv,
+                         nullptr, g.has_land ? a.land : nullptr, nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl,
+                         L, count, pw, lane);
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     // Event loop: S(k) is issued as soon as its data has landed and PV(k-2)
@@ -533,10 +571,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace bwd {
 
 constexpr int kStages = 2;
-constexpr int kAhead = 1;
-// dK/dQ(it-2), which frees stage s(it), are issued after S(it-1): item it-1
-// must be announced before the gather warps block on empty[].
-constexpr bool kFlushBeforeBlock = true;
 constexpr int kTile = 128 * 64, kMask = 128 * 32;
 constexpr int kQ = 0, kK = kTile, kV = 2 * kTile, kdO = 3 * kTile, kQm = 4 * kTile, kKm = kQm + kMask;
 constexpr int kMeta = kKm + kMask;  // int32 src[128] @0, float lse2[128] @512, uint8 live[128] @1024
@@ -567,8 +601,8 @@ __device__ __forceinline__ uint32_t pds_chunk(int i, int c) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    bwd_tc_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
+    bwd_tc_kernel(const BwdArgs a, const __grid_constant__ TmaSet tmq, const __grid_constant__ TmaSet tmk,
+                  const __grid_constant__ TmaSet tmv, const __grid_constant__ TmaSet tmdo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -607,6 +641,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // past the last slot must stay finite for the MMAs
   for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
     reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  // slot rows past the window (n..127) are pads for every item: key mask
+  // -2^100 in every column, no token
+  for (int z = threadIdx.x; z < kStages * 128; z += blockDim.x) {
+    const int st = z / 128, row = z % 128;
+    if (row >= n) {
+      const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
+      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 0)) = make_uint4(nb2, nb2, nb2, nb2);
+      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
+      reinterpret_cast<int *>(smem + st * kStageBytes + kMeta)[row] = -1;
+    }
+  }
   fence_proxy_async_smem();
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -619,122 +665,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kProducerWarp0 && warp < kMmaWarp) {
     // ------------------------------------------------------------ gather ---
-    // Four consecutive threads gather one slot row: thread quad rq takes rows
-    // rq, rq + 24, rq + 48, ...; lane cq copies 16-byte chunk cq of the row's
-    // 64 bytes (one request of two full sectors per row and tensor). The
-    // route and land byte of the next item are prepared one item ahead.
-    const int pt = threadIdx.x - kProducerWarp0 * 32;
-    const int cq = pt & 3, rq = pt >> 2;
-    constexpr int kRowStep = kProducerThreads / 4;
-    constexpr int kRows = (128 + kRowStep - 1) / kRowStep;
-    const __nv_bfloat16 *q = static_cast<const __nv_bfloat16 *>(a.q);
-    const __nv_bfloat16 *k = static_cast<const __nv_bfloat16 *>(a.k);
-    const __nv_bfloat16 *v = static_cast<const __nv_bfloat16 *>(a.v);
-    const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(a.dout);
-    SlotCoord scoord[kRows];
-#pragma unroll
-    for (int rr = 0; rr < kRows; ++rr) {
-      const int row = rq + rr * kRowStep;
-      scoord[rr] = slot_coord(g, row < n ? row : 0);
-    }
-    struct Prep {
-      int h, b;
-      int src[kRows], reg[kRows];
-      uint8_t land[kRows];
-      float lse[kRows];
-    };
-    auto prep = [&](const ItemCursor &c, Prep &p) {
-      p.h = c.h;
-      p.b = c.b;
-#pragma unroll
-      for (int rr = 0; rr < kRows; ++rr) {
-        const int row = rq + rr * kRowStep;
-        const SlotRoute r = (row < n) ? route_slot(g, c.wc, scoord[rr]) : SlotRoute{-1, 0, 0, 0};
-        p.src[rr] = r.src;
-        p.reg[rr] = r.reg;
-        p.land[rr] = (r.src >= 0 && g.has_land) ? __ldg(a.land + (int64_t)c.b * g.tokens + r.src) : (uint8_t)0;
-        p.lse[rr] = (r.src >= 0) ? __ldg(a.lse + ((int64_t)c.b * g.heads + c.h) * g.tokens + r.src) : 0.f;
-      }
-    };
-    ItemCursor cur;
-    Prep pc, pn;
-    if (count > 0) {
-      cur.init(g, L);
-      prep(cur, pc);
-    }
-    int64_t pending = -1;
-    for (int64_t it = 0; it < count; ++it) {
-      const int s = (int)(it % kStages);
-      ItemCursor nx = cur;
-      nx.next(g);
-      if (it + 1 < count) prep(nx, pn);
-      if (it >= kStages) {
-        const uint32_t par = (uint32_t)((it / kStages) - 1) & 1u;
-        if (kFlushBeforeBlock && !__all_sync(0xffffffffu, mbar_test(bar(bEmpty + s), par))) {
-          // about to block: announce everything still pending first
-          cp_async_wait<0>();
-          fence_proxy_async_smem();
-          for (; pending >= 0 && pending < it; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
-          pending = -1;
-        }
-        if (!mbar_wait_warp(bar(bEmpty + s), par, ctl)) break;
-      }
-      const uint32_t st = sbase + s * kStageBytes;
-      uint8_t *sp = smem + s * kStageBytes;
-      const Prep &p = pc;
-      // A window that neither wraps nor has pads in any dim is one box of the
-      // grid tensor: one TMA load per tensor from an elected thread, counted
-      // as transaction bytes on full[s]; other windows take the row gather.
-      bool box = true;
-#pragma unroll
-      for (int d = 0; d < 3; ++d) box = box && cur.wc[d] * g.w[d] + g.w[d] + g.s[d] <= g.G[d];
-      if (box && pt == 0) {
-        mbar_expect_tx(bar(bFull + s), (uint32_t)(4 * n * 64));
-        const int c0 = cur.wc[0] * g.w[0] + g.s[0], c1 = cur.wc[1] * g.w[1] + g.s[1], c2 = cur.wc[2] * g.w[2] + g.s[2];
-        tma_load_5d(st + kQ, &tmq, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
-        tma_load_5d(st + kK, &tmk, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
-        tma_load_5d(st + kV, &tmv, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
-        tma_load_5d(st + kdO, &tmdo, p.h * 32, c2, c1, c0, p.b, bar(bFull + s));
-      }
-#pragma unroll
-      for (int rr = 0; rr < kRows; ++rr) {
-        const int row = rq + rr * kRowStep;
-        if (row < 128) {
-          const bool valid = p.src[rr] >= 0;
-          const bool live = valid && !p.land[rr];
-          const int64_t off = ((int64_t)p.b * g.tokens + (valid ? p.src[rr] : 0)) * g.C + (int64_t)p.h * 32;
-          const uint32_t nb = valid ? 16u : 0u;
-          if (!box) {
-            cp_async16(st + kQ + sw64(row, cq), q + off + 8 * cq, nb);
-            cp_async16(st + kK + sw64(row, cq), k + off + 8 * cq, nb);
-            cp_async16(st + kV + sw64(row, cq), v + off + 8 * cq, nb);
-            cp_async16(st + kdO + sw64(row, cq), dout + off + 8 * cq, nb);
-          }
-          *reinterpret_cast<uint4 *>(sp + (cq < 2 ? kQm : kKm) + sw32(row, cq & 1)) =
-              mask_chunk(live, p.reg[rr], cq >= 2, cq & 1);
-          if (cq == 0) {
-            reinterpret_cast<int *>(sp + kMeta)[row] = valid ? p.src[rr] : -1;
-            reinterpret_cast<float *>(sp + kMeta + 512)[row] = live ? p.lse[rr] * kLog2e : 0.f;
-            (sp + kMeta + 1024)[row] = live ? 1 : 0;
-          }
-        }
-      }
-      cp_async_commit();
-      if (pending < 0) pending = it;
-      if (it - pending >= kAhead) {  // keep at most kAhead newer items in flight
-        cp_async_wait<kAhead>();
-        fence_proxy_async_smem();
-        mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
-        ++pending;
-      }
-      cur = nx;
-      pc = pn;
-    }
-    cp_async_wait_all();
-    if (pending >= 0 && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      fence_proxy_async_smem();
-      for (; pending < count; ++pending) mbar_arrive_warp(bar(bFull + (int)(pending % kStages)));
-    }
+    const int pw = warp - kProducerWarp0;
+    const StageLayout lay{kStageBytes, kQm, kKm, kMeta, kMeta + 1024, kMeta + 512};
+    gather_role<kStages>(g, lay, pw == 0 ? 2 : 1, pw == 0 ? kQ : pw == 1 ? kK : kV, kdO,
+                         pw == 0 ? &tmq : pw == 1 ? &tmk : &tmv, &tmdo, g.has_land ? a.land : nullptr,
+                         pw == 0 ? a.lse : nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl, L, count, pw, lane);
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
@@ -1038,7 +973,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace bwd
 }  // namespace
 
-bool tc_supported(const Geo &g, int dtype) { return dtype == SWIN_BF16 && g.hd == 32 && g.n <= 128; }
+bool tc_supported(const Geo &g, int dtype) {
+  // gather rows are addressed as int32 rows of the [B*T, C] view
+  return dtype == SWIN_BF16 && g.hd == 32 && g.n <= 128 && (int64_t)g.batch * g.tokens <= INT32_MAX;
+}
 int tc_fwd_ctas_per_sm(const Geo &) { return 1; }
 int tc_bwd_ctas_per_sm(const Geo &) { return 1; }
 
@@ -1062,7 +1000,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // Tiled map of a [B, G0, G1, G2, C] bf16 tensor whose box is one window of
 // one head: (32 channels, w2, w1, w0, 1), 64-byte swizzle (the layout of the
 // kernels' operand tiles).
-bool window_tensor_map(CUtensorMap *m, const void *base, const Geo &g) {
+bool box_tensor_map(CUtensorMap *m, const void *base, const Geo &g) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t e = 2;
@@ -1077,12 +1015,30 @@ bool window_tensor_map(CUtensorMap *m, const void *base, const Geo &g) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Row view [B*T, C] of the same tensor for TMA gather4: box one row high,
+// one head's 32 channels wide.
+bool row_tensor_map(CUtensorMap *m, const void *base, const Geo &g) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)g.C, (cuuint64_t)g.batch * (cuuint64_t)g.tokens};
+  cuuint64_t strides[1] = {dims[0] * 2};
+  cuuint32_t box[2] = {32u, 1u};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Both views of one tensor.
+bool tensor_maps(TmaSet *t, const void *base, const Geo &g) {
+  return box_tensor_map(&t->box, base, g) && row_tensor_map(&t->rows, base, g);
+}
+
 }  // namespace
 
 int launch_fwd_tc(const FwdArgs &a, void *stream) {
-  CUtensorMap mq, mk, mv;
-  if (!window_tensor_map(&mq, a.q, a.g) || !window_tensor_map(&mk, a.k, a.g) || !window_tensor_map(&mv, a.v, a.g))
-    return SWIN_ERR_CUDA;
+  TmaSet mq, mk, mv;
+  if (!tensor_maps(&mq, a.q, a.g) || !tensor_maps(&mk, a.k, a.g) || !tensor_maps(&mv, a.v, a.g)) return SWIN_ERR_CUDA;
   auto kern = fwd::fwd_tc_kernel;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmemBytes) != cudaSuccess)
     return SWIN_ERR_CUDA;
@@ -1091,9 +1047,9 @@ int launch_fwd_tc(const FwdArgs &a, void *stream) {
 }
 
 int launch_bwd_tc(const BwdArgs &a, void *stream) {
-  CUtensorMap mq, mk, mv, mdo;
-  if (!window_tensor_map(&mq, a.q, a.g) || !window_tensor_map(&mk, a.k, a.g) || !window_tensor_map(&mv, a.v, a.g) ||
-      !window_tensor_map(&mdo, a.dout, a.g))
+  TmaSet mq, mk, mv, mdo;
+  if (!tensor_maps(&mq, a.q, a.g) || !tensor_maps(&mk, a.k, a.g) || !tensor_maps(&mv, a.v, a.g) ||
+      !tensor_maps(&mdo, a.dout, a.g))
     return SWIN_ERR_CUDA;
   auto kern = bwd::bwd_tc_kernel;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmemBytes) != cudaSuccess)

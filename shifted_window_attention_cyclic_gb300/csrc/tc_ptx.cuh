@@ -131,6 +131,18 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// Four rows (r0..r3) of a 2-D tiled tensor map whose box is one row high,
+// starting at column c0, into four consecutive box-sized slots of shared
+// memory; completion is signalled as transaction bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int c0, int r0, int r1, int r2, int r3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+
 // ---- cp.async (16-byte, zero-filled when src_bytes == 0) -----------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
