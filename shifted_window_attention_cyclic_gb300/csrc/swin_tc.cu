@@ -226,12 +226,16 @@ constexpr int kBiasStride = 132;
 constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
 // barrier indices
 constexpr int bFull = 0, bEmpty = kStages, bSFull = 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
-              bTFree = bOFull + 2, bMax = bTFree + 2, bNever = bMax + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
+              bTFree = bOFull + 2, bNever = bTFree + 2, bDrain = bNever + 1, kNumBars = bDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
-// per-item exchange slots (double-buffered by item parity): float max[2][2][128],
-// float sum[2][2][128], int src[2][128], int live[2][128]; then int roff[128]
+// Per-item exchange slots from the softmax to the epilogue warps (slot it % 4):
+// float max[4][2][128] and float sum[4][2][128], one value per half row;
+// then int roff[128]. Item it may reuse the slot of item it - 4 because S(it)
+// is issued only after PV(it - 2), which waits for the epilogue to be done
+// with item it - 4.
+constexpr int kXchgSlots = 4;
 constexpr int kXchg = kMiscOff + 16;
-constexpr int kRoff = kXchg + 6144;
+constexpr int kRoff = kXchg + kXchgSlots * 2 * 2 * 128 * 4;
 constexpr int kSmemBytes = kRoff + 512 + 1024;  // + alignment slack
 
 // warps 0-7: two softmax warpgroups, each owning half of every row's columns;
@@ -239,7 +243,9 @@ constexpr int kSmemBytes = kRoff + 512 + 1024;  // + alignment slack
 constexpr int kSoftmaxWarps = 8, kEpilogueWarp0 = 8, kProducerWarp0 = 12, kMmaWarp = 15;
 constexpr int kProducerThreads = (kMmaWarp - kProducerWarp0) * 32;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
-// TMEM columns: S/P of warpgroup w at 128*w, O of warpgroup w at 256 + 32*w
+// TMEM columns: S of item parity b at 128*b, its 16-key group k at +16k, with
+// that group's P (bf16 pairs) over its first 8 columns; O of item parity b
+// and key half h (the keys of softmax warpgroup h) at 256 + 64*b + 32*h
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -264,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(bFull + s), kProducerThreads / 32);
-      mbar_init(bar(bEmpty + s), 1);
+      mbar_init(bar(bEmpty + s), 1 + 4);  // MMA commit + epilogue warps (slot metadata read)
     }
     for (int w = 0; w < 2; ++w) {
       mbar_init(bar(bSFull + w), 1);
@@ -272,7 +278,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bOFull + w), 1);
       mbar_init(bar(bTFree + w), 4);  // epilogue warps
     }
-    mbar_init(bar(bMax), kSoftmaxWarps);
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
@@ -325,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16(128, N, 0, 0);
       const uint32_t idesc_pv = idesc_bf16(128, 32, 0, 1);
+      const int ng0 = (NG + 1) >> 1;  // key groups of softmax warpgroup 0
       int64_t ns = 0, npv = 0;
       uint64_t idle_since = 0;
       uint32_t spins = 0;
@@ -353,10 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               (npv < 2 || mbar_test(bar(bTFree + wb), (uint32_t)((npv >> 1) - 1) & 1u))) {
             tc_fence_after();
             const uint32_t st = sbase + s * kStageBytes;
-            const uint32_t d = tmem + kColO + 32u * wb, p = tmem + kColS + 128u * wb;
+            const uint32_t d = tmem + kColO + 64u * wb, p = tmem + kColS + 128u * wb;
+            // keys of warpgroup 0 into O half 0, of warpgroup 1 into O half 1
             for (int kk = 0; kk < NG; ++kk)
-              mma_ts(d, p + 8u * kk, smem_desc(st + kV + 1024u * kk, kTileBytes, 512, kSwizzle64B), idesc_pv,
-                     kk > 0 ? 1u : 0u);
+              mma_ts(kk < ng0 ? d : d + 32u, p + 16u * kk,
+                     smem_desc(st + kV + 1024u * kk, kTileBytes, 512, kSwizzle64B), idesc_pv,
+                     (kk == 0 || kk == ng0) ? 0u : 1u);
             mma_commit(bar(bOFull + wb));
             mma_commit(bar(bEmpty + s));
             ++npv;
@@ -395,65 +403,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= kEpilogueWarp0) {
     // ---------------------------------------------------------- epilogue ---
-    // Per item: O row i (32 fp32 columns of TMEM lane i) divided by the row
-    // sum, rounded to bf16 and stored at the slot's grid token (the reverse
-    // route); the log-sum-exp (m + log2 sum) * ln 2; land rows store zeros.
+    // Per item, O row i arrives in two halves: O_h holds the keys of softmax
+    // warpgroup h, weighted relative to that half's own row max m_h, with
+    // half row sum l_h. With m = max(m_0, m_1) and a_h = exp2(m_h - m):
+    // O = (a_0 O_0 + a_1 O_1) / (a_0 l_0 + a_1 l_1), rounded to bf16 and
+    // stored at the slot's grid token (the reverse route), and the
+    // log-sum-exp (m + log2(a_0 l_0 + a_1 l_1)) * ln 2; land rows store zeros.
     const int q4 = warp & 3, i = q4 * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-    const float *xmax = reinterpret_cast<const float *>(smem + kXchg);
-    const float *xsum = xmax + 512;
-    const int *xsrc = reinterpret_cast<const int *>(xmax + 1024);
-    const int *xlive = xsrc + 256;
+    const float *xmax = reinterpret_cast<const float *>(smem + kXchg);  // [slot][half][128]
+    const float *xsum = xmax + kXchgSlots * 256;
+    const bool two = ((NG + 1) >> 1) < NG;  // warpgroup 1 owns some keys
     ItemCursor x;
     if (count > 0) x.init(g, L);
     for (int64_t it = 0; it < count; ++it, x.next(g)) {
-      const int wb = (int)(it & 1), xb = (int)(it & 1);
+      const int wb = (int)(it & 1), xs = (int)(it % kXchgSlots), s = (int)(it % kStages);
       if (!mbar_wait_warp(bar(bOFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) break;
       tc_fence_after();
-      uint32_t lo[16], hi[16];
-      tmem_ld16(tmem + lane_addr + kColO + 32u * wb, lo);
-      tmem_ld16(tmem + lane_addr + kColO + 32u * wb + 16, hi);
-      const float m = fmaxf(xmax[xb * 256 + i], xmax[xb * 256 + 128 + i]);
-      const float sum = xsum[xb * 256 + i] + xsum[xb * 256 + 128 + i];
-      const int src = xsrc[xb * 128 + i];
-      const bool live = xlive[xb * 128 + i] != 0;
-      tmem_wait_ld_tied(lo, hi);
+      const uint32_t tO = tmem + lane_addr + kColO + 64u * wb;
+      uint32_t o0[16], o1[16], o2[16], o3[16];  // O_0 columns 0-15, 16-31; O_1 columns 0-15, 16-31
+      tmem_ld16(tO, o0);
+      tmem_ld16(tO + 16, o1);
+      tmem_ld16(tO + 32, o2);
+      tmem_ld16(tO + 48, o3);
+      const uint8_t *sp = smem + s * kStageBytes;
+      const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
+      const bool live = (sp + kMeta + 512)[i] != 0;
+      const float m0 = xmax[xs * 256 + i], m1 = xmax[xs * 256 + 128 + i];
+      const float l0 = xsum[xs * 256 + i], l1 = xsum[xs * 256 + 128 + i];
+      mbar_arrive_warp(bar(bEmpty + s));  // done with the stage's slot metadata
+      tmem_wait_ld_tied(o0, o1);
+      tmem_wait_ld_tied(o2, o3);
       tc_fence_before();
       mbar_arrive_warp(bar(bTFree + wb));
       if (i < n && src >= 0) {
         const int64_t tok = (int64_t)x.b * g.tokens + src;
         uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)x.h * 32);
-        const float inv = live ? __frcp_rn(sum) : 0.f;
+        const float m = two ? fmaxf(m0, m1) : m0;
+        const float a0 = ex2(m0 - m), a1 = two ? ex2(m1 - m) : 0.f;
+        const float l = two ? fmaf(a0, l0, a1 * l1) : l0;
+        const float inv = live ? __frcp_rn(l) : 0.f;
+        const float c0 = a0 * inv, c1 = a1 * inv;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const uint32_t *v16 = c < 2 ? lo : hi;
+          const uint32_t *h0 = c < 2 ? o0 : o1;
+          const uint32_t *h1 = c < 2 ? o2 : o3;
           const int o = (c & 1) * 8;
-          op[c] = make_uint4(pack_bf16(__uint_as_float(v16[o + 0]) * inv, __uint_as_float(v16[o + 1]) * inv),
-                             pack_bf16(__uint_as_float(v16[o + 2]) * inv, __uint_as_float(v16[o + 3]) * inv),
-                             pack_bf16(__uint_as_float(v16[o + 4]) * inv, __uint_as_float(v16[o + 5]) * inv),
-                             pack_bf16(__uint_as_float(v16[o + 6]) * inv, __uint_as_float(v16[o + 7]) * inv));
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            float v0 = __uint_as_float(h0[o + e]) * c0, v1 = __uint_as_float(h0[o + e + 1]) * c0;
+            if (two) {
+              v0 = fmaf(__uint_as_float(h1[o + e]), c1, v0);
+              v1 = fmaf(__uint_as_float(h1[o + e + 1]), c1, v1);
+            }
+            w[e >> 1] = pack_bf16(v0, v1);
+          }
+          op[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
         if (a.lse)
-          a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m + __log2f(sum)) * kLn2 : -INFINITY;
+          a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m + __log2f(l)) * kLn2 : -INFINITY;
       }
     }
     tmem_wait_ld();
   } else {
     // ----------------------------------------------------------- softmax ---
     // Thread (grp, i): TMEM lane i (query slot i), 16-column groups [gb, ge)
-    // of the item's S row, loaded into registers with one wait.
-    // x = S*scale*log2e + bias*log2e (this half of bias row i, in smem), half
-    // row max -> exchanged -> row max m; p = exp2(x - m) -> P (bf16) over S;
-    // half row sums, the row max and the slot's token go to the item's
-    // exchange slot for the epilogue warps.
+    // of the item's S row (warpgroup grp's half of the keys), loaded into
+    // registers with one wait. (A load and its wait stay in straight-line
+    // code: registers that an asynchronous TMEM load is still writing must
+    // not be carried around the loop, where the compiler may copy them.)
+    // x = S*scale*log2e + bias*log2e (this half of bias row i, in smem); the
+    // half row max m_h; p = exp2(x - m_h) -> P (bf16) over the first 8 columns
+    // of each of this thread's 16-column S groups (never over columns the
+    // other warpgroup may not have read yet); m_h and the half row sum go to
+    // the item's exchange slot for the epilogue warps, which put the two
+    // halves on one scale. No exchange between the warpgroups.
     const int grp = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane;
     const int ng0 = (NG + 1) >> 1, gb = grp ? ng0 : 0, ge = grp ? NG : ng0;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     float *brow = reinterpret_cast<float *>(smem + kBias) + i * kBiasStride;
-    float *xmax = reinterpret_cast<float *>(smem + kXchg);  // [2][2][128]
-    float *xsum = xmax + 512;                                // [2][2][128]
-    int *xsrc = reinterpret_cast<int *>(xmax + 1024);        // [2][128]
-    int *xlive = xsrc + 256;                                 // [2][128]
+    float *xmax = reinterpret_cast<float *>(smem + kXchg);  // [slot][half][128]
+    float *xsum = xmax + kXchgSlots * 256;
     const int *roff = reinterpret_cast<const int *>(smem + kRoff);
     const float cs = a.scale * kLog2e;
     const float2 cs2 = make_float2(cs, cs);
@@ -477,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cur_h = x.h;
       }
-      const int wb = (int)(it & 1), s = (int)(it % kStages), xb = (int)(it & 1);
+      const int wb = (int)(it & 1), xs = (int)(it % kXchgSlots);
       const uint32_t tS = tmem + lane_addr + kColS + 128u * wb;
       if (!mbar_wait_warp(bar(bSFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) break;
       tc_fence_after();
@@ -485,12 +516,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4)
         if (gb + k4 < ge) tmem_ld16(tS + 16u * (gb + k4), sv[k4]);
-      if (!mbar_wait_warp(bar(bFull + s), (uint32_t)(it / kStages) & 1u, ctl)) break;
-      const uint8_t *sp = smem + s * kStageBytes;
-      const int src = reinterpret_cast<const int *>(sp + kMeta)[i];
-      const bool live = (sp + kMeta + 512)[i] != 0;
-      // the epilogue warps are done with this exchange slot (item it - 2)
-      if (it >= 2 && !mbar_wait_warp(bar(bTFree + wb), (uint32_t)((it >> 1) - 1) & 1u, ctl)) break;
       tmem_wait_ld_tied(sv[0], sv[1]);
       tmem_wait_ld_tied(sv[2], sv[3]);
       // x = S*cs + bias2 (kept in sv), half row max (independent chains)
@@ -514,14 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      xmax[xb * 256 + grp * 128 + i] = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
-      if (grp == 0) {
-        xsrc[xb * 128 + i] = src;
-        xlive[xb * 128 + i] = live ? 1 : 0;
-      }
-      mbar_arrive_warp(bar(bMax));
-      if (!mbar_wait_warp(bar(bMax), (uint32_t)it & 1u, ctl)) break;
-      const float m = fmaxf(xmax[xb * 256 + i], xmax[xb * 256 + 128 + i]);
+      const float m = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
       // p = exp2(x - m), half row sum, P (bf16) over S
       const float2 negm = make_float2(-m, -m);
       float2 sp2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -531,17 +549,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pv[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
-            const float2 xs =
+            const float2 xs2 =
                 __fadd2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), negm);
-            const float2 p = make_float2(ex2(xs.x), ex2(xs.y));
+            const float2 p = make_float2(ex2(xs2.x), ex2(xs2.y));
             sp2[(e >> 1) & 3] = __fadd2_rn(sp2[(e >> 1) & 3], p);
             pv[e >> 1] = pack_bf16(p.x, p.y);
           }
-          tmem_st8(tS + 8u * (gb + k4), pv);
+          tmem_st8(tS + 16u * (gb + k4), pv);  // over the first half of its own S group
         }
       }
       const float2 sum2 = __fadd2_rn(__fadd2_rn(sp2[0], sp2[1]), __fadd2_rn(sp2[2], sp2[3]));
-      xsum[xb * 256 + grp * 128 + i] = sum2.x + sum2.y;
+      xmax[xs * 256 + grp * 128 + i] = m;
+      xsum[xs * 256 + grp * 128 + i] = sum2.x + sum2.y;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(bar(bPFull + wb));
