@@ -47,24 +47,21 @@ __device__ __forceinline__ uint32_t sw32(int r, int c) { return r * 32 + ((c ^ (
 
 __device__ __forceinline__ int round16(int x) { return (x + 15) & ~15; }
 
-// One 16-byte chunk (columns 8*half .. 8*half+7) of a slot's mask row:
-// key = false gives the Qm row, key = true the Km row (see below).
-__device__ __forceinline__ uint4 mask_chunk(bool live, int reg, bool key, int half) {
-  uint32_t r[4];
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int c0 = 8 * half + 2 * t;
-    const bool h0 = live && reg == c0, h1 = live && reg == c0 + 1;
-    const uint32_t lo = key ? (h0 ? 0u : kBf16NegBig) : (h0 ? kBf16One : 0u);
-    const uint32_t hi = key ? (h1 ? 0u : kBf16NegBig) : (h1 ? kBf16One : 0u);
-    r[t] = lo | (hi << 16);
-  }
-  return make_uint4(r[0], r[1], r[2], r[3]);
+// Mask rows of one slot (K = 16 columns, 32-byte swizzle): Qm = one-hot of
+// the query's region code (live queries only); Km = 0 in the column of the
+// key's region code if the key is live, -2^100 everywhere else. Qm Km^T then
+// adds -2^100 to every masked logit. Region codes are below 8, so columns
+// 8-15 are constant (Qm 0, Km -2^100) and written once per stage; per item
+// only the first 16-byte chunk of each row changes.
+__device__ __forceinline__ uint4 mask_row_chunk0(bool live, int reg, bool key) {
+  const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
+  const uint32_t other = key ? nb2 : 0u;
+  const uint32_t hit = !live ? other
+                       : key ? ((reg & 1) ? (uint32_t)kBf16NegBig : (uint32_t)kBf16NegBig << 16)
+                             : ((reg & 1) ? (uint32_t)kBf16One << 16 : (uint32_t)kBf16One);
+  const int t = reg >> 1;
+  return make_uint4(t == 0 ? hit : other, t == 1 ? hit : other, t == 2 ? hit : other, t == 3 ? hit : other);
 }
-
-// Mask rows of one slot: Qm = one-hot of the query's region bits (live
-// queries only); Km = 0 in the column of the key's region if the key is live,
-// -2^100 everywhere else. Qm Km^T then adds -2^100 to every masked logit.
 
 // Where one item's mask rows and slot metadata sit in a stage (the operand
 // tiles, 128 slot rows x 64 B with 64-byte swizzle, are passed per warp).
@@ -192,11 +189,9 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int slot = 4 * lane + j;
-        if (slot < n) {
-          const int reg = (int)((p.reg4 >> (8 * j)) & 0xffu);
-          *reinterpret_cast<uint4 *>(sp + mt + sw32(slot, 0)) = mask_chunk(live[j], reg, key, 0);
-          *reinterpret_cast<uint4 *>(sp + mt + sw32(slot, 1)) = mask_chunk(live[j], reg, key, 1);
-        }
+        if (slot < n)
+          *reinterpret_cast<uint4 *>(sp + mt + sw32(slot, 0)) =
+              mask_row_chunk0(live[j], (int)((p.reg4 >> (8 * j)) & 0xffu), key);
       }
     }
     fence_proxy_async_smem();  // mask rows are read by the tensor cores
@@ -294,14 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
     reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  // slot rows past the window (n..127) are pads for every item: key mask
-  // -2^100 in every column, no token
+  // key mask columns 8-15 are -2^100 for every row and item; slot rows past
+  // the window (n..127) are pads for every item: -2^100 in every column, no
+  // token (query mask rows stay zero)
   for (int z = threadIdx.x; z < kStages * 128; z += blockDim.x) {
     const int st = z / 128, row = z % 128;
+    const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
+    *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
     if (row >= n) {
-      const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
       *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 0)) = make_uint4(nb2, nb2, nb2, nb2);
-      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
       reinterpret_cast<int *>(smem + st * kStageBytes + kMeta)[row] = -1;
     }
   }
@@ -661,14 +657,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
     reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  // slot rows past the window (n..127) are pads for every item: key mask
-  // -2^100 in every column, no token
+  // key mask columns 8-15 are -2^100 for every row and item; slot rows past
+  // the window (n..127) are pads for every item: -2^100 in every column, no
+  // token (query mask rows stay zero)
   for (int z = threadIdx.x; z < kStages * 128; z += blockDim.x) {
     const int st = z / 128, row = z % 128;
+    const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
+    *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
     if (row >= n) {
-      const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
       *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 0)) = make_uint4(nb2, nb2, nb2, nb2);
-      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
       reinterpret_cast<int *>(smem + st * kStageBytes + kMeta)[row] = -1;
     }
   }
