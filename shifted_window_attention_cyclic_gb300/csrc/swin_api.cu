@@ -92,6 +92,25 @@ int check_desc(const swin_attn_desc *d) {
   return SWIN_OK;
 }
 
+// Step of the window order inside an (head, image) block: the integer
+// nearest nwin * (sqrt(5) - 1) / 2 that is coprime with nwin (so that
+// k -> k * step mod nwin is a permutation whose consecutive windows lie far
+// apart on the grid).
+int window_step(int nwin) {
+  if (nwin <= 2) return 1;
+  int st = std::max(1, (int)((double)nwin * 0.6180339887498949 + 0.5));
+  auto gcd = [](int a, int b) {
+    while (b) {
+      const int t = a % b;
+      a = b;
+      b = t;
+    }
+    return a;
+  };
+  while (gcd(st, nwin) != 1) ++st;
+  return st;
+}
+
 Geo make_geo(const swin_attn_desc *d) {
   Geo g;
   std::memset(&g, 0, sizeof(g));
@@ -106,6 +125,7 @@ Geo make_geo(const swin_attn_desc *d) {
   }
   g.n = g.w[0] * g.w[1] * g.w[2];
   g.nwin = g.nw[0] * g.nw[1] * g.nw[2];
+  g.wstep = window_step(g.nwin);
   g.tokens = g.G[0] * g.G[1] * g.G[2];
   g.rstride[2] = 1;
   g.rstride[1] = 2 * g.w[2] - 1;

@@ -23,6 +23,7 @@ struct Geo {
   int lead;        // 3 - ndim: region bit of normalised dim a is (a - lead)
   int n;           // slots per window
   int nwin;        // windows per image
+  int wstep;       // window order inside an (head, image) block: k-th item -> window (k * wstep) mod nwin
   int tokens;      // tokens per image
   int T;           // bias rows
   int rstride[3];  // prod_{e>d} (2 w_e - 1)
@@ -72,42 +73,44 @@ __host__ __device__ __forceinline__ SlotRoute slot_route(const Geo &g, const int
   return r;
 }
 
-// Work items are (head, image, window), head-major: item = (h * B + b) * nwin + omega.
+// Work items are (head, image, window), head-major: item = (h * B + b) * nwin + k,
+// and the k-th item of an (h, b) block is window omega = (k * wstep) mod nwin.
+// wstep is coprime with nwin (a permutation) and near nwin * 0.618, so a
+// CTA's contiguous item range mixes windows from every part of the grid:
+// the windows at the grid's ends (which wrap or pad and load by rows, the
+// slower path) are spread evenly over the CTAs instead of falling in a few
+// CTAs' ranges.
 struct Item {
   int h, b, omega;
 };
 
 __host__ __device__ __forceinline__ Item decode_item(const Geo &g, int64_t it) {
   Item x;
-  x.omega = (int)(it % g.nwin);
+  const int64_t k = it % g.nwin;
+  x.omega = (int)((k * g.wstep) % g.nwin);
   int64_t t = it / g.nwin;
   x.b = (int)(t % g.batch);
   x.h = (int)(t / g.batch);
   return x;
 }
 
-// Sequential walk over work items in head-major order, one step per item,
-// without divisions (a CTA's items are a contiguous range).
+// Sequential walk over work items in order, one step per item, without
+// divisions (a CTA's items are a contiguous range).
 struct ItemCursor {
-  int h, b, omega, wc[3];
+  int h, b, k, omega;
   __host__ __device__ __forceinline__ void init(const Geo &g, int64_t it) {
     const Item x = decode_item(g, it);
     h = x.h;
     b = x.b;
+    k = (int)(it % g.nwin);
     omega = x.omega;
-    window_coords(g, omega, wc);
   }
   __host__ __device__ __forceinline__ void next(const Geo &g) {
-    if (++wc[2] == g.nw[2]) {
-      wc[2] = 0;
-      if (++wc[1] == g.nw[1]) {
-        wc[1] = 0;
-        ++wc[0];
-      }
-    }
-    if (++omega == g.nwin) {
+    omega += g.wstep;
+    if (omega >= g.nwin) omega -= g.nwin;
+    if (++k == g.nwin) {
+      k = 0;
       omega = 0;
-      wc[0] = wc[1] = wc[2] = 0;
       if (++b == g.batch) {
         b = 0;
         ++h;

@@ -115,10 +115,12 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
   auto prep = [&](const ItemCursor &cu, Prep &p) {
     p.h = cu.h;
     p.b = cu.b;
+    int wc[3];
+    window_coords(g, cu.omega, wc);
     p.box = true;
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
-      p.c[d] = cu.wc[d] * g.w[d] + g.s[d];
+      p.c[d] = wc[d] * g.w[d] + g.s[d];
       p.box = p.box && p.c[d] + g.w[d] <= g.G[d];
     }
     const int org = (p.c[0] * g.G[1] + p.c[1]) * g.G[2] + p.c[2];
@@ -131,7 +133,7 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
         if (p.box) {
           src = org + foff[j];
         } else {
-          const SlotRoute r = route_slot(g, cu.wc, sc[j]);
+          const SlotRoute r = route_slot(g, wc, sc[j]);
           src = r.src;
           reg = r.reg;
         }
