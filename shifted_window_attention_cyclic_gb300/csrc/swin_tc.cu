@@ -63,6 +63,31 @@ __device__ __forceinline__ uint4 mask_row_chunk0(bool live, int reg, bool key) {
   return make_uint4(t == 0 ? hit : other, t == 1 ? hit : other, t == 2 ? hit : other, t == 3 ? hit : other);
 }
 
+// Epilogue store of one 32-channel bf16 row per lane (lane = slot row of the
+// warp's 32) to that row's grid token. Written straight from registers, one
+// store instruction would touch 32 rows 512 bytes apart; instead the rows go
+// through the warp's 2 KB staging area (16-byte chunks swizzled by row) and
+// come back four lanes per row, so each store instruction writes 8 whole
+// 64-byte rows. `dst` is the row's destination (nullptr: row not stored).
+__device__ __forceinline__ void store_rows_bf16(uint8_t *stage, const uint32_t (&w)[16], __nv_bfloat16 *dst,
+                                                int lane) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4 *>(stage + lane * 64 + ((c ^ (lane & 3)) << 4)) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  __syncwarp();
+  const uint64_t mine = reinterpret_cast<uint64_t>(dst);
+  const int c = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 8 * k + (lane >> 2);
+    const uint64_t d = __shfl_sync(0xffffffffu, mine, r);
+    const uint4 v = *reinterpret_cast<const uint4 *>(stage + r * 64 + ((c ^ (r & 3)) << 4));
+    if (d) reinterpret_cast<uint4 *>(d)[c] = v;
+  }
+  __syncwarp();
+}
+
 // Where one item's mask rows and slot metadata sit in a stage (the operand
 // tiles, 128 slot rows x 64 B with 64-byte swizzle, are passed per warp).
 struct StageLayout {
@@ -233,7 +258,8 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag
 constexpr int kXchgSlots = 4;
 constexpr int kXchg = kMiscOff + 16;
 constexpr int kRoff = kXchg + kXchgSlots * 2 * 2 * 128 * 4;
-constexpr int kSmemBytes = kRoff + 512 + 1024;  // + alignment slack
+constexpr int kOStage = kRoff + 512;              // 4 epilogue warps x 2 KB store staging
+constexpr int kSmemBytes = kOStage + 8192 + 1024;  // + alignment slack
 
 // warps 0-7: two softmax warpgroups, each owning half of every row's columns;
 // 8-11: epilogue; 12-14: gather; 15: MMA
@@ -434,32 +460,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld_tied(o2, o3);
       tc_fence_before();
       mbar_arrive_warp(bar(bTFree + wb));
-      if (i < n && src >= 0) {
-        const int64_t tok = (int64_t)x.b * g.tokens + src;
-        uint4 *op = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) + tok * g.C + (int64_t)x.h * 32);
+      const bool store = i < n && src >= 0;
+      {
         const float m = two ? fmaxf(m0, m1) : m0;
         const float a0 = ex2(m0 - m), a1 = two ? ex2(m1 - m) : 0.f;
         const float l = two ? fmaf(a0, l0, a1 * l1) : l0;
         const float inv = live ? __frcp_rn(l) : 0.f;
         const float c0 = a0 * inv, c1 = a1 * inv;
+        uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t *h0 = c < 2 ? o0 : o1;
-          const uint32_t *h1 = c < 2 ? o2 : o3;
-          const int o = (c & 1) * 8;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            float v0 = __uint_as_float(h0[o + e]) * c0, v1 = __uint_as_float(h0[o + e + 1]) * c0;
-            if (two) {
-              v0 = fmaf(__uint_as_float(h1[o + e]), c1, v0);
-              v1 = fmaf(__uint_as_float(h1[o + e + 1]), c1, v1);
-            }
-            w[e >> 1] = pack_bf16(v0, v1);
+        for (int e = 0; e < 32; e += 2) {
+          const uint32_t *h0 = e < 16 ? o0 : o1;
+          const uint32_t *h1 = e < 16 ? o2 : o3;
+          const int o = e & 15;
+          float v0 = __uint_as_float(h0[o]) * c0, v1 = __uint_as_float(h0[o + 1]) * c0;
+          if (two) {
+            v0 = fmaf(__uint_as_float(h1[o]), c1, v0);
+            v1 = fmaf(__uint_as_float(h1[o + 1]), c1, v1);
           }
-          op[c] = make_uint4(w[0], w[1], w[2], w[3]);
+          w[e >> 1] = pack_bf16(v0, v1);
         }
-        if (a.lse)
+        __nv_bfloat16 *dst = store ? static_cast<__nv_bfloat16 *>(a.o) +
+                                         ((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * 32
+                                   : nullptr;
+        store_rows_bf16(smem + kOStage + 2048 * q4, w, dst, lane);
+        if (store && a.lse)
           a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m + __log2f(l)) * kLn2 : -INFINITY;
       }
     }
@@ -602,7 +627,8 @@ constexpr int bFull = 0, bEmpty = kStages, bSpFull = 2 * kStages, bPFull = bSpFu
               bDsync = bWsync + 1, bNever = bDsync + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
 constexpr int kDeltaOff = kMiscOff + 16;         // float [2][128]: the two halves of delta_i
-constexpr int kSmemBytes = kDeltaOff + 1024 + 1024;
+constexpr int kOStage = kDeltaOff + 1024;        // 4 epilogue warps x 2 KB store staging
+constexpr int kSmemBytes = kOStage + 8192 + 1024;
 
 // softmax warps 0-7: two warpgroups, each owning half of every row's columns
 // gather warps 12-14: 96 threads cover the 128 slot rows (threads 0-31 take two)
@@ -760,17 +786,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(tmem + lane_addr + col, lo);
         tmem_ld16(tmem + lane_addr + col + 16, hi);
         tmem_wait_ld_tied(lo, hi);
-        if (!store) return;
-        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(base) + off);
+        uint32_t w[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t *src16 = c < 2 ? lo : hi;
-          const int o = (c & 1) * 8;
-          dst[c] = make_uint4(pack_bf16(__uint_as_float(src16[o + 0]) * mul, __uint_as_float(src16[o + 1]) * mul),
-                              pack_bf16(__uint_as_float(src16[o + 2]) * mul, __uint_as_float(src16[o + 3]) * mul),
-                              pack_bf16(__uint_as_float(src16[o + 4]) * mul, __uint_as_float(src16[o + 5]) * mul),
-                              pack_bf16(__uint_as_float(src16[o + 6]) * mul, __uint_as_float(src16[o + 7]) * mul));
+        for (int e = 0; e < 16; e += 2) {
+          w[e >> 1] = pack_bf16(__uint_as_float(lo[e]) * mul, __uint_as_float(lo[e + 1]) * mul);
+          w[8 + (e >> 1)] = pack_bf16(__uint_as_float(hi[e]) * mul, __uint_as_float(hi[e + 1]) * mul);
         }
+        store_rows_bf16(smem + kOStage + 2048 * q4, w, store ? static_cast<__nv_bfloat16 *>(base) + off : nullptr,
+                        lane);
       };
       drain(kColdV, a.dv, 1.f);
       drain(kColdK, a.dk, a.scale);
