@@ -1,22 +1,27 @@
 // swin_tc.cu -- tcgen05/TMEM kernels of SW-MSA for bf16, head_dim 32,
 // windows of up to 128 slots (sm_103a).
 //
-// Forward, per work item (head h, image b, window omega), one item at a time
-// per CTA stage, persistent CTAs over TERRA Eq. (4) contiguous item ranges:
-//  * gather warps (4): route every slot (cyclic shift, ragged edge, pads) and
-//    cp.async its Q, K, V rows (64 B each) straight from the [B, grid, C]
-//    tensors into 64B-swizzled smem tiles; pads are zero-filled. They also
-//    write two K=16 mask tiles: Qm (one-hot of the query's region bits) and
-//    Km (0 where the key is a live key of that region, -2^100 elsewhere), so
-//    that one extra MMA step adds the region/land/pad mask to QK^T.
-//  * MMA warp (1 elected thread): S = Q K^T + Qm Km^T into TMEM (fp32),
-//    then O = P V with P read from TMEM (bf16).
-//  * softmax warpgroups (2, ping-pong on alternate items): one thread per
-//    TMEM lane (query slot). Logits x = S * scale*log2e + bias*log2e, where the
-//    per-head bias tile [slot_i][slot_j] stays resident in TMEM; row max, exp2,
-//    row sum, P written back over S as bf16; after PV the thread normalises
-//    its O row and stores it at the slot's grid token (the reverse route),
-//    plus the log-sum-exp.
+// Work items are (head h, image b, window omega); each CTA (one per SM) takes
+// a contiguous range of items (TERRA Eq. (4)) and runs them through a
+// warp-specialised pipeline over a few shared-memory stages:
+//  * gather warps (3): route every slot of the item (cyclic shift, ragged
+//    edge, pads) and load the Q, K, V (and dO) rows by TMA, one 5-D box per
+//    tensor for windows that neither wrap nor pad, TMA gather4 by rows
+//    otherwise; they also write the slot metadata and two K=16 mask tiles:
+//    Qm (one-hot of the query's region code) and Km (0 where the key is a
+//    live key of that region, -2^100 elsewhere), so that one extra MMA step
+//    adds the region/land/pad mask to QK^T.
+//  * MMA warp (1 elected thread): tcgen05.mma with fp32 accumulators in TMEM.
+//  * softmax warps (2 warpgroups, each half of every row's keys): one thread
+//    per TMEM lane (query slot); logits x = S*scale*log2e + bias*log2e with
+//    the head's bias tile [slot_i][slot_j] resident in shared memory.
+//  * epilogue warps (4): read the accumulators from TMEM and store rows at
+//    the slots' grid tokens (the reverse route).
+// Forward: S = QK^T (+ mask), P = exp2(x - m_h) per warpgroup half, O = P V
+// into two accumulators (one per key half) combined by the epilogue.
+// Backward: S and dP = dO V^T, P from the saved log-sum-exp, delta = sum P dP,
+// dS = P (dP - delta); dV = P^T dO, dK = dS^T Q, dQ = dS K on the tensor
+// cores; dBias accumulated per slot pair in TMEM and folded at head changes.
 // Masked keys get exactly zero probability: exp2 of about -3e29 is +0.
 //
 // Every wait is bounded (globaltimer); on timeout the CTA raises an abort
@@ -104,17 +109,20 @@ struct TmaSet {
 };
 
 // Gather warps (three). Lane l of every warp routes slots 4l .. 4l+3 of the
-// next item one item ahead and loads their land bytes (and, for the warp that
-// writes them, their log-sum-exps), so that those loads are in flight while
-// the current item is issued.
-// Warp w brings in the tiles of tensors w and w + 3 (when there are four),
+// next item one item ahead; warp 0 also loads their land bytes (and
+// log-sum-exps), so that those loads are in flight while the current item is
+// issued.
+// Warps 1 and 2 bring in the operand tiles (tile_a, and tile_b if ntiles = 2),
 // by TMA only. A window that neither wraps nor pads in any dim is one box
 // (lane 0 loads it); any other window is gathered by rows: lane l fetches
 // the rows of its own four slots with one gather4, pads reading token 0 of
 // the image, which the masks discard. Nothing here waits on a copy:
-// completion is counted in transaction bytes on the stage's full barrier. Warp 0 writes the slot metadata, warp 1 the query mask rows
-// (Qm) and warp 2 the key mask rows (Km).
-template <int kStages>
+// completion is counted in transaction bytes on the stage's full barrier.
+// Warp 0 writes the slot metadata. With kSplitMasks, warp 1 writes the query
+// mask rows (Qm) and warp 2 the key mask rows (Km), each loading the land
+// bytes it needs; otherwise warp 0 loads them and writes both mask tiles,
+// and (given no tiles) no copy waits behind its land loads.
+template <int kStages, bool kSplitMasks>
 __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay, int ntiles, uint32_t tile_a,
                                             uint32_t tile_b, const TmaSet *ma, const TmaSet *mb,
                                             const uint8_t *land, const float *lse, uint8_t *smem, uint32_t sbase,
@@ -134,6 +142,7 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
     bool box;
     int src[4];
     uint32_t reg4;
+    bool lvec;         // land[0] holds the four land bytes
     uint32_t land[4];  // raw bytes: consumed one item later
     float lse[4];
   };
@@ -165,8 +174,37 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
       }
       p.src[j] = src;
       p.reg4 |= (uint32_t)reg << (8 * j);
-      p.land[j] = (src >= 0 && land) ? __ldg(land + tok0 + src) : 0u;
-      if (lse) p.lse[j] = src >= 0 ? __ldg(lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens + src) : 0.f;
+    }
+    // land bytes (and LSE values) are read by warp 0 alone, which writes the
+    // slot metadata and both mask tiles. The four slots of a lane are four
+    // consecutive tokens of one row of a box window when w2 % 4 == 0: then
+    // they come as one 4-byte (16-byte) load if it is aligned.
+    p.lvec = false;
+    if (pw != 0 && !kSplitMasks) return;
+    const bool run4 = p.box && (g.w[2] & 3) == 0 && 4 * lane + 3 < n;
+    const int64_t lt = tok0 + p.src[0];
+    const int64_t lo = ((int64_t)cu.b * g.heads + cu.h) * g.tokens + p.src[0];
+    if (land) {
+      if (run4 && (lt & 3) == 0) {
+        p.lvec = true;
+        p.land[0] = __ldg(reinterpret_cast<const unsigned int *>(land + lt));
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 ? __ldg(land + tok0 + p.src[j]) : 0u;
+      }
+    }
+    if (lse && pw == 0) {
+      if (run4 && (lo & 3) == 0) {
+        const float4 l4 = __ldg(reinterpret_cast<const float4 *>(lse + lo));
+        p.lse[0] = l4.x;
+        p.lse[1] = l4.y;
+        p.lse[2] = l4.z;
+        p.lse[3] = l4.w;
+      } else {
+        const float *lrow = lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 ? __ldg(lrow + p.src[j]) : 0.f;
+      }
     }
   };
   ItemCursor cur;
@@ -185,10 +223,12 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
     const uint32_t st = sbase + s * lay.bytes, full = full0 + 8u * s;
     uint8_t *sp = smem + s * lay.bytes;
     const Prep &p = pc;
-    if (lane == 0) mbar_expect_tx(full, (uint32_t)(ntiles * (p.box ? n * 64 : nq4 * 256)));
+    if (lane == 0 && ntiles > 0) mbar_expect_tx(full, (uint32_t)(ntiles * (p.box ? n * 64 : nq4 * 256)));
     __syncwarp();
     const int x = p.h * 32;
-    if (p.box) {
+    if (ntiles == 0) {
+      // warp 0: no operand tiles
+    } else if (p.box) {
       if (lane == 0) {
         tma_load_5d(st + tile_a, &ma->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
         if (ntiles > 1) tma_load_5d(st + tile_b, &mb->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
@@ -199,9 +239,12 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
       tma_gather4(st + tile_a + 256u * lane, &ma->rows, x, r[0], r[1], r[2], r[3], full);
       if (ntiles > 1) tma_gather4(st + tile_b + 256u * lane, &mb->rows, x, r[0], r[1], r[2], r[3], full);
     }
-    bool live[4];
+    bool live[4] = {false, false, false, false};
+    if (kSplitMasks || pw == 0) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) live[j] = p.src[j] >= 0 && p.land[j] == 0;
+      for (int j = 0; j < 4; ++j)
+        live[j] = p.src[j] >= 0 && (!land || (p.lvec ? ((p.land[0] >> (8 * j)) & 0xffu) : p.land[j]) == 0);
+    }
     if (pw == 0) {
       *reinterpret_cast<int4 *>(sp + lay.src + 16 * lane) = make_int4(p.src[0], p.src[1], p.src[2], p.src[3]);
       *reinterpret_cast<uint32_t *>(sp + lay.live + 4 * lane) =
@@ -210,15 +253,17 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
         *reinterpret_cast<float4 *>(sp + lay.lse2 + 16 * lane) =
             make_float4(live[0] ? p.lse[0] * kLog2e : 0.f, live[1] ? p.lse[1] * kLog2e : 0.f,
                         live[2] ? p.lse[2] * kLog2e : 0.f, live[3] ? p.lse[3] * kLog2e : 0.f);
-    } else {
-      const bool key = pw == 2;
-      const uint32_t mt = key ? lay.km : lay.qm;
+    }
+    if (kSplitMasks ? pw != 0 : pw == 0) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int slot = 4 * lane + j;
-        if (slot < n)
-          *reinterpret_cast<uint4 *>(sp + mt + sw32(slot, 0)) =
-              mask_row_chunk0(live[j], (int)((p.reg4 >> (8 * j)) & 0xffu), key);
+        const int slot = 4 * lane + j, reg = (int)((p.reg4 >> (8 * j)) & 0xffu);
+        if (slot < n) {
+          if (!kSplitMasks || pw == 1)
+            *reinterpret_cast<uint4 *>(sp + lay.qm + sw32(slot, 0)) = mask_row_chunk0(live[j], reg, false);
+          if (!kSplitMasks || pw == 2)
+            *reinterpret_cast<uint4 *>(sp + lay.km + sw32(slot, 0)) = mask_row_chunk0(live[j], reg, true);
+        }
       }
     }
     fence_proxy_async_smem();  // mask rows are read by the tensor cores
@@ -343,9 +388,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ gather ---
     const int pw = warp - kProducerWarp0;
     const StageLayout lay{kStageBytes, kQm, kKm, kMeta, kMeta + 512, 0};
-    gather_role<kStages>(g, lay, 1, pw == 0 ? kQ : pw == 1 ? kK : kV, 0, pw == 0 ? &tmq : pw == 1 ? &tmk : &tmv,
-                         nullptr, g.has_land ? a.land : nullptr, nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl,
-                         L, count, pw, lane);
+    // warp 0: masks and metadata; warp 1: Q and K; warp 2: V
+    gather_role<kStages, false>(g, lay, pw == 0 ? 0 : pw == 1 ? 2 : 1, pw == 1 ? kQ : kV, kK, pw == 1 ? &tmq : &tmv,
+                         &tmk, g.has_land ? a.land : nullptr, nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl, L,
+                         count, pw, lane);
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     // Event loop: S(k) is issued as soon as its data has landed and PV(k-2)
@@ -711,9 +757,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ gather ---
     const int pw = warp - kProducerWarp0;
     const StageLayout lay{kStageBytes, kQm, kKm, kMeta, kMeta + 1024, kMeta + 512};
-    gather_role<kStages>(g, lay, pw == 0 ? 2 : 1, pw == 0 ? kQ : pw == 1 ? kK : kV, kdO,
-                         pw == 0 ? &tmq : pw == 1 ? &tmk : &tmv, &tmdo, g.has_land ? a.land : nullptr,
-                         pw == 0 ? a.lse : nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl, L, count, pw, lane);
+    // warp 0: Q, dO and metadata; warp 1: K and the query masks; warp 2: V and the key masks
+    gather_role<kStages, true>(g, lay, pw == 0 ? 2 : 1, pw == 0 ? kQ : pw == 1 ? kK : kV, kdO,
+                               pw == 0 ? &tmq : pw == 1 ? &tmk : &tmv, &tmdo, g.has_land ? a.land : nullptr,
+                               pw == 0 ? a.lse : nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl, L, count, pw,
+                               lane);
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
@@ -1000,7 +1048,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive_warp(bar(bDsFull));
     }
-    if (ok && !__any_sync(0xffffffffu, *abort_flag != 0) && cur_h >= 0 && want_db) flush(a.slot_base[blockIdx.x] + (cur_h - h_first));
+    if (ok && !__any_sync(0xffffffffu, *abort_flag != 0) && cur_h >= 0 && want_db)
+      flush(a.slot_base[blockIdx.x] + (cur_h - h_first));
     tmem_wait_st();
     tmem_wait_ld();
   }

@@ -1,5 +1,5 @@
 // tc_ptx.cuh -- hand-written inline PTX for the sm_103a kernels: mbarriers
-// with bounded waits, cp.async gathers, tcgen05 (TMEM alloc, MMA, commit,
+// with bounded waits, TMA box and gather4 loads, tcgen05 (TMEM alloc, MMA, commit,
 // TMEM loads/stores, fences) and shared-memory matrix descriptors.
 #pragma once
 #include <cstdint>
@@ -142,17 +142,6 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int 
       "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
       : "memory");
 }
-
-// ---- cp.async (16-byte, zero-filled when src_bytes == 0) -----------------
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor core operand reads).
