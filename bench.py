@@ -140,7 +140,8 @@ def oracle_sample_rate(wl, x, windows, seed=0):
     import oracle
     pb = oracle.Problem(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.has_land)
     rng = np.random.default_rng(seed)
-    ids = rng.choice(wl.batch * pb.nwin, size=windows, replace=False)
+    population = wl.batch * pb.nwin
+    ids = rng.choice(population, size=windows, replace=windows > population)  # small grids repeat windows
     win_src = oracle.tables(pb)[0]
     tokens = int(sum((win_src[i % pb.nwin] >= 0).sum() for i in ids))
     t0 = time.perf_counter()
@@ -156,7 +157,7 @@ def cpu_baseline(wl, x, target_s=15.0):
     tok, dt = oracle_sample_rate(wl, x, calib, seed=1)
     per_window = dt / calib
     nwin = oracle.Problem(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim).nwin
-    windows = int(max(calib, min(wl.batch * nwin, target_s / max(per_window, 1e-6))))
+    windows = int(max(calib, min(max(wl.batch * nwin, 4096), target_s / max(per_window, 1e-6))))
     tok, dt = oracle_sample_rate(wl, x, windows, seed=2)
     return {"value": tok / dt / 1e6, "unit": "Mtokens/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": "%d random windows of %s (%d tokens), fwd+bwd, fp64 C oracle, %.1f s" %
@@ -198,13 +199,14 @@ def run_reference(args, wl):
 
 
 def config_of(wl):
+    tensor_mb = wl.batch * wl.tokens * wl.channels * (2 if wl.dtype == "bf16" else 4) / 1e6
     return {"workload": "%s: B=%d grid %s C=%d heads %dx%d window %s shift %s periodic %s land p %s %s" %
                         (wl.name, wl.batch, "x".join(map(str, wl.grid)), wl.channels, wl.heads, wl.head_dim,
                          "x".join(map(str, wl.window)), tuple(wl.shift), tuple(wl.periodic), wl.land_p, wl.dtype),
             "global_batch": wl.batch, "tokens_per_batch": wl.batch * wl.tokens,
             "parallelism": "replicas (independent problem per GPU)",
-            "l2": "inputs larger than L2 (each tensor %.0f MB > 129 MB), no flush" %
-                  (wl.batch * wl.tokens * wl.channels * 2 / 1e6)}
+            "l2": ("inputs larger than L2 (each tensor %.0f MB > 129 MB), no flush" if tensor_mb > 129 else
+                   "inputs smaller than L2 (each tensor %.0f MB), no flush: L2-resident timing") % tensor_mb}
 
 
 def main():
@@ -248,8 +250,10 @@ def main():
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     host = {k_: torch.from_numpy(x[k_]).to(tdt).pin_memory() for k_ in ("q", "k", "v", "dout")}
     host["bias"] = torch.from_numpy(x["bias"]).pin_memory()
-    host["land"] = torch.from_numpy(x["land"]).pin_memory()
+    if x["land"] is not None:
+        host["land"] = torch.from_numpy(x["land"]).pin_memory()
     d = {k_: t.to(dev) for k_, t in host.items()}
+    d_land = d.get("land")
     o = torch.empty(attn.shape, dtype=tdt, device=dev)
     lse = torch.empty(attn.lse_shape, dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty(attn.shape, dtype=tdt, device=dev) for _ in range(3))
@@ -258,8 +262,8 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step():
-        C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], d["bias"], d["land"], o, lse, stream)
-        C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, d["bias"], d["land"], dq, dk, dv, dbias,
+        C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], d["bias"], d_land, o, lse, stream)
+        C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, d["bias"], d_land, dq, dk, dv, dbias,
                         ws, stream)
 
     for _ in range(args.warmup):
@@ -281,9 +285,9 @@ def main():
     start.record(stream)
     for e0, e1, e2 in ev:
         e0.record(stream)
-        C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], d["bias"], d["land"], o, lse, stream)
+        C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], d["bias"], d_land, o, lse, stream)
         e1.record(stream)
-        C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, d["bias"], d["land"], dq, dk, dv, dbias,
+        C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, d["bias"], d_land, dq, dk, dv, dbias,
                         ws, stream)
         e2.record(stream)
     end.record(stream)
