@@ -110,6 +110,12 @@ SWEEP = [
     ((16, 24), (4, 6), (0, 0), (0, 1), 4, 32, 3, "bf16", (0.3, 0.3)),    # W-MSA, batch 3
     ((7, 7), (8, 8), (0, 0), (0, 0), 2, 32, 1, "bf16", None),            # window larger than grid
     ((11, 11), (8, 8), (4, 4), (0, 0), 2, 16, 1, "f32", None),           # ragged, both dims masked
+    # tensor-core path corners: n = 15 < 16 (one key group, no second half),
+    # gathered windows whose last row quad is partly past n, batch 2
+    ((10, 23), (3, 5), (1, 2), (0, 1), 2, 32, 2, "bf16", (0.3, 0.3)),
+    ((9, 30), (3, 7), (2, 3), (1, 1), 3, 32, 1, "bf16", (0.2, 0.2)),     # n = 21
+    # w2 = 4 with an odd lon shift: box rows not 4-token aligned (scalar land/LSE loads)
+    ((4, 12, 20), (2, 4, 4), (1, 2, 1), (0, 0, 1), 2, 32, 1, "bf16", (0.3, 0.5)),
 ]
 
 
