@@ -301,10 +301,13 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag
 // is issued only after PV(it - 2), which waits for the epilogue to be done
 // with item it - 4.
 constexpr int kXchgSlots = 4;
-constexpr int kXchg = kMiscOff + 16;
+constexpr int kXchg = (kMiscOff + 16 + 127) & ~127;
 constexpr int kRoff = kXchg + kXchgSlots * 2 * 2 * 128 * 4;
-constexpr int kOStage = kRoff + 512;              // 4 epilogue warps x 2 KB store staging
-constexpr int kSmemBytes = kOStage + 8192 + 1024;  // + alignment slack
+constexpr int kOStage = (kRoff + 512 + 127) & ~127;  // 4 epilogue warps x 2 KB store staging (16-byte stores)
+constexpr int kSmemBytes = kOStage + 8192 + 1024;    // + alignment slack
+static_assert(kStageBytes % 1024 == 0 && kBias % 16 == 0, "stage tiles need 1024-byte alignment");
+static_assert(kXchg % 16 == 0 && kOStage % 16 == 0, "vector accesses need 16-byte alignment");
+static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
 
 // warps 0-7: two softmax warpgroups, each owning half of every row's columns;
 // 8-11: epilogue; 12-14: gather; 15: MMA
@@ -672,9 +675,12 @@ constexpr int bFull = 0, bEmpty = kStages, bSpFull = 2 * kStages, bPFull = bSpFu
               bAccFull = bDsFull + 1, bAccFree = bAccFull + 1, bDsFree = bAccFree + 1, bWsync = bDsFree + 1,
               bDsync = bWsync + 1, bNever = bDsync + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
-constexpr int kDeltaOff = kMiscOff + 16;         // float [2][128]: the two halves of delta_i
-constexpr int kOStage = kDeltaOff + 1024;        // 4 epilogue warps x 2 KB store staging
+constexpr int kDeltaOff = (kMiscOff + 16 + 127) & ~127;  // float [2][128]: the two halves of delta_i
+constexpr int kOStage = kDeltaOff + 1024;                // 4 epilogue warps x 2 KB store staging (16-byte stores)
 constexpr int kSmemBytes = kOStage + 8192 + 1024;
+static_assert(kStageBytes % 1024 == 0 && kP % 1024 == 0 && kdS % 1024 == 0, "operand tiles need 1024-byte alignment");
+static_assert(kBias % 16 == 0 && kOStage % 16 == 0, "vector accesses need 16-byte alignment");
+static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
 
 // softmax warps 0-7: two warpgroups, each owning half of every row's columns
 // gather warps 12-14: 96 threads cover the 128 slot rows (threads 0-31 take two)
