@@ -135,6 +135,23 @@ def dist_info():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x, device):
+    """The largest x of all ranks (x itself when the job has one rank): each
+    rank times its own replica, and the job is as slow as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world, tokens_per_rank, ms_per_step):
+    """Whole-job throughput in Mtokens/s: every rank processes its own batch."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3) / 1e6
+
+
 def oracle_sample_rate(wl, x, windows, seed=0):
     """Time the oracle (fwd + bwd, fp64) on `windows` windows; returns (tokens, seconds)."""
     import oracle
@@ -299,13 +316,10 @@ def main():
     total_ms = start.elapsed_time(end)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / args.steps
     tokens = wl.batch * wl.tokens
-    value = world * tokens / (ms_per_step * 1e-3) / 1e6
+    value = job_rate(world, tokens, ms_per_step)
     fwd_avg = statistics.mean(fwd_ms)
     bwd_avg = statistics.mean(bwd_ms)
     peaks, peak_kind = load_peaks()
@@ -343,10 +357,7 @@ def main():
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -369,7 +380,7 @@ def main():
                          "peak_source": peak_kind, "traffic": profiled_traffic(khash),
                          "alg_bytes_per_launch": bwd_bytes},
             "clocks": clocks,
-            "e2e": {"value": world * tokens / (e2e_ms * 1e-3) / 1e6, "unit": "Mtokens/s", "ms_per_step": e2e_ms,
+            "e2e": {"value": job_rate(world, tokens, e2e_ms), "unit": "Mtokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 3 * args.steps,
             "impl_kernels": {1: "simt", 2: "tcgen05"}[attn.info.impl],
