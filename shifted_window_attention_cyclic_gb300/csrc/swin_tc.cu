@@ -849,9 +849,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_rows_bf16(smem + kOStage + 2048 * q4, w, store ? static_cast<__nv_bfloat16 *>(base) + off : nullptr,
                         lane);
       };
-      drain(kColdV, a.dv, 1.f);
-      drain(kColdK, a.dk, a.scale);
-      drain(kColdQ, a.dq, a.scale);
+      // one copy of the drain code for the three accumulators (instruction
+      // cache: every role's loop runs on every SM sub-partition at once)
+#pragma unroll 1
+      for (int t = 0; t < 3; ++t)
+        drain(t == 0 ? kColdV : t == 1 ? kColdK : kColdQ, t == 0 ? a.dv : t == 1 ? a.dk : a.dq,
+              t == 0 ? 1.f : a.scale);
       tc_fence_before();
       mbar_arrive_warp(bar(bAccFree));
     }
@@ -966,27 +969,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4 *>(smem + kP + pds_chunk(i, 2 * gi + 1)) = make_uint4(pb[4], pb[5], pb[6], pb[7]);
       };
       {
+        // two groups per TMEM round trip: tcgen05.wait::ld waits for every
+        // load in flight, so a double buffer would wait just as often, and
+        // the round trips (not the arithmetic) set this pass's length
         uint32_t s0[16], d0[16], s1[16], d1[16];
-        tmem_ld16(tS + 16u * gb, s0);
-        tmem_ld16(tdP + 16u * gb, d0);
-#pragma unroll
+#pragma unroll 1
         for (int k2 = 0; k2 < 4; k2 += 2) {
           const int g0 = gb + k2, g1 = gb + k2 + 1;
           if (g0 < ge) {
-            tmem_wait_ld_tied(s0, d0);
+            tmem_ld16(tS + 16u * g0, s0);
+            tmem_ld16(tdP + 16u * g0, d0);
             if (g1 < ge) {
               tmem_ld16(tS + 16u * g1, s1);
               tmem_ld16(tdP + 16u * g1, d1);
             }
+            tmem_wait_ld_tied(s0, d0);
             p_group(g0, s0, d0);
-          }
-          if (g1 < ge) {
-            tmem_wait_ld_tied(s1, d1);
-            if (g1 + 1 < ge) {
-              tmem_ld16(tS + 16u * (g1 + 1), s0);
-              tmem_ld16(tdP + 16u * (g1 + 1), d0);
+            if (g1 < ge) {
+              tmem_tie(s1, d1);
+              p_group(g1, s1, d1);
             }
-            p_group(g1, s1, d1);
           }
         }
       }
@@ -1032,19 +1034,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 8; ++e) av[e] = 0u;
           }
         };
+        // two sub-groups per TMEM round trip (se - sb is even)
         const int sb = 2 * gb, se = 2 * ge;
-        load3(sb, p0, d0, a0);
-#pragma unroll
+#pragma unroll 1
         for (int k2 = 0; k2 < 8; k2 += 2) {
           const int s0 = sb + k2, s1 = sb + k2 + 1;
           if (s0 < se) {
+            load3(s0, p0, d0, a0);
+            load3(s1, p1, d1, a1);
             tmem_wait_ld_tied(p0, d0, a0);
-            if (s1 < se) load3(s1, p1, d1, a1);
+            tmem_tie(p1, d1, a1);
             ds_sub(s0, p0, d0, a0);
-          }
-          if (s1 < se) {
-            tmem_wait_ld_tied(p1, d1, a1);
-            if (s1 + 1 < se) load3(s1 + 1, p0, d0, a0);
             ds_sub(s1, p1, d1, a1);
           }
         }
