@@ -673,7 +673,8 @@ constexpr int kBiasStride = 132;
 constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
 constexpr int bFull = 0, bEmpty = kStages, bSpFull = 2 * kStages, bPFull = bSpFull + 1, bDsFull = bPFull + 1,
               bAccFull = bDsFull + 1, bAccFree = bAccFull + 1, bDsFree = bAccFree + 1, bWsync = bDsFree + 1,
-              bDsync = bWsync + 1, bNever = bDsync + 1, bDrain = bNever + 1, kNumBars = bDrain + 1;
+              bDsync = bWsync + 1, bNever = bDsync + 1, bDrain = bNever + 1, bVFree = bDrain + 1,
+              kNumBars = bVFree + 2;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
 constexpr int kDeltaOff = (kMiscOff + 16 + 127) & ~127;  // float [2][128]: the two halves of delta_i
 constexpr int kOStage = kDeltaOff + 1024;                // 4 epilogue warps x 2 KB store staging (16-byte stores)
@@ -687,8 +688,11 @@ static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may 
 constexpr int kSoftmaxThreads = 256, kEpilogueWarp0 = 8, kProducerWarp0 = 12, kMmaWarp = 15;
 constexpr int kProducerThreads = (kMmaWarp - kProducerWarp0) * 32;
 constexpr int kThreads = (kMmaWarp + 1) * 32;
+// dV has two buffers (item parity): dV(it) is issued as soon as P(it) is
+// written, while the epilogue may still be draining item it - 1; dK and dQ
+// wait for that drain.
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColdP = 128, kColdV = 256, kColdK = 288, kColdQ = 320,
-                   kColAcc = 384;
+                   kColdV1 = 352, kColAcc = 384;
 
 // byte offset of the 16-byte chunk holding j = 8c..8c+7 of row i in a P/dS tile
 __device__ __forceinline__ uint32_t pds_chunk(int i, int c) {
@@ -729,6 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bDsync), kSoftmaxThreads / 32);
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
+    mbar_init(bar(bVFree), 4);
+    mbar_init(bar(bVFree + 1), 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -794,15 +800,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t it = 0; ok && it < count; ++it) {
         const int s = (int)(it % kStages);
         const uint32_t st = sbase + s * kStageBytes;
+        const int vb = (int)(it & 1);
         if (!mbar_wait(bar(bPFull), (uint32_t)it & 1u, ctl)) break;
-        if (it >= 1 && !mbar_wait(bar(bAccFree), (uint32_t)(it - 1) & 1u, ctl)) break;
+        if (it >= 2 && !mbar_wait(bar(bVFree + vb), (uint32_t)((it >> 1) - 1) & 1u, ctl)) break;
         tc_fence_after();
         for (int kk = 0; kk < 8; ++kk)  // dV = P^T dO: M = keys, K = queries
-          mma_ss(tmem + kColdV, smem_desc(sbase + kP + 2048u * kk, 16384, 1024, kSwizzle128B),
+          mma_ss(tmem + (vb ? kColdV1 : kColdV), smem_desc(sbase + kP + 2048u * kk, 16384, 1024, kSwizzle128B),
                  smem_desc(st + kdO + 1024u * kk, kTile, 512, kSwizzle64B), idesc_mn, kk > 0 ? 1u : 0u);
         if (!mbar_wait(bar(bDsFull), (uint32_t)it & 1u, ctl)) break;
         tc_fence_after();
         if (it + 1 < count && !issue_sdp(it + 1)) break;
+        if (it >= 1 && !mbar_wait(bar(bAccFree), (uint32_t)(it - 1) & 1u, ctl)) break;
+        tc_fence_after();
         for (int kk = 0; kk < 8; ++kk)  // dK = dS^T Q
           mma_ss(tmem + kColdK, smem_desc(sbase + kdS + 2048u * kk, 16384, 1024, kSwizzle128B),
                  smem_desc(st + kQ + 1024u * kk, kTile, 512, kSwizzle64B), idesc_mn, kk > 0 ? 1u : 0u);
@@ -850,11 +859,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lane);
       };
       // one copy of the drain code for the three accumulators (instruction
-      // cache: every role's loop runs on every SM sub-partition at once)
+      // cache: every role's loop runs on every SM sub-partition at once);
+      // the dV buffer is handed back as soon as it is read
+      const int vb = (int)(it & 1);
 #pragma unroll 1
-      for (int t = 0; t < 3; ++t)
-        drain(t == 0 ? kColdV : t == 1 ? kColdK : kColdQ, t == 0 ? a.dv : t == 1 ? a.dk : a.dq,
+      for (int t = 0; t < 3; ++t) {
+        drain(t == 0 ? (vb ? kColdV1 : kColdV) : t == 1 ? kColdK : kColdQ, t == 0 ? a.dv : t == 1 ? a.dk : a.dq,
               t == 0 ? 1.f : a.scale);
+        if (t == 0) {
+          tc_fence_before();
+          mbar_arrive_warp(bar(bVFree + vb));
+        }
+      }
       tc_fence_before();
       mbar_arrive_warp(bar(bAccFree));
     }
