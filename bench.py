@@ -278,12 +278,15 @@ def main():
     ws = attn.workspace()
     stream = torch.cuda.current_stream()
 
-    def step(src=None):
+    outs = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv, "dbias": dbias}
+
+    def step(src=None, out=None):
         src = d if src is None else src
+        r = outs if out is None else out
         land_ = src.get("land")
-        C.swin_attn_fwd(attn.plan, src["q"], src["k"], src["v"], src["bias"], land_, o, lse, stream)
-        C.swin_attn_bwd(attn.plan, src["q"], src["k"], src["v"], src["dout"], lse, src["bias"], land_, dq, dk, dv,
-                        dbias, ws, stream)
+        C.swin_attn_fwd(attn.plan, src["q"], src["k"], src["v"], src["bias"], land_, r["o"], r["lse"], stream)
+        C.swin_attn_bwd(attn.plan, src["q"], src["k"], src["v"], src["dout"], r["lse"], src["bias"], land_, r["dq"],
+                        r["dk"], r["dv"], r["dbias"], ws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -339,37 +342,50 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
     # Every step copies its inputs host->device and its results device->host
-    # inside the timed region. As in a training input pipeline, the next
-    # step's input copies run on a second stream (into the other of two
-    # device input sets) while this step computes and copies its results back.
-    copy_stream = torch.cuda.Stream(device=dev)
+    # inside the timed region. As in a training input pipeline, the copies
+    # run on two more streams and both device sets (inputs, results) are
+    # double-buffered: step k+1's inputs come in and step k-1's results go
+    # out while step k computes (the two copy directions overlap).
+    in_stream, out_stream = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     dsets = [d, {k_: torch.empty_like(t) for k_, t in d.items()}]
-    in_ready = [torch.cuda.Event(), torch.cuda.Event()]
-    in_free = [torch.cuda.Event(), torch.cuda.Event()]
+    osets = [outs, {k_: torch.empty_like(t) for k_, t in outs.items()}]
+    in_ready, in_free, out_ready, out_free = ([torch.cuda.Event(), torch.cuda.Event()] for _ in range(4))
 
     def h2d_copy(j):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(in_free[j])
+        with torch.cuda.stream(in_stream):
+            in_stream.wait_event(in_free[j])
             for k_, t in host.items():
                 dsets[j][k_].copy_(t, non_blocking=True)
-            in_ready[j].record(copy_stream)
+            in_ready[j].record(in_stream)
 
-    def compute_d2h(j):
+    def compute(j):
         stream.wait_event(in_ready[j])
-        step(dsets[j])
+        stream.wait_event(out_free[j])
+        step(dsets[j], osets[j])
         in_free[j].record(stream)
-        for k_, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv), ("dbias", dbias)):
-            host_out[k_].copy_(t, non_blocking=True)
+        out_ready[j].record(stream)
+
+    def d2h_copy(j):
+        with torch.cuda.stream(out_stream):
+            out_stream.wait_event(out_ready[j])
+            for k_ in host_out:
+                host_out[k_].copy_(osets[j][k_], non_blocking=True)
+            out_free[j].record(out_stream)
 
     def e2e_run(steps):
         start = torch.cuda.Event()
         start.record(stream)
-        copy_stream.wait_event(start)
+        in_stream.wait_event(start)
+        out_stream.wait_event(start)
         h2d_copy(0)
         for k_ in range(steps):
             if k_ + 1 < steps:
                 h2d_copy((k_ + 1) % 2)
-            compute_d2h(k_ % 2)
+            compute(k_ % 2)
+            d2h_copy(k_ % 2)
+        done = torch.cuda.Event()
+        done.record(out_stream)
+        stream.wait_event(done)  # the timed region ends after the last result copy
 
     e2e_run(2)
     torch.cuda.synchronize()
