@@ -99,7 +99,8 @@ typedef struct {
   int32_t fwd_ctas;    /* persistent CTAs of the forward kernel */
   int32_t bwd_ctas;    /* persistent CTAs of the backward kernel */
   int32_t num_sms;
-  int64_t work_items;  /* heads * B * windows_per_image (one window and head each) */
+  int64_t work_items;  /* heads * B * ceil(windows_per_image / k): one head and k windows each, k = 2 on
+                          the tensor-core path when two windows fit one 128-slot tile, else 1 */
   int64_t dbias_slots; /* partial dBias tables in the workspace */
 } swin_attn_plan_info;
 

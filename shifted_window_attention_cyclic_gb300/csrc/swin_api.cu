@@ -111,6 +111,18 @@ int window_step(int nwin) {
   return st;
 }
 
+// Windows per work item. The tensor-core kernels put two windows in one
+// 128-row tile when both fit with the second starting on a 16-row boundary
+// (whole 1 KB swizzle spans and 16-key MMA groups); the mask step's 16
+// columns hold the two windows' region codes (8 each).
+void set_pack(Geo &g, int pack) {
+  g.pack = pack;
+  g.offb = pack == 2 ? ((g.n + 15) & ~15) : g.n;
+  g.rows = pack == 2 ? g.offb + g.n : g.n;
+  g.nitem = (g.nwin + pack - 1) / pack;
+  g.istep = (int)(((int64_t)pack * g.wstep) % g.nwin);
+}
+
 Geo make_geo(const swin_attn_desc *d) {
   Geo g;
   std::memset(&g, 0, sizeof(g));
@@ -136,6 +148,7 @@ Geo make_geo(const swin_attn_desc *d) {
   g.C = d->heads * d->head_dim;
   g.batch = (int)d->batch;
   g.has_land = d->has_land;
+  set_pack(g, 1);
   return g;
 }
 
@@ -206,7 +219,8 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
     return SWIN_ERR_UNSUPPORTED;
   }
   p->impl = desc->impl == SWIN_IMPL_AUTO ? (tc_ok ? SWIN_IMPL_TC : SWIN_IMPL_SIMT) : desc->impl;
-  p->items = (int64_t)g.heads * g.batch * g.nwin;
+  if (p->impl == SWIN_IMPL_TC && ((g.n + 15) & ~15) + g.n <= 128) set_pack(p->g, 2);
+  p->items = (int64_t)g.heads * g.batch * g.nitem;
   int fwd_bps = 1, bwd_bps = 1;
   if (p->impl == SWIN_IMPL_SIMT) {
     if (simt_occupancy(false, g, desc->dtype, &fwd_bps) || simt_occupancy(true, g, desc->dtype, &bwd_bps)) {
@@ -220,7 +234,7 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
   p->fwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, fwd_bps) * p->num_sms);
   p->bwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, bwd_bps) * p->num_sms);
   // workspace slots: one partial dBias table per (CTA, head it touches)
-  const int64_t per_head = (int64_t)g.batch * g.nwin;
+  const int64_t per_head = (int64_t)g.batch * g.nitem;
   std::vector<int> slot_base(p->bwd_ctas), slot_head;
   for (int r = 0; r < p->bwd_ctas; ++r) {
     int64_t L, R;

@@ -23,7 +23,13 @@ struct Geo {
   int lead;        // 3 - ndim: region bit of normalised dim a is (a - lead)
   int n;           // slots per window
   int nwin;        // windows per image
-  int wstep;       // window order inside an (head, image) block: k-th item -> window (k * wstep) mod nwin
+  int wstep;       // window order inside an (head, image) block: the i-th window is (i * wstep) mod nwin
+  // Windows per work item (tensor-core kernels): with pack = 2 the two
+  // windows 2k and 2k+1 of that order share one 128-row tile, the first in
+  // rows [0, n), the second in rows [offb, offb + n); rows = tile rows used.
+  int pack, nitem;  // nitem = ceil(nwin / pack) items per (head, image) block
+  int offb, rows;
+  int istep;        // (pack * wstep) mod nwin: window step from one item to the next
   int tokens;      // tokens per image
   int T;           // bias rows
   int rstride[3];  // prod_{e>d} (2 w_e - 1)
@@ -73,8 +79,10 @@ __host__ __device__ __forceinline__ SlotRoute slot_route(const Geo &g, const int
   return r;
 }
 
-// Work items are (head, image, window), head-major: item = (h * B + b) * nwin + k,
-// and the k-th item of an (h, b) block is window omega = (k * wstep) mod nwin.
+// Work items are (head, image, window group), head-major: item = (h * B + b) *
+// nitem + k, and the k-th item of an (h, b) block holds windows number
+// pack*k .. pack*k + pack - 1 of the order i -> (i * wstep) mod nwin (the
+// second one only if pack*k + 1 < nwin).
 // wstep is coprime with nwin (a permutation) and near nwin * 0.618, so a
 // CTA's contiguous item range mixes windows from every part of the grid:
 // the windows at the grid's ends (which wrap or pad and load by rows, the
@@ -86,9 +94,9 @@ struct Item {
 
 __host__ __device__ __forceinline__ Item decode_item(const Geo &g, int64_t it) {
   Item x;
-  const int64_t k = it % g.nwin;
-  x.omega = (int)((k * g.wstep) % g.nwin);
-  int64_t t = it / g.nwin;
+  const int64_t k = it % g.nitem;
+  x.omega = (int)((k * g.pack * g.wstep) % g.nwin);  // the item's first window
+  int64_t t = it / g.nitem;
   x.b = (int)(t % g.batch);
   x.h = (int)(t / g.batch);
   return x;
@@ -102,13 +110,19 @@ struct ItemCursor {
     const Item x = decode_item(g, it);
     h = x.h;
     b = x.b;
-    k = (int)(it % g.nwin);
+    k = (int)(it % g.nitem);
     omega = x.omega;
   }
+  // the item's second window (pack = 2), if the image has it
+  __host__ __device__ __forceinline__ bool has2(const Geo &g) const { return g.pack == 2 && 2 * k + 1 < g.nwin; }
+  __host__ __device__ __forceinline__ int omega2(const Geo &g) const {
+    const int o = omega + g.wstep;
+    return o >= g.nwin ? o - g.nwin : o;
+  }
   __host__ __device__ __forceinline__ void next(const Geo &g) {
-    omega += g.wstep;
+    omega += g.istep;
     if (omega >= g.nwin) omega -= g.nwin;
-    if (++k == g.nwin) {
+    if (++k == g.nitem) {
       k = 0;
       omega = 0;
       if (++b == g.batch) {
@@ -118,6 +132,15 @@ struct ItemCursor {
     }
   }
 };
+
+// Tile row -> slot of its window (u = 0 or 1 for pack = 2), or -1 for a row
+// that no window slot uses.
+template <int kPack>
+__host__ __device__ __forceinline__ int tile_slot(const Geo &g, int row, int &u) {
+  u = (kPack == 2 && row >= g.offb) ? 1 : 0;
+  const int s = row - u * g.offb;
+  return s < g.n ? s : -1;
+}
 
 // In-window coordinates of one slot, computed once per thread.
 struct SlotCoord {

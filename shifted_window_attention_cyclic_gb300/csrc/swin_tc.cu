@@ -122,161 +122,344 @@ struct TmaSet {
 // mask rows (Qm) and warp 2 the key mask rows (Km), each loading the land
 // bytes it needs; otherwise warp 0 loads them and writes both mask tiles,
 // and (given no tiles) no copy waits behind its land loads.
-template <int kStages, bool kSplitMasks>
+template <int kStages, bool kSplitMasks, int kPack>
 __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay, int ntiles, uint32_t tile_a,
                                             uint32_t tile_b, const TmaSet *ma, const TmaSet *mb,
                                             const uint8_t *land, const float *lse, uint8_t *smem, uint32_t sbase,
                                             uint32_t full0, uint32_t empty0, const WaitCtl &ctl, int64_t L,
                                             int64_t count, int pw, int lane) {
-  const int n = g.n, nq4 = (n + 3) >> 2;
-  SlotCoord sc[4];
-  int foff[4];  // token offset of slot 4l + j from the window's origin when the window is a box
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int slot = 4 * lane + j;
-    sc[j] = slot_coord(g, slot < n ? slot : 0);
-    foff[j] = (sc[j].sc[0] * g.G[1] + sc[j].sc[1]) * g.G[2] + sc[j].sc[2];
-  }
-  struct Prep {
-    int h, b, c[3];  // c: the window's first grid coordinate in each dim (a box's corner)
-    bool box;
-    int src[4];
-    uint32_t reg4;
-    bool lvec;         // land[0] holds the four land bytes
-    uint32_t land[4];  // raw bytes: consumed one item later
-    float lse[4];
-  };
-  auto prep = [&](const ItemCursor &cu, Prep &p) {
-    p.h = cu.h;
-    p.b = cu.b;
-    int wc[3];
-    window_coords(g, cu.omega, wc);
-    p.box = true;
-#pragma unroll
-    for (int d = 0; d < 3; ++d) {
-      p.c[d] = wc[d] * g.w[d] + g.s[d];
-      p.box = p.box && p.c[d] + g.w[d] <= g.G[d];
-    }
-    const int org = (p.c[0] * g.G[1] + p.c[1]) * g.G[2] + p.c[2];
-    const int64_t tok0 = (int64_t)cu.b * g.tokens;
-    p.reg4 = 0;
+  // The one-window forward keeps the gather code from before two-window items
+  // existed: measured, the general body below slowed that kernel by 2-4 %
+  // (instruction layout; the work is the same), while it runs the backward
+  // slightly faster.
+  if constexpr (kPack == 1 && !kSplitMasks) {
+    const int n = g.n, nq4 = (n + 3) >> 2;
+    SlotCoord sc[4];
+    int foff[4];  // token offset of slot 4l + j from the window's origin when the window is a box
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      int src = -1, reg = 0;
-      if (4 * lane + j < n) {
-        if (p.box) {
-          src = org + foff[j];
-        } else {
-          const SlotRoute r = route_slot(g, wc, sc[j]);
-          src = r.src;
-          reg = r.reg;
-        }
-      }
-      p.src[j] = src;
-      p.reg4 |= (uint32_t)reg << (8 * j);
+      const int slot = 4 * lane + j;
+      sc[j] = slot_coord(g, slot < n ? slot : 0);
+      foff[j] = (sc[j].sc[0] * g.G[1] + sc[j].sc[1]) * g.G[2] + sc[j].sc[2];
     }
-    // land bytes (and LSE values) are read by warp 0 alone, which writes the
-    // slot metadata and both mask tiles. The four slots of a lane are four
-    // consecutive tokens of one row of a box window when w2 % 4 == 0: then
-    // they come as one 4-byte (16-byte) load if it is aligned.
-    p.lvec = false;
-    if (pw != 0 && !kSplitMasks) return;
-    const bool run4 = p.box && (g.w[2] & 3) == 0 && 4 * lane + 3 < n;
-    const int64_t lt = tok0 + p.src[0];
-    const int64_t lo = ((int64_t)cu.b * g.heads + cu.h) * g.tokens + p.src[0];
-    if (land) {
-      if (run4 && (lt & 3) == 0) {
-        p.lvec = true;
-        p.land[0] = __ldg(reinterpret_cast<const unsigned int *>(land + lt));
-      } else {
+    struct Prep {
+      int h, b, c[3];  // c: the window's first grid coordinate in each dim (a box's corner)
+      bool box;
+      int src[4];
+      uint32_t reg4;
+      bool lvec;         // land[0] holds the four land bytes
+      uint32_t land[4];  // raw bytes: consumed one item later
+      float lse[4];
+    };
+    auto prep = [&](const ItemCursor &cu, Prep &p) {
+      p.h = cu.h;
+      p.b = cu.b;
+      int wc[3];
+      window_coords(g, cu.omega, wc);
+      p.box = true;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 ? __ldg(land + tok0 + p.src[j]) : 0u;
+      for (int d = 0; d < 3; ++d) {
+        p.c[d] = wc[d] * g.w[d] + g.s[d];
+        p.box = p.box && p.c[d] + g.w[d] <= g.G[d];
       }
-    }
-    if (lse && pw == 0) {
-      if (run4 && (lo & 3) == 0) {
-        const float4 l4 = __ldg(reinterpret_cast<const float4 *>(lse + lo));
-        p.lse[0] = l4.x;
-        p.lse[1] = l4.y;
-        p.lse[2] = l4.z;
-        p.lse[3] = l4.w;
-      } else {
-        const float *lrow = lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 ? __ldg(lrow + p.src[j]) : 0.f;
-      }
-    }
-  };
-  ItemCursor cur;
-  Prep pc, pn;
-  if (count > 0) {
-    cur.init(g, L);
-    prep(cur, pc);
-  }
-  int64_t it = 0;
-  for (; it < count; ++it) {
-    const int s = (int)(it % kStages);
-    ItemCursor nx = cur;
-    nx.next(g);
-    if (it + 1 < count) prep(nx, pn);
-    if (it >= kStages && !mbar_wait_warp(empty0 + 8u * s, (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
-    const uint32_t st = sbase + s * lay.bytes, full = full0 + 8u * s;
-    uint8_t *sp = smem + s * lay.bytes;
-    const Prep &p = pc;
-    if (lane == 0 && ntiles > 0) mbar_expect_tx(full, (uint32_t)(ntiles * (p.box ? n * 64 : nq4 * 256)));
-    __syncwarp();
-    const int x = p.h * 32;
-    if (ntiles == 0) {
-      // warp 0: no operand tiles
-    } else if (p.box) {
-      if (lane == 0) {
-        tma_load_5d(st + tile_a, &ma->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
-        if (ntiles > 1) tma_load_5d(st + tile_b, &mb->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
-      }
-    } else if (lane < nq4) {
-      const int r0 = p.b * g.tokens;  // row of token 0 of the image in the [B*T, C] view
-      const int r[4] = {r0 + max(p.src[0], 0), r0 + max(p.src[1], 0), r0 + max(p.src[2], 0), r0 + max(p.src[3], 0)};
-      tma_gather4(st + tile_a + 256u * lane, &ma->rows, x, r[0], r[1], r[2], r[3], full);
-      if (ntiles > 1) tma_gather4(st + tile_b + 256u * lane, &mb->rows, x, r[0], r[1], r[2], r[3], full);
-    }
-    bool live[4] = {false, false, false, false};
-    if (kSplitMasks || pw == 0) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        live[j] = p.src[j] >= 0 && (!land || (p.lvec ? ((p.land[0] >> (8 * j)) & 0xffu) : p.land[j]) == 0);
-    }
-    if (pw == 0) {
-      *reinterpret_cast<int4 *>(sp + lay.src + 16 * lane) = make_int4(p.src[0], p.src[1], p.src[2], p.src[3]);
-      *reinterpret_cast<uint32_t *>(sp + lay.live + 4 * lane) =
-          (live[0] ? 1u : 0u) | (live[1] ? 0x100u : 0u) | (live[2] ? 0x10000u : 0u) | (live[3] ? 0x1000000u : 0u);
-      if (lse)
-        *reinterpret_cast<float4 *>(sp + lay.lse2 + 16 * lane) =
-            make_float4(live[0] ? p.lse[0] * kLog2e : 0.f, live[1] ? p.lse[1] * kLog2e : 0.f,
-                        live[2] ? p.lse[2] * kLog2e : 0.f, live[3] ? p.lse[3] * kLog2e : 0.f);
-    }
-    if (kSplitMasks ? pw != 0 : pw == 0) {
+      const int org = (p.c[0] * g.G[1] + p.c[1]) * g.G[2] + p.c[2];
+      const int64_t tok0 = (int64_t)cu.b * g.tokens;
+      p.reg4 = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int slot = 4 * lane + j, reg = (int)((p.reg4 >> (8 * j)) & 0xffu);
-        if (slot < n) {
-          if (!kSplitMasks || pw == 1)
-            *reinterpret_cast<uint4 *>(sp + lay.qm + sw32(slot, 0)) = mask_row_chunk0(live[j], reg, false);
-          if (!kSplitMasks || pw == 2)
-            *reinterpret_cast<uint4 *>(sp + lay.km + sw32(slot, 0)) = mask_row_chunk0(live[j], reg, true);
+        int src = -1, reg = 0;
+        if (4 * lane + j < n) {
+          if (p.box) {
+            src = org + foff[j];
+          } else {
+            const SlotRoute r = route_slot(g, wc, sc[j]);
+            src = r.src;
+            reg = r.reg;
+          }
+        }
+        p.src[j] = src;
+        p.reg4 |= (uint32_t)reg << (8 * j);
+      }
+      // land bytes (and LSE values) are read by warp 0 alone, which writes the
+      // slot metadata and both mask tiles. The four slots of a lane are four
+      // consecutive tokens of one row of a box window when w2 % 4 == 0: then
+      // they come as one 4-byte (16-byte) load if it is aligned.
+      p.lvec = false;
+      if (pw != 0 && !kSplitMasks) return;
+      const bool run4 = p.box && (g.w[2] & 3) == 0 && 4 * lane + 3 < n;
+      const int64_t lt = tok0 + p.src[0];
+      const int64_t lo = ((int64_t)cu.b * g.heads + cu.h) * g.tokens + p.src[0];
+      if (land) {
+        if (run4 && (lt & 3) == 0) {
+          p.lvec = true;
+          p.land[0] = __ldg(reinterpret_cast<const unsigned int *>(land + lt));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 ? __ldg(land + tok0 + p.src[j]) : 0u;
         }
       }
+      if (lse && pw == 0) {
+        if (run4 && (lo & 3) == 0) {
+          const float4 l4 = __ldg(reinterpret_cast<const float4 *>(lse + lo));
+          p.lse[0] = l4.x;
+          p.lse[1] = l4.y;
+          p.lse[2] = l4.z;
+          p.lse[3] = l4.w;
+        } else {
+          const float *lrow = lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 ? __ldg(lrow + p.src[j]) : 0.f;
+        }
+      }
+    };
+    ItemCursor cur;
+    Prep pc, pn;
+    if (count > 0) {
+      cur.init(g, L);
+      prep(cur, pc);
     }
-    fence_proxy_async_smem();  // mask rows are read by the tensor cores
-    mbar_arrive_warp(full);
-    cur = nx;
-    pc = pn;
+    int64_t it = 0;
+    for (; it < count; ++it) {
+      const int s = (int)(it % kStages);
+      ItemCursor nx = cur;
+      nx.next(g);
+      if (it + 1 < count) prep(nx, pn);
+      if (it >= kStages && !mbar_wait_warp(empty0 + 8u * s, (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      const uint32_t st = sbase + s * lay.bytes, full = full0 + 8u * s;
+      uint8_t *sp = smem + s * lay.bytes;
+      const Prep &p = pc;
+      if (lane == 0 && ntiles > 0) mbar_expect_tx(full, (uint32_t)(ntiles * (p.box ? n * 64 : nq4 * 256)));
+      __syncwarp();
+      const int x = p.h * 32;
+      if (ntiles == 0) {
+        // warp 0: no operand tiles
+      } else if (p.box) {
+        if (lane == 0) {
+          tma_load_5d(st + tile_a, &ma->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
+          if (ntiles > 1) tma_load_5d(st + tile_b, &mb->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
+        }
+      } else if (lane < nq4) {
+        const int r0 = p.b * g.tokens;  // row of token 0 of the image in the [B*T, C] view
+        const int r[4] = {r0 + max(p.src[0], 0), r0 + max(p.src[1], 0), r0 + max(p.src[2], 0), r0 + max(p.src[3], 0)};
+        tma_gather4(st + tile_a + 256u * lane, &ma->rows, x, r[0], r[1], r[2], r[3], full);
+        if (ntiles > 1) tma_gather4(st + tile_b + 256u * lane, &mb->rows, x, r[0], r[1], r[2], r[3], full);
+      }
+      bool live[4] = {false, false, false, false};
+      if (kSplitMasks || pw == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          live[j] = p.src[j] >= 0 && (!land || (p.lvec ? ((p.land[0] >> (8 * j)) & 0xffu) : p.land[j]) == 0);
+      }
+      if (pw == 0) {
+        *reinterpret_cast<int4 *>(sp + lay.src + 16 * lane) = make_int4(p.src[0], p.src[1], p.src[2], p.src[3]);
+        *reinterpret_cast<uint32_t *>(sp + lay.live + 4 * lane) =
+            (live[0] ? 1u : 0u) | (live[1] ? 0x100u : 0u) | (live[2] ? 0x10000u : 0u) | (live[3] ? 0x1000000u : 0u);
+        if (lse)
+          *reinterpret_cast<float4 *>(sp + lay.lse2 + 16 * lane) =
+              make_float4(live[0] ? p.lse[0] * kLog2e : 0.f, live[1] ? p.lse[1] * kLog2e : 0.f,
+                          live[2] ? p.lse[2] * kLog2e : 0.f, live[3] ? p.lse[3] * kLog2e : 0.f);
+      }
+      if (kSplitMasks ? pw != 0 : pw == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int slot = 4 * lane + j, reg = (int)((p.reg4 >> (8 * j)) & 0xffu);
+          if (slot < n) {
+            if (!kSplitMasks || pw == 1)
+              *reinterpret_cast<uint4 *>(sp + lay.qm + sw32(slot, 0)) = mask_row_chunk0(live[j], reg, false);
+            if (!kSplitMasks || pw == 2)
+              *reinterpret_cast<uint4 *>(sp + lay.km + sw32(slot, 0)) = mask_row_chunk0(live[j], reg, true);
+          }
+        }
+      }
+      fence_proxy_async_smem();  // mask rows are read by the tensor cores
+      mbar_arrive_warp(full);
+      cur = nx;
+      pc = pn;
+    }
+    // Copies still in flight must land before the CTA exits. Unless a role gave
+    // up early these stages were consumed already and the waits return at once.
+    volatile int no_abort = 0;
+    const WaitCtl dctl{&no_abort, ctl.status, ctl.limit_ns < 50000000ull ? ctl.limit_ns : 50000000ull};
+    for (int64_t k = it > kStages ? it - kStages : 0; k < it; ++k)
+      mbar_wait_warp(full0 + 8u * (uint32_t)(k % kStages), (uint32_t)(k / kStages) & 1u, dctl);
+  } else {
+    const int n = g.n, nq4 = (n + 3) >> 2;
+    // The lane's tile rows 4l .. 4l+3 belong to window u of the item (the
+    // second window starts at row offb, a multiple of 16) and hold its slots
+    // s0 .. s0+3.
+    const int u = (kPack == 2 && 4 * lane >= g.offb) ? 1 : 0;
+    const int s0 = 4 * lane - u * g.offb;
+    SlotCoord sc[4];
+    int foff[4];  // token offset of slot s0 + j from the window's origin when the window is a box
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int slot = s0 + j;
+      sc[j] = slot_coord(g, slot < n ? slot : 0);
+      foff[j] = (sc[j].sc[0] * g.G[1] + sc[j].sc[1]) * g.G[2] + sc[j].sc[2];
+    }
+    struct Prep {
+      int h, b, c[3];  // c: the lane's window's first grid coordinate in each dim (a box's corner)
+      bool box;        // the lane's window is one box
+      bool has;        // the lane's window exists (the item may hold one window only)
+      uint32_t tx;     // bytes one tile of the item brings in (both windows)
+      int src[4];
+      uint32_t reg4;
+      bool lvec;         // land[0] holds the four land bytes
+      uint32_t land[4];  // raw bytes: consumed one item later
+      float lse[4];
+    };
+    auto prep = [&](const ItemCursor &cu, Prep &p) {
+      p.h = cu.h;
+      p.b = cu.b;
+      int wc[3] = {0, 0, 0};
+      p.tx = 0;
+      p.has = false;
+      p.box = false;
+#pragma unroll
+      for (int uu = 0; uu < kPack; ++uu) {
+        if (uu == 1 && !cu.has2(g)) break;
+        int wcu[3], cc[3];
+        window_coords(g, uu == 0 ? cu.omega : cu.omega2(g), wcu);
+        bool box = true;
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+          cc[d] = wcu[d] * g.w[d] + g.s[d];
+          box = box && cc[d] + g.w[d] <= g.G[d];
+        }
+        p.tx += box ? (uint32_t)n * 64u : (uint32_t)nq4 * 256u;
+        if (uu == u) {
+          p.has = true;
+          p.box = box;
+#pragma unroll
+          for (int d = 0; d < 3; ++d) {
+            wc[d] = wcu[d];
+            p.c[d] = cc[d];
+          }
+        }
+      }
+      const int org = (p.c[0] * g.G[1] + p.c[1]) * g.G[2] + p.c[2];
+      const int64_t tok0 = (int64_t)cu.b * g.tokens;
+      p.reg4 = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        int src = -1, reg = 0;
+        if (p.has && s0 + j < n) {
+          if (p.box) {
+            src = org + foff[j];
+          } else {
+            const SlotRoute r = route_slot(g, wc, sc[j]);
+            src = r.src;
+            reg = r.reg;
+          }
+        }
+        p.src[j] = src;
+        p.reg4 |= (uint32_t)reg << (8 * j);
+      }
+      // land bytes (and LSE values) are read by warp 0 alone, which writes the
+      // slot metadata and both mask tiles. The four slots of a lane are four
+      // consecutive tokens of one row of a box window when w2 % 4 == 0: then
+      // they come as one 4-byte (16-byte) load if it is aligned.
+      p.lvec = false;
+      if (pw != 0 && !kSplitMasks) return;
+      const bool run4 = p.box && (g.w[2] & 3) == 0 && s0 + 3 < n;
+      const int64_t lt = tok0 + p.src[0];
+      const int64_t lo = ((int64_t)cu.b * g.heads + cu.h) * g.tokens + p.src[0];
+      if (land) {
+        if (run4 && (lt & 3) == 0) {
+          p.lvec = true;
+          p.land[0] = __ldg(reinterpret_cast<const unsigned int *>(land + lt));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 ? __ldg(land + tok0 + p.src[j]) : 0u;
+        }
+      }
+      if (lse && pw == 0) {
+        if (run4 && (lo & 3) == 0) {
+          const float4 l4 = __ldg(reinterpret_cast<const float4 *>(lse + lo));
+          p.lse[0] = l4.x;
+          p.lse[1] = l4.y;
+          p.lse[2] = l4.z;
+          p.lse[3] = l4.w;
+        } else {
+          const float *lrow = lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 ? __ldg(lrow + p.src[j]) : 0.f;
+        }
+      }
+    };
+    ItemCursor cur;
+    Prep pc, pn;
+    if (count > 0) {
+      cur.init(g, L);
+      prep(cur, pc);
+    }
+    int64_t it = 0;
+    for (; it < count; ++it) {
+      const int s = (int)(it % kStages);
+      ItemCursor nx = cur;
+      nx.next(g);
+      if (it + 1 < count) prep(nx, pn);
+      if (it >= kStages && !mbar_wait_warp(empty0 + 8u * s, (uint32_t)((it / kStages) - 1) & 1u, ctl)) break;
+      const uint32_t st = sbase + s * lay.bytes, full = full0 + 8u * s;
+      uint8_t *sp = smem + s * lay.bytes;
+      const Prep &p = pc;
+      if (lane == 0 && ntiles > 0) mbar_expect_tx(full, (uint32_t)ntiles * p.tx);
+      __syncwarp();
+      const int x = p.h * 32;
+      if (ntiles == 0 || !p.has) {
+        // warp 0 of the forward (no operand tiles), or no window in these rows
+      } else if (p.box) {
+        if (s0 == 0) {  // the window's first lane: rows [u * offb, u * offb + n)
+          const uint32_t row0 = (uint32_t)(u * g.offb) * 64u;
+          tma_load_5d(st + tile_a + row0, &ma->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
+          if (ntiles > 1) tma_load_5d(st + tile_b + row0, &mb->box, x, p.c[2], p.c[1], p.c[0], p.b, full);
+        }
+      } else if (s0 < n) {
+        const int r0 = p.b * g.tokens;  // row of token 0 of the image in the [B*T, C] view
+        const int r[4] = {r0 + max(p.src[0], 0), r0 + max(p.src[1], 0), r0 + max(p.src[2], 0), r0 + max(p.src[3], 0)};
+        tma_gather4(st + tile_a + 256u * lane, &ma->rows, x, r[0], r[1], r[2], r[3], full);
+        if (ntiles > 1) tma_gather4(st + tile_b + 256u * lane, &mb->rows, x, r[0], r[1], r[2], r[3], full);
+      }
+      bool live[4] = {false, false, false, false};
+      if (kSplitMasks || pw == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          live[j] = p.src[j] >= 0 && (!land || (p.lvec ? ((p.land[0] >> (8 * j)) & 0xffu) : p.land[j]) == 0);
+      }
+      if (pw == 0) {
+        *reinterpret_cast<int4 *>(sp + lay.src + 16 * lane) = make_int4(p.src[0], p.src[1], p.src[2], p.src[3]);
+        *reinterpret_cast<uint32_t *>(sp + lay.live + 4 * lane) =
+            (live[0] ? 1u : 0u) | (live[1] ? 0x100u : 0u) | (live[2] ? 0x10000u : 0u) | (live[3] ? 0x1000000u : 0u);
+        if (lse)
+          *reinterpret_cast<float4 *>(sp + lay.lse2 + 16 * lane) =
+              make_float4(live[0] ? p.lse[0] * kLog2e : 0.f, live[1] ? p.lse[1] * kLog2e : 0.f,
+                          live[2] ? p.lse[2] * kLog2e : 0.f, live[3] ? p.lse[3] * kLog2e : 0.f);
+      }
+      if (kSplitMasks ? pw != 0 : pw == 0) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // window u's region codes sit in mask columns 8u .. 8u+7 (chunk u)
+          const int row = 4 * lane + j, reg = (int)((p.reg4 >> (8 * j)) & 0xffu);
+          if (s0 + j < n) {
+            if (!kSplitMasks || pw == 1)
+              *reinterpret_cast<uint4 *>(sp + lay.qm + sw32(row, u)) = mask_row_chunk0(live[j], reg, false);
+            if (!kSplitMasks || pw == 2)
+              *reinterpret_cast<uint4 *>(sp + lay.km + sw32(row, u)) = mask_row_chunk0(live[j], reg, true);
+          }
+        }
+      }
+      fence_proxy_async_smem();  // mask rows are read by the tensor cores
+      mbar_arrive_warp(full);
+      cur = nx;
+      pc = pn;
+    }
+    // Copies still in flight must land before the CTA exits. Unless a role gave
+    // up early these stages were consumed already and the waits return at once.
+    volatile int no_abort = 0;
+    const WaitCtl dctl{&no_abort, ctl.status, ctl.limit_ns < 50000000ull ? ctl.limit_ns : 50000000ull};
+    for (int64_t k = it > kStages ? it - kStages : 0; k < it; ++k)
+      mbar_wait_warp(full0 + 8u * (uint32_t)(k % kStages), (uint32_t)(k / kStages) & 1u, dctl);
   }
-  // Copies still in flight must land before the CTA exits. Unless a role gave
-  // up early these stages were consumed already and the waits return at once.
-  volatile int no_abort = 0;
-  const WaitCtl dctl{&no_abort, ctl.status, ctl.limit_ns < 50000000ull ? ctl.limit_ns : 50000000ull};
-  for (int64_t k = it > kStages ? it - kStages : 0; k < it; ++k)
-    mbar_wait_warp(full0 + 8u * (uint32_t)(k % kStages), (uint32_t)(k / kStages) & 1u, dctl);
 }
 
 // ---------------------------------------------------------------- forward ---
@@ -319,6 +502,9 @@ constexpr int kThreads = (kMmaWarp + 1) * 32;
 // and key half h (the keys of softmax warpgroup h) at 256 + 64*b + 32*h
 constexpr uint32_t kTmemCols = 512, kColS = 0, kColO = 256;
 
+// kPack: windows per work item (1 or 2), a compile-time copy per value so
+// that the one-window kernel carries no code for the second window.
+template <int kPack>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const FwdArgs a, const __grid_constant__ TmaSet tmq, const __grid_constant__ TmaSet tmk,
                   const __grid_constant__ TmaSet tmv) {
@@ -332,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const Geo &g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = g.n, N = round16(n), NG = N >> 4;
+  const int N = round16(kPack == 2 ? g.rows : g.n), NG = N >> 4;  // key columns of the tile (both windows)
   int64_t L, R;
   eq4_range(a.items, a.ctas, blockIdx.x, L, R);
   const int64_t count = R - L;
@@ -358,22 +544,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // key side of every slot's bias row offset, for the bias-row builds
     int *roff = reinterpret_cast<int *>(smem + kRoff);
     int wc0[3] = {0, 0, 0};
-    if (threadIdx.x < 128) roff[threadIdx.x] = threadIdx.x < n ? slot_route(g, wc0, threadIdx.x).roff : 0;
+    if (threadIdx.x < 128) {
+      int u;
+      const int sg = tile_slot<kPack>(g, threadIdx.x, u);
+      roff[threadIdx.x] = sg >= 0 ? slot_route(g, wc0, sg).roff : 0;
+    }
   }
   // stage tiles start zeroed: box loads fill only the window's rows, and rows
   // past the last slot must stay finite for the MMAs
   for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
     reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  // key mask columns 8-15 are -2^100 for every row and item; slot rows past
-  // the window (n..127) are pads for every item: -2^100 in every column, no
-  // token (query mask rows stay zero)
+  // A row of window u has its region codes in mask columns 8u .. 8u+7; the
+  // other 8 key-mask columns are -2^100 for every item. Rows no window slot
+  // uses are pads for every item: -2^100 in every key-mask column, no token
+  // (query mask rows stay zero).
   for (int z = threadIdx.x; z < kStages * 128; z += blockDim.x) {
     const int st = z / 128, row = z % 128;
+    int u;
+    const int sg = tile_slot<kPack>(g, row, u);
     const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
-    *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
-    if (row >= n) {
-      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 0)) = make_uint4(nb2, nb2, nb2, nb2);
+    *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1 - u)) = make_uint4(nb2, nb2, nb2, nb2);
+    if (sg < 0) {
+      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, u)) = make_uint4(nb2, nb2, nb2, nb2);
       reinterpret_cast<int *>(smem + st * kStageBytes + kMeta)[row] = -1;
     }
   }
@@ -392,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pw = warp - kProducerWarp0;
     const StageLayout lay{kStageBytes, kQm, kKm, kMeta, kMeta + 512, 0};
     // warp 0: masks and metadata; warp 1: Q and K; warp 2: V
-    gather_role<kStages, false>(g, lay, pw == 0 ? 0 : pw == 1 ? 2 : 1, pw == 1 ? kQ : kV, kK, pw == 1 ? &tmq : &tmv,
+    gather_role<kStages, false, kPack>(g, lay, pw == 0 ? 0 : pw == 1 ? 2 : 1, pw == 1 ? kQ : kV, kK, pw == 1 ? &tmq : &tmv,
                          &tmk, g.has_land ? a.land : nullptr, nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl, L,
                          count, pw, lane);
   } else if (warp == kMmaWarp) {
@@ -509,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld_tied(o2, o3);
       tc_fence_before();
       mbar_arrive_warp(bar(bTFree + wb));
-      const bool store = i < n && src >= 0;
+      const bool store = src >= 0;  // pad rows carry src = -1
       {
         const float m = two ? fmaxf(m0, m1) : m0;
         const float a0 = ex2(m0 - m), a1 = two ? ex2(m1 - m) : 0.f;
@@ -561,7 +754,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float cs = a.scale * kLog2e;
     const float2 cs2 = make_float2(cs, cs);
     int wc0[3] = {0, 0, 0};
-    const int rbase = (i < n) ? slot_route(g, wc0, i).rbase : 0;
+    int ui;
+    const int si = tile_slot<kPack>(g, i, ui);  // this row's slot and window
+    const int rbase = si >= 0 ? slot_route(g, wc0, si).rbase : 0;
     int cur_h = -1;
     bool ok = true;
     if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
@@ -575,8 +770,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 16
         for (int jj = 0; jj < 64; ++jj) {
           const int j = 16 * gb + jj;
+          int uj;
+          const bool pair = si >= 0 && tile_slot<kPack>(g, j, uj) >= 0 && uj == ui;  // query and key of one window
           if (j < 16 * ge)
-            brow[j] = (bcol && i < n && j < n) ? __ldg(bcol + (int64_t)(rbase - roff[j]) * g.heads) * kLog2e : 0.f;
+            brow[j] = (bcol && pair) ? __ldg(bcol + (int64_t)(rbase - roff[j]) * g.heads) * kLog2e : 0.f;
         }
         cur_h = x.h;
       }
@@ -699,6 +896,7 @@ __device__ __forceinline__ uint32_t pds_chunk(int i, int c) {
   return (c >> 3) * 16384 + (i >> 3) * 1024 + (i & 7) * 128 + (((c & 7) ^ (i & 7)) << 4);
 }
 
+template <int kPack>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const BwdArgs a, const __grid_constant__ TmaSet tmq, const __grid_constant__ TmaSet tmk,
                   const __grid_constant__ TmaSet tmv, const __grid_constant__ TmaSet tmdo) {
@@ -712,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const Geo &g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = g.n, N = round16(n), NG = N >> 4;
+  const int N = round16(kPack == 2 ? g.rows : g.n), NG = N >> 4;  // key columns of the tile (both windows)
   int64_t L, R;
   eq4_range(a.items, a.ctas, blockIdx.x, L, R);
   const int64_t count = R - L;
@@ -743,15 +941,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
     reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
-  // key mask columns 8-15 are -2^100 for every row and item; slot rows past
-  // the window (n..127) are pads for every item: -2^100 in every column, no
-  // token (query mask rows stay zero)
+  // A row of window u has its region codes in mask columns 8u .. 8u+7; the
+  // other 8 key-mask columns are -2^100 for every item. Rows no window slot
+  // uses are pads for every item: -2^100 in every key-mask column, no token
+  // (query mask rows stay zero).
   for (int z = threadIdx.x; z < kStages * 128; z += blockDim.x) {
     const int st = z / 128, row = z % 128;
+    int u;
+    const int sg = tile_slot<kPack>(g, row, u);
     const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
-    *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1)) = make_uint4(nb2, nb2, nb2, nb2);
-    if (row >= n) {
-      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 0)) = make_uint4(nb2, nb2, nb2, nb2);
+    *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, 1 - u)) = make_uint4(nb2, nb2, nb2, nb2);
+    if (sg < 0) {
+      *reinterpret_cast<uint4 *>(smem + st * kStageBytes + kKm + sw32(row, u)) = make_uint4(nb2, nb2, nb2, nb2);
       reinterpret_cast<int *>(smem + st * kStageBytes + kMeta)[row] = -1;
     }
   }
@@ -770,7 +971,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pw = warp - kProducerWarp0;
     const StageLayout lay{kStageBytes, kQm, kKm, kMeta, kMeta + 1024, kMeta + 512};
     // warp 0: Q, dO and metadata; warp 1: K and the query masks; warp 2: V and the key masks
-    gather_role<kStages, true>(g, lay, pw == 0 ? 2 : 1, pw == 0 ? kQ : pw == 1 ? kK : kV, kdO,
+    gather_role<kStages, true, kPack>(g, lay, pw == 0 ? 2 : 1, pw == 0 ? kQ : pw == 1 ? kK : kV, kdO,
                                pw == 0 ? &tmq : pw == 1 ? &tmk : &tmv, &tmdo, g.has_land ? a.land : nullptr,
                                pw == 0 ? a.lse : nullptr, smem, sbase, bar(bFull), bar(bEmpty), ctl, L, count, pw,
                                lane);
@@ -842,7 +1043,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(bar(bAccFull), (uint32_t)it & 1u, ctl)) break;
       tc_fence_after();
       // one 32-column accumulator at a time: TMEM -> registers -> bf16 -> grid
-      const bool store = e < n && src >= 0;
+      const bool store = src >= 0;  // pad rows carry src = -1
       const int64_t off = ((int64_t)x.b * g.tokens + (store ? src : 0)) * g.C + (int64_t)x.h * 32;
       auto drain = [&](uint32_t col, void *base, float mul) {
         uint32_t lo[16], hi[16];
@@ -889,7 +1090,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float2 cs2 = make_float2(cs, cs);
     const bool want_db = a.ws != nullptr;
     int wc0[3] = {0, 0, 0};
-    const SlotRoute ri = slot_route(g, wc0, i < n ? i : 0);
+    int ui;
+    const int si = tile_slot<kPack>(g, i, ui);  // this row's slot and window
+    const SlotRoute ri = slot_route(g, wc0, si >= 0 ? si : 0);
     int cur_h = -1, h_first = -1;
     uint32_t wsync_phase = 0;
     bool ok = true;
@@ -921,6 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int qi = (i0 * g.w[1] + i1) * g.w[2] + i2;
               const int kj = ((i0 - dlt[0]) * g.w[1] + (i1 - dlt[1])) * g.w[2] + (i2 - dlt[2]);
               sum += acc[qi * kBiasStride + kj];
+              if (kPack == 2) sum += acc[(g.offb + qi) * kBiasStride + g.offb + kj];  // the second window
             }
         a.ws[(int64_t)slot * g.T + t] = sum;
       }
@@ -936,8 +1140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (cur_h >= 0 && want_db && !flush(a.slot_base[blockIdx.x] + (cur_h - h_first))) break;
         for (int j = 16 * gb; j < 16 * ge; ++j) {
           float b = 0.f;
-          if (i < n && j < n && a.bias)
-            b = a.bias[(int64_t)(ri.rbase - slot_route(g, wc0, j).roff) * g.heads + x.h] * kLog2e;
+          int uj;
+          const int sj = tile_slot<kPack>(g, j, uj);
+          if (si >= 0 && sj >= 0 && uj == ui && a.bias)  // query and key of one window
+            b = a.bias[(int64_t)(ri.rbase - slot_route(g, wc0, sj).roff) * g.heads + x.h] * kLog2e;
           brow[j] = b;
         }
         if (want_db) {
@@ -1151,7 +1357,7 @@ bool tensor_maps(TmaSet *t, const void *base, const Geo &g) {
 int launch_fwd_tc(const FwdArgs &a, void *stream) {
   TmaSet mq, mk, mv;
   if (!tensor_maps(&mq, a.q, a.g) || !tensor_maps(&mk, a.k, a.g) || !tensor_maps(&mv, a.v, a.g)) return SWIN_ERR_CUDA;
-  auto kern = fwd::fwd_tc_kernel;
+  auto kern = a.g.pack == 2 ? fwd::fwd_tc_kernel<2> : fwd::fwd_tc_kernel<1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, fwd::kSmemBytes) != cudaSuccess)
     return SWIN_ERR_CUDA;
   kern<<<a.ctas, fwd::kThreads, fwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mk, mv);
@@ -1163,7 +1369,7 @@ int launch_bwd_tc(const BwdArgs &a, void *stream) {
   if (!tensor_maps(&mq, a.q, a.g) || !tensor_maps(&mk, a.k, a.g) || !tensor_maps(&mv, a.v, a.g) ||
       !tensor_maps(&mdo, a.dout, a.g))
     return SWIN_ERR_CUDA;
-  auto kern = bwd::bwd_tc_kernel;
+  auto kern = a.g.pack == 2 ? bwd::bwd_tc_kernel<2> : bwd::bwd_tc_kernel<1>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bwd::kSmemBytes) != cudaSuccess)
     return SWIN_ERR_CUDA;
   kern<<<a.ctas, bwd::kThreads, bwd::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mk, mv, mdo);

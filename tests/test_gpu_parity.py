@@ -116,6 +116,11 @@ SWEEP = [
     ((9, 30), (3, 7), (2, 3), (1, 1), 3, 32, 1, "bf16", (0.2, 0.2)),     # n = 21
     # w2 = 4 with an odd lon shift: box rows not 4-token aligned (scalar land/LSE loads)
     ((4, 12, 20), (2, 4, 4), (1, 2, 1), (0, 0, 1), 2, 32, 1, "bf16", (0.3, 0.5)),
+    # two windows per tensor-core item: 9 windows (the last item holds one),
+    # a 3-D case, and n = 60 (second window from tile row 64, 124 rows used)
+    ((11, 21), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3)),
+    ((3, 10, 13), (2, 4, 4), (1, 2, 2), (0, 0, 1), 2, 32, 2, "bf16", (0.3, 0.5)),
+    ((13, 31), (6, 10), (3, 5), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3)),
 ]
 
 
@@ -126,6 +131,18 @@ def test_small_sweep(case, impl):
     wl = workloads.custom(grid, window, shift, periodic, heads, hd, batch, dtype, land_p,
                           seed_index=300 + SWEEP.index(case))
     _full_parity(wl, workloads.generate(wl), impl)
+
+
+@pytest.mark.parametrize("grid, window, windows, per_item",
+                         [((11, 21), (4, 8), 9, 2), ((13, 31), (6, 10), 12, 2), ((11, 21), (8, 9), 6, 1)])
+def test_two_windows_per_item_when_they_fit(grid, window, windows, per_item):
+    # the tensor-core plan puts two windows in one 128-row tile when the
+    # second can start on a 16-row boundary (round16(n) + n <= 128)
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    attn = SwinWindowAttention(grid, window, (window[0] // 2, window[1] // 2), (0, 1), 2, 32, 1, "bf16")
+    info = attn.info
+    assert info.impl == 2 and info.windows_per_image == windows
+    assert info.work_items == 2 * -(-windows // per_item)
 
 
 def test_all_land_image_gives_zero_output():
