@@ -756,6 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int wc0[3] = {0, 0, 0};
     int ui;
     const int si = tile_slot<kPack>(g, i, ui);  // this row's slot and window
+    // With two windows per item, warpgroup grp's key columns are exactly
+    // window grp's (the second window starts at column offb = 16 * ng0): a
+    // warp whose rows all belong to the other window (or are pads) has only
+    // masked keys in its half and writes P = 0 without computing it.
+    const bool idle = kPack == 2 && !__any_sync(0xffffffffu, si >= 0 && ui == grp);
     const int rbase = si >= 0 ? slot_route(g, wc0, si).rbase : 0;
     int cur_h = -1;
     bool ok = true;
@@ -781,6 +786,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tS = tmem + lane_addr + kColS + 128u * wb;
       if (!mbar_wait_warp(bar(bSFull + wb), (uint32_t)(it >> 1) & 1u, ctl)) break;
       tc_fence_after();
+      if (idle) {
+        const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          if (gb + k4 < ge) tmem_st8(tS + 16u * (gb + k4), z);
+        xmax[xs * 256 + grp * 128 + i] = -1e30f;  // weight exp2(-1e30 - m) = 0 in the epilogue
+        xsum[xs * 256 + grp * 128 + i] = 0.f;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive_warp(bar(bPFull + wb));
+        continue;
+      }
       uint32_t sv[4][16];
 #pragma unroll
       for (int k4 = 0; k4 < 4; ++k4)
@@ -1092,6 +1109,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int wc0[3] = {0, 0, 0};
     int ui;
     const int si = tile_slot<kPack>(g, i, ui);  // this row's slot and window
+    // With two windows per item, warpgroup grp's key columns are exactly
+    // window grp's: a warp whose rows all belong to the other window (or are
+    // pads) has P = dS = 0 in its half; it writes those zeros to the P and
+    // dS tiles and adds nothing to delta or dBias.
+    const bool idle = kPack == 2 && !__any_sync(0xffffffffu, si >= 0 && ui == grp);
+    auto zero_chunks = [&](int tile) {
+      for (int c = 2 * gb; c < 2 * ge; ++c)
+        *reinterpret_cast<uint4 *>(smem + tile + pds_chunk(i, c)) = make_uint4(0u, 0u, 0u, 0u);
+    };
     const SlotRoute ri = slot_route(g, wc0, si >= 0 ? si : 0);
     int cur_h = -1, h_first = -1;
     uint32_t wsync_phase = 0;
@@ -1190,7 +1216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4 *>(smem + kP + pds_chunk(i, 2 * gi)) = make_uint4(pb[0], pb[1], pb[2], pb[3]);
         *reinterpret_cast<uint4 *>(smem + kP + pds_chunk(i, 2 * gi + 1)) = make_uint4(pb[4], pb[5], pb[6], pb[7]);
       };
-      {
+      if (idle) {
+        zero_chunks(kP);
+      } else {
         // two groups per TMEM round trip: tcgen05.wait::ld waits for every
         // load in flight, so a double buffer would wait just as often, and
         // the round trips (not the arithmetic) set this pass's length
@@ -1244,7 +1272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (want_db) tmem_st8(tAcc + 8u * sg, av);
         *reinterpret_cast<uint4 *>(smem + kdS + pds_chunk(i, sg)) = make_uint4(db[0], db[1], db[2], db[3]);
       };
-      {
+      if (idle) {
+        zero_chunks(kdS);
+      } else {
         uint32_t p0[8], d0[8], a0[8], p1[8], d1[8], a1[8];
         auto load3 = [&](int sg, uint32_t (&pv)[8], uint32_t (&dpv)[8], uint32_t (&av)[8]) {
           tmem_ld8(tS + 8u * sg, pv);
