@@ -476,7 +476,8 @@ constexpr int kBiasStride = 132;
 constexpr int kBarOff = kBias + 128 * kBiasStride * 4;
 // barrier indices
 constexpr int bFull = 0, bEmpty = kStages, bSFull = 2 * kStages, bPFull = bSFull + 2, bOFull = bPFull + 2,
-              bTFree = bOFull + 2, bNever = bTFree + 2, bDrain = bNever + 1, kNumBars = bDrain + 1;
+              bTFree = bOFull + 2, bNever = bTFree + 2, bDrain = bNever + 1, bBsync = bDrain + 1,
+              kNumBars = bBsync + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
 // Per-item exchange slots from the softmax to the epilogue warps (slot it % 4):
 // float max[4][2][128] and float sum[4][2][128], one value per half row;
@@ -486,7 +487,12 @@ constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag
 constexpr int kXchgSlots = 4;
 constexpr int kXchg = (kMiscOff + 16 + 127) & ~127;
 constexpr int kRoff = kXchg + kXchgSlots * 2 * 2 * 128 * 4;
-constexpr int kOStage = (kRoff + 512 + 127) & ~127;  // 4 epilogue warps x 2 KB store staging (16-byte stores)
+// the current head's bias column (bias*log2e, up to kMaxBiasRows rows), staged
+// once per head by the softmax warps: the table is read by every CTA at once,
+// and one load per row and CTA keeps that hot spot cool
+constexpr int kMaxBiasRows = 768;
+constexpr int kBvec = (kRoff + 512 + 127) & ~127;
+constexpr int kOStage = kBvec + kMaxBiasRows * 4;  // 4 epilogue warps x 2 KB store staging (16-byte stores)
 constexpr int kSmemBytes = kOStage + 8192 + 1024;    // + alignment slack
 static_assert(kStageBytes % 1024 == 0 && kBias % 16 == 0, "stage tiles need 1024-byte alignment");
 static_assert(kXchg % 16 == 0 && kOStage % 16 == 0, "vector accesses need 16-byte alignment");
@@ -536,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(bTFree + w), 4);  // epilogue warps
     }
     mbar_init(bar(bNever), 1);
+    mbar_init(bar(bBsync), kSoftmaxWarps);
     mbar_init(bar(bDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -763,6 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool idle = kPack == 2 && !__any_sync(0xffffffffu, si >= 0 && ui == grp);
     const int rbase = si >= 0 ? slot_route(g, wc0, si).rbase : 0;
     int cur_h = -1;
+    uint32_t bs_phase = 0;
+    float *bvec = reinterpret_cast<float *>(smem + kBvec);
     bool ok = true;
     if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
     ItemCursor x;
@@ -771,14 +780,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (x.h != cur_h) {
         // head change: this thread alone reads this half of bias row i; the
         // loads are independent so their latencies overlap
-        const float *bcol = a.bias ? a.bias + x.h : nullptr;
+        // The head's bias column goes to shared memory first (one load per
+        // row and CTA; every CTA reads the table at once, and 64 loads per
+        // thread made it an L2 hot spot, about 20 us per head change), then
+        // each thread builds its half row from there.
+        if (cur_h >= 0) {  // everyone is done with the previous column
+          mbar_arrive_warp(bar(bBsync));
+          if (!mbar_wait_warp(bar(bBsync), bs_phase & 1u, ctl)) break;
+          ++bs_phase;
+        }
+        for (int t = grp * 128 + i; t < g.T; t += 256)
+          bvec[t] = a.bias ? __ldg(a.bias + (int64_t)t * g.heads + x.h) * kLog2e : 0.f;
+        mbar_arrive_warp(bar(bBsync));
+        if (!mbar_wait_warp(bar(bBsync), bs_phase & 1u, ctl)) break;
+        ++bs_phase;
 #pragma unroll 16
         for (int jj = 0; jj < 64; ++jj) {
           const int j = 16 * gb + jj;
           int uj;
           const bool pair = si >= 0 && tile_slot<kPack>(g, j, uj) >= 0 && uj == ui;  // query and key of one window
-          if (j < 16 * ge)
-            brow[j] = (bcol && pair) ? __ldg(bcol + (int64_t)(rbase - roff[j]) * g.heads) * kLog2e : 0.f;
+          if (j < 16 * ge) brow[j] = pair ? bvec[rbase - roff[j]] : 0.f;
         }
         cur_h = x.h;
       }
@@ -891,7 +912,8 @@ constexpr int bFull = 0, bEmpty = kStages, bSpFull = 2 * kStages, bPFull = bSpFu
               kNumBars = bVFree + 2;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
 constexpr int kDeltaOff = (kMiscOff + 16 + 127) & ~127;  // float [2][128]: the two halves of delta_i
-constexpr int kOStage = kDeltaOff + 1024;                // 4 epilogue warps x 2 KB store staging (16-byte stores)
+constexpr int kRoff = kDeltaOff + 1024;                  // int [128]: key side of every slot's bias row offset
+constexpr int kOStage = kRoff + 512;                     // 4 epilogue warps x 2 KB store staging (16-byte stores)
 constexpr int kSmemBytes = kOStage + 8192 + 1024;
 static_assert(kStageBytes % 1024 == 0 && kP % 1024 == 0 && kdS % 1024 == 0, "operand tiles need 1024-byte alignment");
 static_assert(kBias % 16 == 0 && kOStage % 16 == 0, "vector accesses need 16-byte alignment");
@@ -958,6 +980,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int z = threadIdx.x; z < kStages * kStageBytes / 16; z += blockDim.x)
     reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
+  {
+    int *ro = reinterpret_cast<int *>(smem + kRoff);
+    int wc0[3] = {0, 0, 0};
+    if (threadIdx.x < 128) {
+      int u;
+      const int sg = tile_slot<kPack>(g, threadIdx.x, u);
+      ro[threadIdx.x] = sg >= 0 ? slot_route(g, wc0, sg).roff : 0;
+    }
+  }
   // A row of window u has its region codes in mask columns 8u .. 8u+7; the
   // other 8 key-mask columns are -2^100 for every item. Rows no window slot
   // uses are pads for every item: -2^100 in every key-mask column, no token
@@ -1103,6 +1134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_addr + kColS, tdP = tmem + lane_addr + kColdP, tAcc = tmem + lane_addr + kColAcc;
     float *brow = reinterpret_cast<float *>(smem + kBias) + i * kBiasStride;
     float *dpart = reinterpret_cast<float *>(smem + kDeltaOff);
+    const int *roff = reinterpret_cast<const int *>(smem + kRoff);
     const float cs = a.scale * kLog2e;
     const float2 cs2 = make_float2(cs, cs);
     const bool want_db = a.ws != nullptr;
@@ -1164,14 +1196,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t it = 0; ok && it < count; ++it, x.next(g)) {
       if (x.h != cur_h) {
         if (cur_h >= 0 && want_db && !flush(a.slot_base[blockIdx.x] + (cur_h - h_first))) break;
+        // The head's bias column goes to shared memory first (one load per
+        // row and CTA; every CTA reads the table at once, and 64 loads per
+        // thread made it an L2 hot spot), staged in the P tile once dV, dK
+        // and dQ of the previous item are done with it; each thread then
+        // builds its half row from there, and all are done reading before
+        // pass 1 writes P.
+        float *bvec = reinterpret_cast<float *>(smem + kP);
+        if (it >= 1 && !mbar_wait_warp(bar(bDsFree), (uint32_t)(it - 1) & 1u, ctl)) break;
+        for (int t = tid; t < g.T; t += kSoftmaxThreads)
+          bvec[t] = a.bias ? __ldg(a.bias + (int64_t)t * g.heads + x.h) * kLog2e : 0.f;
+        mbar_arrive_warp(bar(bWsync));
+        if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) break;
+        ++wsync_phase;
         for (int j = 16 * gb; j < 16 * ge; ++j) {
-          float b = 0.f;
           int uj;
           const int sj = tile_slot<kPack>(g, j, uj);
-          if (si >= 0 && sj >= 0 && uj == ui && a.bias)  // query and key of one window
-            b = a.bias[(int64_t)(ri.rbase - slot_route(g, wc0, sj).roff) * g.heads + x.h] * kLog2e;
-          brow[j] = b;
+          brow[j] = si >= 0 && sj >= 0 && uj == ui ? bvec[ri.rbase - roff[j]] : 0.f;  // query and key of one window
         }
+        mbar_arrive_warp(bar(bWsync));
+        if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) break;
+        ++wsync_phase;
         if (want_db) {
           uint32_t z[16];
 #pragma unroll
@@ -1323,7 +1368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 bool tc_supported(const Geo &g, int dtype) {
   // gather rows are addressed as int32 rows of the [B*T, C] view
-  return dtype == SWIN_BF16 && g.hd == 32 && g.n <= 128 && (int64_t)g.batch * g.tokens <= INT32_MAX;
+  return dtype == SWIN_BF16 && g.hd == 32 && g.n <= 128 && g.T <= fwd::kMaxBiasRows &&
+         (int64_t)g.batch * g.tokens <= INT32_MAX;
 }
 int tc_fwd_ctas_per_sm(const Geo &) { return 1; }
 int tc_bwd_ctas_per_sm(const Geo &) { return 1; }
