@@ -93,6 +93,27 @@ __device__ __forceinline__ void store_rows_bf16(uint8_t *stage, const uint32_t (
   __syncwarp();
 }
 
+// One head's bias column (bias*log2e, 0 without a bias) held by the 256
+// softmax threads, thread t rows t, t+256, t+512 (at most 735 rows for a
+// window of up to 128 slots). It is loaded one head ahead, at kernel entry
+// for the first head and right after each head change for the next, so that
+// the shared-memory copy made at a head change waits on no load.
+struct BiasColumn {
+  float v[3];
+  __device__ __forceinline__ void load(const float *bias, const Geo &g, int h, int t) {
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int r = t + 256 * k;
+      v[k] = (bias && r < g.T) ? __ldg(bias + (int64_t)r * g.heads + h) * kLog2e : 0.f;
+    }
+  }
+  __device__ __forceinline__ void store(float *col, const Geo &g, int t) const {
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      if (t + 256 * k < g.T) col[t + 256 * k] = v[k];
+  }
+};
+
 // Where one item's mask rows and slot metadata sit in a stage (the operand
 // tiles, 128 slot rows x 64 B with 64-byte swizzle, are passed per warp).
 struct StageLayout {
@@ -529,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   eq4_range(a.items, a.ctas, blockIdx.x, L, R);
   const int64_t count = R - L;
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns};
+  BiasColumn bcol;  // softmax threads: the first head's column, in flight during the set-up
+  if (threadIdx.x < 256 && count > 0) bcol.load(a.bias, g, decode_item(g, L).h, threadIdx.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -770,6 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool idle = kPack == 2 && !__any_sync(0xffffffffu, si >= 0 && ui == grp);
     const int rbase = si >= 0 ? slot_route(g, wc0, si).rbase : 0;
     int cur_h = -1;
+    const int h_last = count > 0 ? decode_item(g, R - 1).h : 0;  // heads rise by one along the range
     uint32_t bs_phase = 0;
     float *bvec = reinterpret_cast<float *>(smem + kBvec);
     bool ok = true;
@@ -789,11 +813,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait_warp(bar(bBsync), bs_phase & 1u, ctl)) break;
           ++bs_phase;
         }
-        for (int t = grp * 128 + i; t < g.T; t += 256)
-          bvec[t] = a.bias ? __ldg(a.bias + (int64_t)t * g.heads + x.h) * kLog2e : 0.f;
+        bcol.store(bvec, g, grp * 128 + i);  // loaded one head ahead
         mbar_arrive_warp(bar(bBsync));
         if (!mbar_wait_warp(bar(bBsync), bs_phase & 1u, ctl)) break;
         ++bs_phase;
+        if (x.h < h_last) bcol.load(a.bias, g, x.h + 1, grp * 128 + i);
 #pragma unroll 16
         for (int jj = 0; jj < 64; ++jj) {
           const int j = 16 * gb + jj;
@@ -954,6 +978,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   eq4_range(a.items, a.ctas, blockIdx.x, L, R);
   const int64_t count = R - L;
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns};
+  BiasColumn bcol;  // softmax threads: the first head's column, in flight during the set-up
+  if (threadIdx.x < 256 && count > 0) bcol.load(a.bias, g, decode_item(g, L).h, threadIdx.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -1152,6 +1178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     const SlotRoute ri = slot_route(g, wc0, si >= 0 ? si : 0);
     int cur_h = -1, h_first = -1;
+    const int h_last = count > 0 ? decode_item(g, R - 1).h : 0;  // heads rise by one along the range
     uint32_t wsync_phase = 0;
     bool ok = true;
     if (a.debug_force_timeout) ok = mbar_wait_warp(bar(bNever), 0, ctl);
@@ -1204,8 +1231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // pass 1 writes P.
         float *bvec = reinterpret_cast<float *>(smem + kP);
         if (it >= 1 && !mbar_wait_warp(bar(bDsFree), (uint32_t)(it - 1) & 1u, ctl)) break;
-        for (int t = tid; t < g.T; t += kSoftmaxThreads)
-          bvec[t] = a.bias ? __ldg(a.bias + (int64_t)t * g.heads + x.h) * kLog2e : 0.f;
+        bcol.store(bvec, g, tid);  // loaded one head ahead
+        if (x.h < h_last) bcol.load(a.bias, g, x.h + 1, tid);
         mbar_arrive_warp(bar(bWsync));
         if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) break;
         ++wsync_phase;
