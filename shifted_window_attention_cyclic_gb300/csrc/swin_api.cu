@@ -233,6 +233,15 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
   }
   p->fwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, fwd_bps) * p->num_sms);
   p->bwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, bwd_bps) * p->num_sms);
+  if (p->impl == SWIN_IMPL_TC && g.heads <= p->num_sms) {
+    // A whole number of CTAs per head: the Eq. (4) split then gives CTA
+    // h*k + j the same windows of every head h, so CTAs of adjacent heads
+    // run in step and each 128-byte L2 fill (two heads' 64-byte rows of one
+    // token) is used by both. Otherwise they drift apart and the DRAM reads
+    // double.
+    const int k = p->num_sms / g.heads;
+    p->fwd_ctas = p->bwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)k * g.heads);
+  }
   // workspace slots: one partial dBias table per (CTA, head it touches)
   const int64_t per_head = (int64_t)g.batch * g.nitem;
   std::vector<int> slot_base(p->bwd_ctas), slot_head;
