@@ -121,6 +121,9 @@ SWEEP = [
     ((11, 21), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3)),
     ((3, 10, 13), (2, 4, 4), (1, 2, 2), (0, 0, 1), 2, 32, 2, "bf16", (0.3, 0.5)),
     ((13, 31), (6, 10), (3, 5), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3)),
+    # the largest bias table a 128-token window can have: 7 x 7 x 15 = 735
+    # offsets, ragged in all three dimensions; three heads over the CTAs
+    ((6, 9, 17), (4, 4, 8), (2, 2, 4), (0, 0, 1), 3, 32, 1, "bf16", (0.3, 0.5)),
 ]
 
 
