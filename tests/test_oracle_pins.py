@@ -351,3 +351,28 @@ def test_bwd_window_subset_matches_full(oracle_mod):
     o_sub, l_sub = oracle.fwd_windows(pb, q, k, v, bias, landm, win_ids=ids)
     np.testing.assert_array_equal(o_sub, o_full[ids])
     np.testing.assert_array_equal(l_sub, l_full[ids])
+
+
+@pytest.mark.parametrize("case", [FWD_CASES[1], FWD_CASES[4], ((9, 20), (3, 8), (1, 4), (1, 1), 2, 8, 2, True)])
+def test_bwd_softmax_gradient_sums(oracle_mod, case):
+    """Every softmax row sums to one, so its gradient row dS sums to zero.
+    Summed over all tokens (the route is a bijection): dBias sums to zero per
+    head, dK sums to zero per channel, and dV sums to the sum of dO over the
+    tokens whose output is not forced to zero (sea tokens). Using P or dS
+    untransposed for dK or dV breaks these sums, since column sums are not one
+    or zero."""
+    grid, window, shift, periodic, heads, hd, batch, land = case
+    pb = Problem(grid=grid, window=window, shift=shift, periodic=periodic, heads=heads, head_dim=hd,
+                 batch=batch, has_land=land)
+    q, k, v, bias, dout, landm = _inputs(pb, 31, land_p=0.3)
+    g = oracle.bwd(pb, q, k, v, bias, landm, dout)
+    C = pb.channels
+    scale = np.abs(g["dk"]).max() + np.abs(g["dbias"]).max()
+    np.testing.assert_allclose(g["dbias"].sum(axis=0), 0.0, atol=1e-12 * scale * g["dbias"].size)
+    np.testing.assert_allclose(g["dk"].reshape(-1, C).sum(axis=0), 0.0, atol=1e-12 * scale * g["dk"].size)
+    sea = np.ones(g["dv"].shape[:-1], bool) if landm is None else ~landm.astype(bool)
+    want = np.asarray(dout, np.float64)[sea].sum(axis=0)
+    np.testing.assert_allclose(g["dv"].reshape(-1, C).sum(axis=0), want, rtol=0, atol=1e-10)
+    if landm is not None:
+        for key in ("dq", "dk", "dv"):
+            assert np.all(g[key][~sea] == 0.0)
