@@ -66,15 +66,17 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_hash):
+def profiled_traffic(kernel_hash, workload, kernels, path=None):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, only if it was captured from the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    summary, only if it was captured from the current kernel sources, for
+    this workload and this kernel family; None otherwise."""
+    path = path or os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         t = json.load(f)
-    if t.get("kernel_source_hash") != kernel_hash:
+    if (t.get("kernel_source_hash") != kernel_hash or t.get("workload") != workload
+            or t.get("kernels") != kernels):
         return None
     return t.get("bwd_dram_bytes_per_launch")
 
@@ -404,6 +406,7 @@ def main():
         cpu = cpu_baseline(wl, x)
 
     if rank == 0:
+        kernels = {1: "simt", 2: "tcgen05"}[attn.info.impl]
         line = {
             "metric": METRIC, "value": value, "unit": "Mtokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -417,13 +420,14 @@ def main():
             "fwd_bwd": {"mtok_s": value / world, "roof_frac": (fwd_roof_us + bwd_roof_us) / (ms_per_step * 1e3)},
             "roofline": {"bound": "hbm", "kernel": "swin_attn_bwd (main kernel + dBias fold)",
                          "achieved": bwd_gbs, "peak": hbm, "unit": "GB/s", "frac": bwd_gbs / hbm,
-                         "peak_source": peak_kind, "traffic": profiled_traffic(khash),
+                         "peak_source": peak_kind,
+                         "traffic": profiled_traffic(khash, args.workload, kernels),
                          "alg_bytes_per_launch": bwd_bytes},
             "clocks": clocks,
             "e2e": {"value": job_rate(world, tokens, e2e_ms), "unit": "Mtokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": 3 * args.steps,
-            "impl_kernels": {1: "simt", 2: "tcgen05"}[attn.info.impl],
+            "impl_kernels": kernels,
             "kernel_source_hash": khash,
             "cpu_baseline": cpu,
         }
