@@ -57,6 +57,8 @@ def workload_counts(wl, win_src, land):
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources (csrc/*.cu, *.cuh) that the kernels and their
+    launch plans compile from; host-only .cpp files are not part of it."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shifted_window_attention_cyclic_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):

@@ -191,6 +191,20 @@ const char *swin_attn_strerror(int status);
  * split. Errors: INVALID_ARG (M < 0, P < 1, r outside [0, P), NULL). */
 int swin_attn_window_range(int64_t M, int64_t P, int64_t r, int64_t *L, int64_t *R);
 
+/* TERRA Sec. V.A, Eq. (3): the fixed (two-dimensional round-robin) window
+ * assignment over an m x n mesh pads each input dimension until every rank
+ * owns the same number of whole windows. For one dimension of `extent` input
+ * points, `stride` input points per token (patch size times sampling factor,
+ * p*alpha), `window` tokens per window and `ranks` mesh ranks along that
+ * dimension (m or n): *padded = ceil(extent / q) * q, q = stride*window*ranks.
+ * ranks = 1 gives the least padding to whole windows, the padding that the
+ * ragged assignment of Eq. (4) keeps. Host-only arithmetic; the attention
+ * kernels never pad (pad slots of ragged windows are masked instead).
+ * Errors: INVALID_ARG (extent, stride, window or ranks below 1, NULL, or a
+ * result above INT64_MAX). */
+int swin_attn_fixed_padded_extent(int64_t extent, int64_t stride, int64_t window, int64_t ranks,
+                                  int64_t *padded);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,6 +1,7 @@
 """Build the in-tree CUDA library libswin_attn.so for sm_103a with nvcc.
 
-Each .cu translation unit compiles in parallel to an object under _build/,
+Each .cu (and host-only .cpp) translation unit compiles in parallel to an
+object under _build/,
 then nvcc links the shared library next to this file (CUDA runtime linked
 statically, so loading the library needs no GPU).
 """
@@ -28,7 +29,7 @@ def _nvcc():
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
@@ -49,7 +50,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc] + ARCH + FLAGS + list(extra_flags) + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -94,6 +94,8 @@ def load_library():
     lib.swin_attn_strerror.restype = ctypes.c_char_p
     lib.swin_attn_window_range.argtypes = [i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.swin_attn_window_range.restype = ctypes.c_int
+    lib.swin_attn_fixed_padded_extent.argtypes = [i64, i64, i64, i64, ctypes.POINTER(i64)]
+    lib.swin_attn_fixed_padded_extent.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -239,6 +241,13 @@ def swin_attn_window_range(M: int, P: int, r: int):
     _check(load_library().swin_attn_window_range(M, P, r, ctypes.byref(L), ctypes.byref(R)),
            "swin_attn_window_range")
     return L.value, R.value
+
+
+def swin_attn_fixed_padded_extent(extent: int, stride: int, window: int, ranks: int) -> int:
+    padded = ctypes.c_int64()
+    _check(load_library().swin_attn_fixed_padded_extent(extent, stride, window, ranks, ctypes.byref(padded)),
+           "swin_attn_fixed_padded_extent")
+    return padded.value
 
 
 def swin_attn_strerror(code: int) -> str:

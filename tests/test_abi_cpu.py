@@ -1,6 +1,7 @@
 """C-ABI checks that need no GPU: the library loads, exports every entry point
 declared in include/swin_attn.h, rejects bad descriptors before touching CUDA,
-and its TERRA Eq. (4) window split matches the pages' worked examples."""
+and its TERRA Eq. (4) window split and Eq. (3) padding match the pages'
+worked examples."""
 import ctypes
 import os
 
@@ -113,3 +114,41 @@ def test_null_plan_is_rejected(lib):
     assert lib.swin_attn_status(None, None) == C.SWIN_ERR_INVALID_ARG
     assert lib.swin_attn_workspace_bytes(None) == 0
     lib.swin_attn_plan_destroy(None)
+
+
+def test_eq3_padding_matches_worked_example(lib):
+    with open(os.path.join(GOLDEN, "padding_eq3.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            head, vals = line.split(":")
+            H, W, stride, w, m, n = (int(x) for x in head.split())
+            mh, mw, pct = vals.split()
+            Hp = C.swin_attn_fixed_padded_extent(H, stride, w, m)
+            Wp = C.swin_attn_fixed_padded_extent(W, stride, w, n)
+            assert (Hp // (stride * w), Wp // (stride * w)) == (int(mh), int(mw))
+            assert Hp % (stride * w * m) == 0 and Wp % (stride * w * n) == 0
+            assert round(100.0 * (Hp * Wp / (H * W) - 1.0), 1) == float(pct)
+
+
+def test_eq3_padding_is_the_least_multiple(lib):
+    # Fig. 6 of TERRA Sec. V.A: a 9 x 5 window grid on a 2 x 2 mesh pads to
+    # 10 x 6 windows (extents counted in windows: stride = window = 1)
+    assert C.swin_attn_fixed_padded_extent(9, 1, 1, 2) == 10
+    assert C.swin_attn_fixed_padded_extent(5, 1, 1, 2) == 6
+    for extent in (1, 7, 8, 9, 255, 256, 257, 4320):
+        for stride, w, r in ((1, 1, 1), (8, 8, 1), (8, 128, 4), (4, 12, 3)):
+            q = stride * w * r
+            got = C.swin_attn_fixed_padded_extent(extent, stride, w, r)
+            assert got % q == 0 and extent <= got < extent + q
+
+
+def test_eq3_padding_rejects_bad_arguments(lib):
+    bad = [(0, 8, 8, 1), (10, 0, 8, 1), (10, 8, 0, 1), (10, 8, 8, 0), (-1, 8, 8, 1),
+           (2 ** 62, 2 ** 31, 2 ** 31, 2), (2 ** 63 - 1, 1, 1, 2)]
+    out = ctypes.c_int64(-7)
+    for args in bad:
+        assert lib.swin_attn_fixed_padded_extent(*args, ctypes.byref(out)) == C.SWIN_ERR_INVALID_ARG
+        assert out.value == -7
+    assert lib.swin_attn_fixed_padded_extent(10, 8, 8, 1, None) == C.SWIN_ERR_INVALID_ARG
