@@ -152,3 +152,15 @@ def test_eq3_padding_rejects_bad_arguments(lib):
         assert lib.swin_attn_fixed_padded_extent(*args, ctypes.byref(out)) == C.SWIN_ERR_INVALID_ARG
         assert out.value == -7
     assert lib.swin_attn_fixed_padded_extent(10, 8, 8, 1, None) == C.SWIN_ERR_INVALID_ARG
+
+
+def test_missing_library_raises_no_fallback(monkeypatch):
+    # without the CUDA library every entry point raises; nothing falls back
+    monkeypatch.setattr(C, "_lib", None)
+    monkeypatch.setattr(C, "LIB_PATH", os.path.join(GOLDEN, "no_such_libswin_attn.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        C.load_library()
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        C.swin_attn_window_range(10, 4, 0)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        C.swin_attn_plan(C.make_desc((8, 16), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16"))
