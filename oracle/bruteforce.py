@@ -73,7 +73,8 @@ def fwd(pb, q, k, v, bias, land=None):
             l = e.sum(1, keepdims=True)
             p = e / np.where(l > 0, l, 1.0)
             o[b, :, h] = p @ v[b, :, h]
-            lse[b, h] = (m + np.log(l))[:, 0]
+            with np.errstate(divide="ignore"):  # a row with no visible key: log 0 = -inf
+                lse[b, h] = (m + np.log(l))[:, 0]
             if land_b is not None:
                 o[b, land_b, h] = 0.0
                 lse[b, h, land_b] = -np.inf
