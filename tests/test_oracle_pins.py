@@ -143,6 +143,8 @@ FWD_CASES = [
     ((11, 9), (4, 4), (3, 1), (0, 1), 3, 4, 1, False),
     ((4, 7, 10), (2, 4, 4), (1, 2, 2), (0, 0, 1), 2, 8, 1, True),
     ((3, 5, 9), (2, 3, 4), (0, 0, 0), (0, 0, 1), 1, 8, 2, False),
+    # periodic along depth and lon, ragged in all three dims, unequal shifts
+    ((5, 6, 11), (2, 4, 4), (1, 2, 3), (1, 0, 1), 2, 8, 1, True),
 ]
 
 
