@@ -12,6 +12,47 @@ from . import swin_attn as C
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
 
 
+def check_tensor(name, t, shape, dtype, device):
+    """Raise ValueError unless `t` is a contiguous `dtype` tensor of exactly
+    `shape` on `device` whose data starts on a 16-byte boundary. The library
+    reads and writes every tensor through a raw pointer and cannot check any
+    of this itself; a wrong shape or dtype would read or write past the
+    caller's buffers."""
+    if not isinstance(t, torch.Tensor):
+        raise ValueError("%s: expected a torch.Tensor, got %s" % (name, type(t).__name__))
+    if t.device != device:
+        raise ValueError("%s: on %s, expected %s" % (name, t.device, device))
+    if t.dtype != dtype:
+        raise ValueError("%s: dtype %s, expected %s" % (name, t.dtype, dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s: shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s: not contiguous" % name)
+    if t.data_ptr() % 16:
+        raise ValueError("%s: data not 16-byte aligned" % name)
+
+
+def check_call(tensors, shape, lse_shape, bias_shape, dtype, device, has_land):
+    """Check every tensor of one forward or backward call (None = not passed).
+    Activations and their gradients are `dtype` [B, *grid, C]; lse is fp32
+    [B, heads, *grid]; bias and dbias are fp32 [rows, heads]; land is uint8
+    [B, *grid] and required exactly when the plan was made with a land mask."""
+    for name, t in tensors.items():
+        if t is None:
+            if name == "land" and has_land:
+                raise ValueError("land: the plan was made with a land mask; pass uint8 %s" % (tuple(shape[:-1]),))
+            continue
+        if name in ("bias", "dbias"):
+            check_tensor(name, t, bias_shape, torch.float32, device)
+        elif name == "lse":
+            check_tensor(name, t, lse_shape, torch.float32, device)
+        elif name == "land":
+            if has_land:
+                check_tensor(name, t, shape[:-1], torch.uint8, device)
+        else:
+            check_tensor(name, t, shape, dtype, device)
+
+
 class SwinWindowAttention:
     """Shifted-window multi-head self-attention over a [B, *grid, C] tensor.
 
@@ -31,8 +72,13 @@ class SwinWindowAttention:
         self.lse_shape = (batch, heads) + tuple(grid)
         self.heads = heads
         self.has_land = has_land
+        self.bias_shape = (self.plan.info.bias_rows, heads)
         self.device = torch.device("cuda", torch.cuda.current_device())
         self._ws = None
+
+    def _check(self, **tensors):
+        check_call(tensors, self.shape, self.lse_shape, self.bias_shape, self.torch_dtype, self.device,
+                   self.has_land)
 
     @property
     def info(self):
@@ -48,6 +94,7 @@ class SwinWindowAttention:
         return torch.zeros((self.info.bias_rows, self.heads), dtype=torch.float32, device=self.device)
 
     def forward(self, q, k, v, bias=None, land=None, o=None, lse=None, need_lse=True, stream=None):
+        self._check(q=q, k=k, v=v, bias=bias, land=land, o=o, lse=lse)
         if o is None:
             o = torch.empty(self.shape, dtype=self.torch_dtype, device=self.device)
         if lse is None and need_lse:
@@ -57,6 +104,9 @@ class SwinWindowAttention:
 
     def backward(self, q, k, v, dout, lse, bias=None, land=None, dq=None, dk=None, dv=None, dbias=None,
                  want_dbias=True, stream=None):
+        if lse is None:
+            raise ValueError("lse: the backward needs the forward's log-sum-exp")
+        self._check(q=q, k=k, v=v, dout=dout, lse=lse, bias=bias, land=land, dq=dq, dk=dk, dv=dv, dbias=dbias)
         dq = torch.empty_like(q) if dq is None else dq
         dk = torch.empty_like(k) if dk is None else dk
         dv = torch.empty_like(v) if dv is None else dv
