@@ -378,3 +378,79 @@ def test_bwd_softmax_gradient_sums(oracle_mod, case):
     if landm is not None:
         for key in ("dq", "dk", "dv"):
             assert np.all(g[key][~sea] == 0.0)
+
+
+# ------------------------------------------------- random tiny geometries ---
+
+def _random_problems(count, seed):
+    """Seeded descriptors over the whole valid space at tiny sizes: 2-D and
+    3-D, windows that do not divide (or exceed) the grid, every shift and
+    periodic combination, batch and heads 1-2, with and without land."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        nd = int(rng.integers(2, 4))
+        grid = tuple(int(rng.integers(1, 10 if nd == 2 else 7)) for _ in range(nd))
+        window = tuple(int(rng.integers(1, min(g + 2, 6) + 1)) for g in grid)
+        if int(np.prod(window)) > 128:
+            continue
+        shift = tuple(int(rng.integers(0, w)) for w in window)
+        shift = tuple(s if s < g else 0 for s, g in zip(shift, grid))
+        periodic = tuple(int(rng.integers(0, 2)) for _ in range(nd))
+        out.append(Problem(grid=grid, window=window, shift=shift, periodic=periodic,
+                           heads=int(rng.integers(1, 3)), head_dim=int(rng.choice([4, 8])),
+                           batch=int(rng.integers(1, 3)), has_land=bool(rng.integers(0, 2))))
+    return out
+
+
+RANDOM = _random_problems(40, 2026)
+
+
+def _bruteforce_grads(pb, q, k, v, bias, land, dout):
+    """dQ, dK, dV, dBias by torch autograd (float64) through the token-pair
+    form: full N x N visibility from the definition, no window table. Land
+    queries have O = 0, so they pass no gradient."""
+    win, off, region = bruteforce._token_geometry(pb.grid, pb.window, pb.shift, pb.periodic)
+    rows = torch.from_numpy(bruteforce._pair_rows(off, pb.window))
+    shape = (pb.batch, pb.tokens, pb.heads, pb.head_dim)
+    t = [torch.tensor(np.asarray(x, np.float64).reshape(shape), requires_grad=True) for x in (q, k, v)]
+    btab = torch.tensor(np.asarray(bias, np.float64), requires_grad=True)
+    go = torch.from_numpy(np.asarray(dout, np.float64).reshape(shape))
+    total = 0.0
+    for b in range(pb.batch):
+        land_b = None if land is None else np.asarray(land).reshape(pb.batch, pb.tokens)[b].astype(bool)
+        vis = torch.from_numpy(bruteforce.visibility(pb.grid, pb.window, pb.shift, pb.periodic, land_b))
+        sea = torch.ones(pb.tokens, dtype=torch.float64) if land_b is None else torch.from_numpy(~land_b).double()
+        empty = ~vis.any(1)
+        for h in range(pb.heads):
+            s = t[0][b, :, h] @ t[1][b, :, h].T / np.sqrt(pb.head_dim) + btab[rows, h]
+            s = s.masked_fill(~vis, float("-inf")).masked_fill(empty[:, None], 0.0)
+            o = torch.softmax(s, 1) @ t[2][b, :, h] * sea[:, None]
+            total = total + (o * go[b, :, h]).sum()
+    total.backward()
+    g = {n: x.grad.numpy().reshape((pb.batch,) + tuple(pb.grid) + (pb.channels,))
+         for n, x in zip(("dq", "dk", "dv"), t)}
+    g["dbias"] = btab.grad.numpy()
+    return g
+
+
+@pytest.mark.parametrize("pb", RANDOM, ids=lambda pb: "g%s_w%s_s%s_p%s" % (
+    "x".join(map(str, pb.grid)), "x".join(map(str, pb.window)), "".join(map(str, pb.shift)),
+    "".join(map(str, pb.periodic))))
+def test_random_geometry_matches_bruteforce(oracle_mod, pb):
+    win_src, region, tok_dst, _ = oracle.tables(pb)
+    ws2, reg2 = _slot_side_tables(pb)
+    np.testing.assert_array_equal(win_src, ws2)
+    np.testing.assert_array_equal(region, reg2)
+    flat = win_src.reshape(-1)
+    assert np.array_equal(np.sort(flat[flat >= 0]), np.arange(pb.tokens))
+    assert np.array_equal(flat[tok_dst], np.arange(pb.tokens))
+    q, k, v, bias, dout, landm = _inputs(pb, 41, land_p=0.35)
+    o, lse = oracle.fwd(pb, q, k, v, bias, landm)
+    o2, lse2 = bruteforce.fwd(pb, q, k, v, bias, landm)
+    np.testing.assert_allclose(o, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse2, rtol=0, atol=1e-12)
+    g = oracle.bwd(pb, q, k, v, bias, landm, dout)
+    g2 = _bruteforce_grads(pb, q, k, v, bias, landm, dout)
+    for key in ("dq", "dk", "dv", "dbias"):
+        np.testing.assert_allclose(g[key], g2[key], rtol=0, atol=1e-11, err_msg=key)
