@@ -30,8 +30,12 @@
  * Conventions for every entry point:
  *  - Returns SWIN_OK (0) or a negative status; nothing is launched when an
  *    argument check fails.
- *  - Tensors are owned by the caller, device-resident, contiguous; every
- *    q/k/v/o/dout/dq/dk/dv pointer must be 16-byte aligned.
+ *  - Tensors are owned by the caller, device-resident, contiguous. Every
+ *    q/k/v/o/dout/dq/dk/dv pointer and lse must be 16-byte aligned, land,
+ *    bias and dbias 4-byte aligned: the tensor-core kernels read four
+ *    consecutive LSE values, or land bytes, with one load. (The entry points
+ *    reject a misaligned q..dv, bias, dbias, or an lse off a 4-byte boundary;
+ *    the rest is the caller's to keep, like the buffer sizes.)
  *  - q, k, v, o, dout, dq, dk, dv: [B, grid..., C] channel-last, C = heads *
  *    head_dim, head h in channels [h*hd, (h+1)*hd); element type = desc.dtype.
  *  - bias, dbias: float32 [rows][heads], rows = prod(2 w_d - 1).

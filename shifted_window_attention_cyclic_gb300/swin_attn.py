@@ -192,8 +192,21 @@ def swin_attn_workspace_bytes(plan: Plan) -> int:
     return int(load_library().swin_attn_workspace_bytes(plan.handle))
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _ptr(t, align=1, what=""):
+    """Raw device address of a tensor (None passes NULL). `align` is the
+    alignment the library reads it with: 16 bytes for the activations and
+    lse (the tensor-core kernels read four LSE values in one load), 4 for
+    land (four land bytes in one load), bias and dbias."""
+    if t is None:
+        return None
+    p = t.data_ptr()
+    if p % align:
+        raise SwinAttnError(SWIN_ERR_ALIGNMENT, "%s not %d-byte aligned" % (what, align))
+    return ctypes.c_void_p(p)
+
+
+def _acts(*named):
+    return [_ptr(t, 16, n) for n, t in named]
 
 
 def _stream(stream):
@@ -204,22 +217,28 @@ def _stream(stream):
 
 
 def swin_attn_fwd(plan: Plan, q, k, v, bias, land, o, lse, stream=None) -> None:
-    _check(load_library().swin_attn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(land), _ptr(o),
-                                        _ptr(lse), _stream(stream)), "swin_attn_fwd")
+    pq, pk, pv, po, plse = _acts(("q", q), ("k", k), ("v", v), ("o", o), ("lse", lse))
+    _check(load_library().swin_attn_fwd(plan.handle, pq, pk, pv, _ptr(bias, 4, "bias"), _ptr(land, 4, "land"), po,
+                                        plse, _stream(stream)), "swin_attn_fwd")
 
 
 def swin_attn_bwd(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv, dbias, workspace, stream=None) -> None:
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(load_library().swin_attn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(bias),
-                                        _ptr(land), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(workspace),
-                                        ws_bytes, _stream(stream)), "swin_attn_bwd")
+    pq, pk, pv, pdo, plse, pdq, pdk, pdv = _acts(("q", q), ("k", k), ("v", v), ("dout", dout), ("lse", lse),
+                                                 ("dq", dq), ("dk", dk), ("dv", dv))
+    _check(load_library().swin_attn_bwd(plan.handle, pq, pk, pv, pdo, plse, _ptr(bias, 4, "bias"),
+                                        _ptr(land, 4, "land"), pdq, pdk, pdv, _ptr(dbias, 4, "dbias"),
+                                        _ptr(workspace, 256, "workspace"), ws_bytes, _stream(stream)),
+           "swin_attn_bwd")
 
 
 def swin_attn_bwd_noalloc(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv, dbias, stream=None) -> None:
     """Backward without a workspace argument: the partial dBias tables live in
     a fixed array inside the library, so the call allocates nothing."""
-    _check(load_library().swin_attn_bwd_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse),
-                                                _ptr(bias), _ptr(land), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
+    pq, pk, pv, pdo, plse, pdq, pdk, pdv = _acts(("q", q), ("k", k), ("v", v), ("dout", dout), ("lse", lse),
+                                                 ("dq", dq), ("dk", dk), ("dv", dv))
+    _check(load_library().swin_attn_bwd_noalloc(plan.handle, pq, pk, pv, pdo, plse, _ptr(bias, 4, "bias"),
+                                                _ptr(land, 4, "land"), pdq, pdk, pdv, _ptr(dbias, 4, "dbias"),
                                                 _stream(stream)), "swin_attn_bwd_noalloc")
 
 

@@ -164,3 +164,25 @@ def test_missing_library_raises_no_fallback(monkeypatch):
         C.swin_attn_window_range(10, 4, 0)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         C.swin_attn_plan(C.make_desc((8, 16), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16"))
+
+
+def test_binding_refuses_misaligned_lse_land_and_activations(lib):
+    # the tensor-core kernels read four LSE values (16 bytes) and four land
+    # bytes with one load each; the binding refuses pointers off those
+    # boundaries before the call (CPU tensors: nothing reaches a device)
+    import types
+    torch = pytest.importorskip("torch")
+    plan = types.SimpleNamespace(handle=None)
+    f32 = torch.zeros(64, dtype=torch.float32)
+    u8 = torch.zeros(64, dtype=torch.uint8)
+    good = f32[:16]
+    with pytest.raises(C.SwinAttnError, match="lse not 16-byte aligned"):
+        C.swin_attn_fwd(plan, good, good, good, None, None, good, f32[1:17])
+    with pytest.raises(C.SwinAttnError, match="land not 4-byte aligned"):
+        C.swin_attn_fwd(plan, good, good, good, None, u8[1:], good, good)
+    with pytest.raises(C.SwinAttnError, match="q not 16-byte aligned"):
+        C.swin_attn_bwd(plan, f32[2:18], good, good, good, good, None, None, good, good, good, None, None)
+    with pytest.raises(C.SwinAttnError, match="land not 4-byte aligned"):
+        C.swin_attn_bwd(plan, good, good, good, good, good, None, u8[2:], good, good, good, None, None)
+    with pytest.raises(C.SwinAttnError, match="lse not 16-byte aligned"):
+        C.swin_attn_bwd_noalloc(plan, good, good, good, good, f32[3:19], None, None, good, good, good, None)
