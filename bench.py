@@ -171,6 +171,52 @@ def oracle_sample_rate(wl, x, windows, seed=0):
     return tokens, time.perf_counter() - t0
 
 
+PARITY_BAR = {"bf16": {"rel_l2": 5e-3, "max_abs": 2e-2}, "f32": {"rel_l2": None, "max_abs": 1e-5}}
+
+
+def parity_sample(wl, x, outs, windows=512, seed=7):
+    """Part of the cpu_baseline leg: the oracle against this run's own device
+    results (the timed launch configuration, full size, same inputs) on a
+    sample of windows, namely the corner, seam and ragged-edge windows of
+    each dimension plus random ones. Returns max-abs and rel-L2 of O, dQ, dK
+    and dV over the sampled windows' real slots, and whether they meet the bar."""
+    import itertools
+    import torch
+    import oracle
+    pb = oracle.Problem(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.has_land)
+    nwd = pb.windows_per_dim
+    edge = {int(np.ravel_multi_index(c, nwd))
+            for c in itertools.product(*[sorted({0, 1, n // 2, n - 2, n - 1} & set(range(n))) for n in nwd])}
+    rng = np.random.default_rng(seed)
+    total = wl.batch * pb.nwin
+    rand = rng.choice(total, size=min(windows, total), replace=False)
+    ids = np.array(sorted(set(rand.tolist()) | {b * pb.nwin + w for b in range(wl.batch) for w in edge}), np.int64)
+    win_src = oracle.tables(pb)[0]
+    o_ref, _ = oracle.fwd_windows(pb, x["q"], x["k"], x["v"], x["bias"], x["land"], win_ids=ids)
+    g_ref = oracle.bwd_windows(pb, x["q"], x["k"], x["v"], x["bias"], x["land"], x["dout"], win_ids=ids,
+                               want=("dq", "dk", "dv"))
+    src = win_src[ids % pb.nwin]
+    valid = src >= 0
+    rows = ((ids // pb.nwin)[:, None] * pb.tokens + np.maximum(src, 0))[valid]
+    res = {}
+    bar = PARITY_BAR[wl.dtype]
+    ok = True
+    for key, ref in (("o", o_ref), ("dq", g_ref["dq"]), ("dk", g_ref["dk"]), ("dv", g_ref["dv"])):
+        dev = outs[key].reshape(-1, pb.channels)
+        got = dev[torch.from_numpy(rows).to(dev.device)].double().cpu().numpy()
+        r = np.asarray(ref, np.float64)[valid]
+        err = got - r
+        max_abs = float(np.abs(err).max())
+        rel_l2 = float(np.linalg.norm(err) / max(np.linalg.norm(r), 1e-300))
+        res[key] = {"max_abs": max_abs, "rel_l2": rel_l2}
+        ok &= max_abs <= bar["max_abs"] and (bar["rel_l2"] is None or rel_l2 <= bar["rel_l2"])
+    res["bar"] = bar
+    res["within_bar"] = bool(ok)
+    res["sample"] = "%d windows (corner, seam, ragged edges and random), %d tokens, fp64 C oracle" % (
+        len(ids), int(valid.sum()))
+    return res
+
+
 def cpu_baseline(wl, x, target_s=15.0):
     import oracle
     oracle.build()
@@ -403,9 +449,13 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dev)
 
-    cpu = None
+    cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, x)
+        try:  # a report only: its failure must not cost the measurement
+            parity = parity_sample(wl, x, outs)
+        except Exception as e:  # noqa: BLE001
+            parity = {"error": repr(e)}
 
     if rank == 0:
         kernels = {1: "simt", 2: "tcgen05"}[attn.info.impl]
@@ -432,6 +482,7 @@ def main():
             "impl_kernels": kernels,
             "kernel_source_hash": khash,
             "cpu_baseline": cpu,
+            "parity": parity,
         }
         print(json.dumps(line))
     if world > 1:

@@ -3,6 +3,7 @@ import json
 import os
 import sys
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -29,3 +30,26 @@ def test_traffic_only_for_its_workload_kernels_and_sources(tmp_path):
     assert bench.profiled_traffic("abc", "ragged", "tcgen05", str(path)) is None
     assert bench.profiled_traffic("abc", "depth3d", "simt", str(path)) is None
     assert bench.profiled_traffic("abc", "depth3d", "tcgen05", str(tmp_path / "missing.json")) is None
+
+
+def test_parity_sample_reads_the_bar():
+    # device results stood in by the oracle's own full outputs, rounded to
+    # bf16 as the kernels round them: within the bar; one planted error of
+    # 0.05 in dK (over the bf16 max-abs bar of 0.02) is caught
+    torch = pytest.importorskip("torch")
+    import oracle
+    from shifted_window_attention_cyclic_gb300 import workloads
+    wl = workloads.custom((13, 27), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3), seed_index=60)
+    x = workloads.generate(wl)
+    pb = oracle.Problem(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.has_land)
+    o, _ = oracle.fwd(pb, x["q"], x["k"], x["v"], x["bias"], x["land"])
+    g = oracle.bwd(pb, x["q"], x["k"], x["v"], x["bias"], x["land"], x["dout"])
+    outs = {"o": torch.from_numpy(o).to(torch.bfloat16)}
+    outs.update({k: torch.from_numpy(g[k]).to(torch.bfloat16) for k in ("dq", "dk", "dv")})
+    res = bench.parity_sample(wl, x, outs, windows=64)
+    assert res["within_bar"], res
+    assert all(res[k]["max_abs"] < 2e-2 and res[k]["rel_l2"] < 5e-3 for k in ("o", "dq", "dk", "dv"))
+    sea = np.argwhere(~x["land"][0].astype(bool))[0]
+    outs["dk"][(0,) + tuple(sea)][3] += 0.05
+    res = bench.parity_sample(wl, x, outs, windows=10 ** 6)  # every window
+    assert not res["within_bar"] and res["dk"]["max_abs"] > 2e-2
