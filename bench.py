@@ -7,6 +7,11 @@ A step is one pass of the whole path over one batch of the depth3d workload
 swin_attn_bwd (dQ, dK, dV, dBias). Every input tensor (604 MB each) is larger
 than the 129 MB L2, so no flush runs between steps.
 
+The same line carries `configs`: all five workloads (tiny_fp32, grid1deg,
+ragged, eddy_ocean, depth3d) timed one launch at a time with a 1 GiB L2
+flush before every launch, the median of >= 50 repetitions after >= 10
+warm-ups, with each one's roofline fraction against its algorithmic bytes.
+
 Prints one JSON line (rank 0). --impl reference times the CPU oracle on the
 same workload instead (bounded samples of windows, fp64).
 """
@@ -41,8 +46,16 @@ def load_peaks():
     return dict(PEAKS_FALLBACK), "fallback"
 
 
-def workload_counts(wl, win_src, land):
-    """Algorithmic FLOPs and bytes per step (forward, backward)."""
+def workload_counts(wl, win_src, land, lse_written=True):
+    """Algorithmic FLOPs and bytes per launch, as the measurement section of
+    the survey counts them: forward = 4 * B * sum over windows of (real
+    slots)^2 * C FLOPs, backward = 2.5x that; forward bytes = Q, K, V in and O
+    out (4 N C e) + LSE (4 N heads, when written) + land + bias; backward
+    bytes = Q, K, V, O, dO in and dQ, dK, dV out (8 N C e) + LSE and delta
+    (2 x 4 N heads) + land + bias in + dBias out. Returns (fwd_flop,
+    bwd_flop, fwd_bytes, bwd_bytes, bwd_bytes_moved), where bwd_bytes_moved
+    is what this backward actually has to move: it recomputes delta from P
+    and dP, so it reads neither O nor delta (7 N C e + LSE + land + 2 bias)."""
     n_real = (win_src >= 0).sum(1).astype(np.float64)  # real slots per window
     N = wl.batch * wl.tokens
     C, H, e = wl.channels, wl.heads, 2 if wl.dtype == "bf16" else 4
@@ -51,9 +64,93 @@ def workload_counts(wl, win_src, land):
     bwd_flop = 2.5 * fwd_flop
     land_b = N if land is not None else 0
     bias_b = rows * H * 4
-    fwd_bytes = 4 * N * C * e + 4 * N * H + land_b + bias_b                 # q,k,v in; o, lse out
-    bwd_bytes = 7 * N * C * e + 4 * N * H + land_b + 2 * bias_b             # q,k,v,dO,lse in; dq,dk,dv, dbias out
-    return fwd_flop, bwd_flop, fwd_bytes, bwd_bytes
+    lse_b = 4 * N * H
+    fwd_bytes = 4 * N * C * e + (lse_b if lse_written else 0) + land_b + bias_b
+    bwd_bytes = 8 * N * C * e + 2 * lse_b + land_b + 2 * bias_b
+    bwd_moved = 7 * N * C * e + lse_b + land_b + 2 * bias_b
+    return fwd_flop, bwd_flop, fwd_bytes, bwd_bytes, bwd_moved
+
+
+def roof_us(flop, nbytes, peaks):
+    """Roofline time of one launch: the slower of the bf16 tensor-core time
+    (burst peak) and the HBM time, both from the measured peaks."""
+    return max(flop / (peaks["bf16_tflops"] * 1e12), nbytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+
+
+# per-config bars: forward >= 50 % and backward >= 35 % of the roofline (bf16)
+TARGETS = {"tiny_fp32": None, "grid1deg": {"fwd": 0.50}, "ragged": {"fwd": 0.50, "bwd": 0.35},
+           "eddy_ocean": {"fwd": 0.50, "bwd": 0.35}, "depth3d": {"fwd": 0.50, "bwd": 0.35}}
+NOTES = {"tiny_fp32": "fp32 SIMT path, 512 tokens: launch-bound, parity only",
+         "grid1deg": "forward only (inference: no LSE written, its bytes not counted)",
+         "eddy_ocean": "not ragged: 256 = 32 x 8 rows divide into 8-row windows; irregular through the land mask"}
+FLUSH_BYTES = 1 << 30
+
+
+def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
+    """One workload timed launch by launch: before every launch a 1 GiB buffer
+    is written (L2 flush), then CUDA events on the launching stream bracket
+    the launch alone. Median over `reps` after `warmup` repetitions."""
+    import torch
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    dev = torch.device("cuda", torch.cuda.current_device())
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch,
+                               wl.dtype, wl.has_land, kernels)
+    win_src = C.swin_attn_plan_tables(attn.plan)[0]
+    fwd_flop, bwd_flop, fwd_bytes, bwd_bytes, bwd_moved = workload_counts(wl, win_src, x["land"],
+                                                                         lse_written=wl.backward)
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    d = {k_: torch.from_numpy(x[k_]).to(dev).to(tdt) for k_ in ("q", "k", "v", "dout")}
+    bias = torch.from_numpy(x["bias"]).to(dev)
+    land = torch.from_numpy(x["land"]).to(dev) if x["land"] is not None else None
+    o = torch.empty(attn.shape, dtype=tdt, device=dev)
+    lse = torch.empty(attn.lse_shape, dtype=torch.float32, device=dev)
+    dq, dk, dv = (torch.empty(attn.shape, dtype=tdt, device=dev) for _ in range(3))
+    dbias = attn.new_bias()
+    ws = attn.workspace()
+    stream = torch.cuda.current_stream()
+    fwd_t, bwd_t = [], []
+    for r in range(warmup + reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.add_(1)
+        ev[0].record(stream)
+        C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], bias, land, o, lse if wl.backward else None, stream)
+        ev[1].record(stream)
+        if wl.backward:
+            flush.add_(1)
+            ev[2].record(stream)
+            C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, bias, land, dq, dk, dv, dbias, ws,
+                            stream)
+            ev[3].record(stream)
+        torch.cuda.synchronize()
+        if r >= warmup:
+            fwd_t.append(ev[0].elapsed_time(ev[1]) * 1e3)
+            if wl.backward:
+                bwd_t.append(ev[2].elapsed_time(ev[3]) * 1e3)
+    assert C.swin_attn_status(attn.plan) == 0
+    tokens = wl.batch * wl.tokens
+    fwd_us = statistics.median(fwd_t)
+    f_roof = roof_us(fwd_flop, fwd_bytes, peaks)
+    res = {"kernels": {1: "simt", 2: "tcgen05"}[attn.info.impl], "tokens": tokens, "reps": reps, "warmup": warmup,
+           "l2": "1 GiB written before every launch", "timing": "median of CUDA-event launch times",
+           "fwd": {"us": fwd_us, "us_min": min(fwd_t), "mtok_s": tokens / fwd_us, "tflops": fwd_flop / fwd_us / 1e6,
+                   "roof_us": f_roof, "roof_frac": f_roof / fwd_us, "alg_bytes": fwd_bytes,
+                   "lse_written": bool(wl.backward)}}
+    if wl.backward:
+        bwd_us = statistics.median(bwd_t)
+        b_roof = roof_us(bwd_flop, bwd_bytes, peaks)
+        res["bwd"] = {"us": bwd_us, "us_min": min(bwd_t), "tflops": bwd_flop / bwd_us / 1e6, "roof_us": b_roof,
+                      "roof_frac": b_roof / bwd_us, "alg_bytes": bwd_bytes,
+                      "roof_frac_moved": roof_us(bwd_flop, bwd_moved, peaks) / bwd_us, "alg_bytes_moved": bwd_moved}
+        res["fwd_bwd_mtok_s"] = tokens / (fwd_us + bwd_us)
+    tgt = TARGETS.get(wl.name)
+    res["target"] = tgt
+    if tgt:
+        res["meets_target"] = all(res[k_]["roof_frac"] >= v for k_, v in tgt.items())
+    if wl.name in NOTES:
+        res["note"] = NOTES[wl.name]
+    del attn
+    return res
 
 
 def kernel_source_hash():
@@ -217,7 +314,10 @@ def parity_sample(wl, x, outs, windows=512, seed=7):
     return res
 
 
-def cpu_baseline(wl, x, target_s=15.0):
+def cpu_baseline(wl, x, target_s=15.0, target_1core_s=10.0):
+    """The oracle as it stands, timed on this host's cores over a bounded
+    sample of windows (fwd + bwd): once with every core (OpenMP default) and
+    once single-threaded (a child process with OMP_NUM_THREADS=1)."""
     import oracle
     oracle.build()
     calib = 256
@@ -226,9 +326,34 @@ def cpu_baseline(wl, x, target_s=15.0):
     nwin = oracle.Problem(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim).nwin
     windows = int(max(calib, min(max(wl.batch * nwin, 4096), target_s / max(per_window, 1e-6))))
     tok, dt = oracle_sample_rate(wl, x, windows, seed=2)
-    return {"value": tok / dt / 1e6, "unit": "Mtokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "%d random windows of %s (%d tokens), fwd+bwd, fp64 C oracle, %.1f s" %
-                      (windows, wl.name, tok, dt)}
+    cores = oracle.num_threads()
+    res = {"value": tok / dt / 1e6, "unit": "Mtokens/s", "cores": cores, "kind": "oracle",
+           "sample": "%d random windows of %s (%d tokens), fwd+bwd, fp64 C oracle, %.1f s" %
+                     (windows, wl.name, tok, dt)}
+    w1 = int(max(8, min(windows, target_1core_s / max(per_window * cores, 1e-6))))
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", str(w1), "--workload", wl.name],
+                       capture_output=True, text=True, env=env, timeout=600)
+    try:
+        one = json.loads(r.stdout.strip().splitlines()[-1])
+        res["single_core"] = {"value": one["tokens"] / one["seconds"] / 1e6, "unit": "Mtokens/s",
+                              "cores": one["cores"],
+                              "sample": "%d random windows (%d tokens), %.1f s" % (w1, one["tokens"], one["seconds"])}
+    except (IndexError, ValueError, KeyError):
+        res["single_core"] = {"error": (r.stderr or r.stdout)[-300:]}
+    return res
+
+
+def oracle_sample_main(windows, wl):
+    """Child process of cpu_baseline: time the oracle on `windows` windows with
+    the thread count its environment sets, print one JSON line."""
+    from shifted_window_attention_cyclic_gb300 import workloads
+    import oracle
+    oracle.build()
+    x = workloads.generate(wl)
+    tok, dt = oracle_sample_rate(wl, x, windows, seed=4)
+    print(json.dumps({"tokens": tok, "seconds": dt, "cores": oracle.num_threads()}))
+    return 0
 
 
 def run_reference(args, wl):
@@ -280,17 +405,22 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--kernels", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config table (all five workloads)")
+    ap.add_argument("--config-reps", type=int, default=50)
+    ap.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
     from shifted_window_attention_cyclic_gb300 import workloads
     wl = workloads.WORKLOADS[args.workload]
+    if args.oracle_sample:
+        return oracle_sample_main(args.oracle_sample, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
 
@@ -313,7 +443,7 @@ def main():
     attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch,
                                wl.dtype, wl.has_land, args.kernels)
     win_src = C.swin_attn_plan_tables(attn.plan)[0]
-    fwd_flop, bwd_flop, fwd_bytes, bwd_bytes = workload_counts(wl, win_src, x["land"])
+    fwd_flop, bwd_flop, fwd_bytes, bwd_bytes, bwd_moved = workload_counts(wl, win_src, x["land"])
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     host = {k_: torch.from_numpy(x[k_]).to(tdt).pin_memory() for k_ in ("q", "k", "v", "dout")}
     host["bias"] = torch.from_numpy(x["bias"]).pin_memory()
@@ -375,13 +505,12 @@ def main():
     ms_per_step = total_ms / args.steps
     tokens = wl.batch * wl.tokens
     value = job_rate(world, tokens, ms_per_step)
-    fwd_avg = statistics.mean(fwd_ms)
-    bwd_avg = statistics.mean(bwd_ms)
+    fwd_avg = statistics.median(fwd_ms)  # per-launch breakdown: medians of the K steps
+    bwd_avg = statistics.median(bwd_ms)
     peaks, peak_kind = load_peaks()
     hbm = peaks["hbm_gbs"]
-    tflops = peaks["bf16_tflops_sustained"]
-    fwd_roof_us = max(fwd_flop / (tflops * 1e12), fwd_bytes / (hbm * 1e9)) * 1e6
-    bwd_roof_us = max(bwd_flop / (tflops * 1e12), bwd_bytes / (hbm * 1e9)) * 1e6
+    fwd_roof_us = roof_us(fwd_flop, fwd_bytes, peaks)
+    bwd_roof_us = roof_us(bwd_flop, bwd_bytes, peaks)
     bwd_gbs = bwd_bytes / (bwd_avg * 1e-3) / 1e9
     khash = kernel_source_hash()
 
@@ -449,6 +578,25 @@ def main():
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, dev)
 
+    # every workload, launch by launch, L2 flushed before each launch
+    configs = None
+    if rank == 0 and not args.no_configs:
+        flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        flush.zero_()
+        csampler = ClockSampler(dev.index)
+        csampler.start()
+        configs = {}
+        for name in TARGETS:
+            cwl = workloads.WORKLOADS[name]
+            cx = x if name == wl.name else workloads.generate(cwl)
+            configs[name] = time_config(cwl, cx, peaks, flush, reps=args.config_reps, warmup=10)
+            configs[name]["config"] = config_of(cwl)["workload"]
+        configs["clocks"] = csampler.stop()
+        configs["peaks"] = {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
+                            "source": peak_kind, "which": "burst bf16 peak, measured copy bandwidth"}
+        del flush
+        torch.cuda.empty_cache()
+
     cpu = parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, x)
@@ -468,13 +616,19 @@ def main():
                     "roof_frac": fwd_roof_us / (fwd_avg * 1e3), "tflops": fwd_flop / (fwd_avg * 1e-3) / 1e12,
                     "alg_bytes": fwd_bytes},
             "bwd": {"us": bwd_avg * 1e3, "roof_us": bwd_roof_us, "roof_frac": bwd_roof_us / (bwd_avg * 1e3),
-                    "tflops": bwd_flop / (bwd_avg * 1e-3) / 1e12, "alg_bytes": bwd_bytes},
+                    "tflops": bwd_flop / (bwd_avg * 1e-3) / 1e12, "alg_bytes": bwd_bytes,
+                    "alg_bytes_moved": bwd_moved,
+                    "roof_frac_moved": roof_us(bwd_flop, bwd_moved, peaks) / (bwd_avg * 1e3)},
             "fwd_bwd": {"mtok_s": value / world, "roof_frac": (fwd_roof_us + bwd_roof_us) / (ms_per_step * 1e3)},
             "roofline": {"bound": "hbm", "kernel": "swin_attn_bwd (main kernel + dBias fold)",
                          "achieved": bwd_gbs, "peak": hbm, "unit": "GB/s", "frac": bwd_gbs / hbm,
-                         "peak_source": peak_kind,
+                         "peak_source": peak_kind + " (copy bandwidth, burst)",
                          "traffic": profiled_traffic(khash, args.workload, kernels),
-                         "alg_bytes_per_launch": bwd_bytes},
+                         "alg_bytes_per_launch": bwd_bytes,
+                         "alg_bytes_note": "Q, K, V, O, dO, dQ, dK, dV + LSE, delta, land, bias, dBias; this "
+                                           "backward reads neither O nor delta: it moves alg_bytes_moved",
+                         "frac_moved": bwd_moved / (bwd_avg * 1e-3) / 1e9 / hbm},
+            "configs": configs,
             "clocks": clocks,
             "e2e": {"value": job_rate(world, tokens, e2e_ms), "unit": "Mtokens/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

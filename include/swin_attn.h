@@ -33,9 +33,9 @@
  *  - Tensors are owned by the caller, device-resident, contiguous. Every
  *    q/k/v/o/dout/dq/dk/dv pointer and lse must be 16-byte aligned, land,
  *    bias and dbias 4-byte aligned: the tensor-core kernels read four
- *    consecutive LSE values, or land bytes, with one load. (The entry points
- *    reject a misaligned q..dv, bias, dbias, or an lse off a 4-byte boundary;
- *    the rest is the caller's to keep, like the buffer sizes.)
+ *    consecutive LSE values, or land bytes, with one load. fwd and bwd
+ *    return SWIN_ERR_ALIGNMENT (launching nothing) for any pointer that
+ *    breaks this rule; buffer sizes are the caller's to keep.
  *  - q, k, v, o, dout, dq, dk, dv: [B, grid..., C] channel-last, C = heads *
  *    head_dim, head h in channels [h*hd, (h+1)*hd); element type = desc.dtype.
  *  - bias, dbias: float32 [rows][heads], rows = prod(2 w_d - 1).
@@ -58,7 +58,7 @@ extern "C" {
 #define SWIN_OK 0
 #define SWIN_ERR_INVALID_ARG (-1) /* NULL/inconsistent argument or descriptor */
 #define SWIN_ERR_UNSUPPORTED (-2) /* window > 128 slots, head_dim not 16/32, ... */
-#define SWIN_ERR_ALIGNMENT (-3)   /* a tensor pointer is not 16-byte aligned */
+#define SWIN_ERR_ALIGNMENT (-3)   /* a pointer breaks its alignment rule (see Conventions) */
 #define SWIN_ERR_WORKSPACE (-4)   /* workspace NULL or smaller than required */
 #define SWIN_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
 #define SWIN_ERR_TIMEOUT (-6)     /* a kernel gave up a bounded wait (device status word) */
@@ -83,7 +83,7 @@ typedef struct {
   int32_t ndim;        /* 2: (lat, lon); 3: (depth, lat, lon) */
   int32_t impl;        /* SWIN_IMPL_* */
   int64_t batch;       /* B >= 1 */
-  int32_t grid[3];     /* G_d >= 1, outermost first; prod(G) < 2^31 */
+  int32_t grid[3];     /* G_d >= 1, outermost first; batch * prod(G) < 2^31 */
   int32_t window[3];   /* w_d >= 1; prod(w) <= 128 */
   int32_t shift[3];    /* 0 <= s_d < w_d, s_d < G_d (or 0); all zero = W-MSA */
   int32_t periodic[3]; /* 1 = cyclic neighbour (no region bit), 0 = region-masked */
@@ -143,7 +143,9 @@ int swin_attn_fwd(swin_attn_plan_t plan, const void *q, const void *k, const voi
  * OVERWRITES dbias (may be NULL: not computed). lse is the forward's output
  * for the same inputs (required). delta_i = sum_j P_ij dP_ij is recomputed
  * in-kernel, so O is not an input. workspace: device, >=
- * swin_attn_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored.
+ * swin_attn_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored
+ * (not needed when dbias is NULL: pass NULL, 0). When swin_attn_status then
+ * reports SWIN_ERR_TIMEOUT, every output of the call is undefined.
  * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, CUDA. */
 int swin_attn_bwd(swin_attn_plan_t plan, const void *q, const void *k, const void *v,
                   const void *dout, const float *lse, const float *bias,
@@ -159,12 +161,17 @@ int swin_attn_bwd(swin_attn_plan_t plan, const void *q, const void *k, const voi
  * workspace: the partial dBias tables go to a fixed device array inside this
  * library (SWIN_NOALLOC_MAX_WORKSPACE_BYTES, held on every GPU that loads the
  * library until the process exits). Nothing is allocated by any call.
- *  - Plans whose swin_attn_workspace_bytes() exceeds the array are rejected
- *    with SWIN_ERR_WORKSPACE (nothing is launched).
- *  - The first call on a device looks up the array's device address (with
- *    that device current); make that first call before any stream capture.
+ *  - With dbias != NULL, plans whose swin_attn_workspace_bytes() exceeds
+ *    the array are rejected with SWIN_ERR_WORKSPACE (nothing is launched).
+ *    With dbias == NULL the array is not used and any plan is accepted.
+ *  - The first call in a CUDA context (per device, and again after
+ *    cudaDeviceReset or in another context on that device) looks up the
+ *    array's device address in that context; make that first call before
+ *    any stream capture.
  *  - All calls share the one array: calls that can overlap on the GPU (other
- *    streams, other threads) race on it; serialise them.
+ *    streams, other threads) race on it; serialise them. Each call writes
+ *    every partial table it reads; when swin_attn_status reports
+ *    SWIN_ERR_TIMEOUT, that call's outputs (dbias included) are undefined.
  * Errors: those of swin_attn_bwd, WORKSPACE as above, CUDA. */
 #define SWIN_NOALLOC_MAX_WORKSPACE_BYTES ((size_t)4 << 20)
 int swin_attn_bwd_noalloc(swin_attn_plan_t plan, const void *q, const void *k, const void *v,

@@ -4,6 +4,13 @@ Each .cu (and host-only .cpp) translation unit compiles in parallel to an
 object under _build/,
 then nvcc links the shared library next to this file (CUDA runtime linked
 statically, so loading the library needs no GPU).
+
+build(check_bounds=True) makes libswin_attn_bounds.so from the same sources
+with -DSWIN_CHECK_BOUNDS: every raw global load and store that a kernel
+addresses itself is range-checked first, and a violation is recorded in the
+plan's status word (swin_attn_status returns SWIN_ERR_DEVICE) and the access
+skipped. The binding loads it instead of the product library when the
+environment sets SWIN_ATTN_CHECK_BOUNDS=1 (a testing build).
 """
 from __future__ import annotations
 
@@ -17,6 +24,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libswin_attn.so")
+BOUNDS_BUILD = os.path.join(HERE, "_build_bounds")
+BOUNDS_LIB = os.path.join(HERE, "libswin_attn_bounds.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -36,21 +45,24 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), check_bounds: bool = False) -> str:
+    lib, out_dir = (BOUNDS_LIB, BOUNDS_BUILD) if check_bounds else (LIB, BUILD)
+    if check_bounds:
+        extra_flags = list(extra_flags) + ["-DSWIN_CHECK_BOUNDS"]
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc] + ARCH + FLAGS + list(extra_flags) + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,16 +73,17 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else []))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else [],
+                check_bounds="--check-bounds" in sys.argv))

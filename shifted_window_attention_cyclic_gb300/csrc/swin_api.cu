@@ -68,6 +68,7 @@ __global__ void fold_kernel(FoldArgs a) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 int check_desc(const swin_attn_desc *d) {
   if (!d) return SWIN_ERR_INVALID_ARG;
@@ -88,6 +89,9 @@ int check_desc(const swin_attn_desc *d) {
   }
   if (n > 128) return SWIN_ERR_UNSUPPORTED;
   if (d->head_dim != 16 && d->head_dim != 32) return SWIN_ERR_UNSUPPORTED;
+  // The kernels keep the batch in an int and address the [B*T, C] row view
+  // (TMA coordinates, land bytes) with 32-bit row numbers.
+  if (d->batch > INT32_MAX || d->batch * tokens >= (int64_t(1) << 31)) return SWIN_ERR_UNSUPPORTED;
   if (d->batch * tokens * d->heads >= (int64_t(1) << 40)) return SWIN_ERR_UNSUPPORTED;
   return SWIN_OK;
 }
@@ -179,7 +183,7 @@ const char *swin_attn_strerror(int status) {
     case SWIN_OK: return "ok";
     case SWIN_ERR_INVALID_ARG: return "invalid argument";
     case SWIN_ERR_UNSUPPORTED: return "unsupported problem (slots > 128, head_dim not 16/32, dtype or impl)";
-    case SWIN_ERR_ALIGNMENT: return "tensor pointer not 16-byte aligned";
+    case SWIN_ERR_ALIGNMENT: return "pointer misaligned (16 bytes; 4 for bias, dbias and land; 256 for workspace)";
     case SWIN_ERR_WORKSPACE: return "workspace missing or too small";
     case SWIN_ERR_CUDA: return "CUDA runtime error";
     case SWIN_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
@@ -320,7 +324,9 @@ int swin_attn_fwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   if (!p || !q || !k || !v || !o) return SWIN_ERR_INVALID_ARG;
   if (p->d.has_land && !land) return SWIN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return SWIN_ERR_ALIGNMENT;
-  if ((bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+  // lse and land are read four slots per load where four slots are
+  // consecutive tokens: 16 and 4 bytes
+  if ((bias && !aligned4(bias)) || (lse && !aligned16(lse)) || (p->d.has_land && !aligned4(land)))
     return SWIN_ERR_ALIGNMENT;
   int rc = current_device_matches(p);
   if (rc) return rc;
@@ -351,8 +357,8 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
       !aligned16(dv))
     return SWIN_ERR_ALIGNMENT;
-  if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (bias && (reinterpret_cast<uintptr_t>(bias) & 3u)) ||
-      (dbias && (reinterpret_cast<uintptr_t>(dbias) & 3u)))
+  if (!aligned16(lse) || (bias && !aligned4(bias)) || (dbias && !aligned4(dbias)) ||
+      (p->d.has_land && !aligned4(land)))
     return SWIN_ERR_ALIGNMENT;
   if (dbias) {
     if (!workspace || workspace_bytes < swin_attn_workspace_bytes(p)) return SWIN_ERR_WORKSPACE;
@@ -374,6 +380,7 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.dv = dv;
   a.ws = dbias ? static_cast<float *>(workspace) : nullptr;
   a.slot_base = p->d_slot_base;
+  a.ws_slots = p->ws_slots;
   a.status = p->d_status;
   a.items = p->items;
   a.ctas = p->bwd_ctas;

@@ -187,6 +187,23 @@ __host__ __device__ __forceinline__ void eq4_range(int64_t M, int64_t P, int64_t
 // Device status word values (first error wins).
 enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusBounds = 2 };
 
+// Bounds-checked build (-DSWIN_CHECK_BOUNDS): a raw global access of elements
+// [idx, idx + len) of a buffer of `count` elements first checks the range; a
+// violation records kStatusBounds in the status word (read by
+// swin_attn_status as SWIN_ERR_DEVICE) and the caller skips the access. In
+// the normal build the check is a constant true.
+__device__ __forceinline__ bool in_bounds(int64_t idx, int64_t len, int64_t count, int *status) {
+#ifdef SWIN_CHECK_BOUNDS
+  if (idx < 0 || idx + len > count) {
+    atomicCAS(status, 0, kStatusBounds);
+    return false;
+  }
+#else
+  (void)idx, (void)len, (void)count, (void)status;
+#endif
+  return true;
+}
+
 struct FwdArgs {
   Geo g;
   const void *q, *k, *v;
@@ -209,6 +226,7 @@ struct BwdArgs {
   const uint8_t *land;
   void *dq, *dk, *dv;
   float *ws;              // [slots][T] partial dBias tables, or nullptr (dbias not wanted)
+  int64_t ws_slots;       // slots of ws
   const int *slot_base;   // [ctas] first workspace slot of each CTA
   int *status;
   int64_t items;

@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads) fwd_simt_kernel(const FwdArgs a) {
     int64_t tok = 0;
     if (tid < g.n) {
       r = slot_route(g, wc, tid);
+      if (r.src >= 0 && !in_bounds((int64_t)x.b * g.tokens + r.src, 1, (int64_t)g.batch * g.tokens, a.status)) r.src = -1;
       if (r.src >= 0) {
         tok = (int64_t)x.b * g.tokens + r.src;
         const bool land = g.has_land && a.land[tok];
@@ -253,6 +254,7 @@ __global__ void __launch_bounds__(kThreads) bwd_simt_kernel(const BwdArgs a) {
     int64_t tok = 0;
     if (tid < g.n) {
       r = slot_route(g, wc, tid);
+      if (r.src >= 0 && !in_bounds((int64_t)x.b * g.tokens + r.src, 1, (int64_t)g.batch * g.tokens, a.status)) r.src = -1;
       if (r.src >= 0) {
         tok = (int64_t)x.b * g.tokens + r.src;
         live = !(g.has_land && a.land[tok]);

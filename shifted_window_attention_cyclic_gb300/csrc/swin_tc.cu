@@ -213,15 +213,15 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
       if (land) {
         if (run4 && (lt & 3) == 0) {
           p.lvec = true;
-          p.land[0] = __ldg(reinterpret_cast<const unsigned int *>(land + lt));
+          p.land[0] = in_bounds(lt, 4, (int64_t)g.batch * g.tokens, ctl.status) ? __ldg(reinterpret_cast<const unsigned int *>(land + lt)) : 0u;
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 ? __ldg(land + tok0 + p.src[j]) : 0u;
+          for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 && in_bounds(tok0 + p.src[j], 1, (int64_t)g.batch * g.tokens, ctl.status) ? __ldg(land + tok0 + p.src[j]) : 0u;
         }
       }
       if (lse && pw == 0) {
         if (run4 && (lo & 3) == 0) {
-          const float4 l4 = __ldg(reinterpret_cast<const float4 *>(lse + lo));
+          const float4 l4 = in_bounds(lo, 4, (int64_t)g.batch * g.heads * g.tokens, ctl.status) ? __ldg(reinterpret_cast<const float4 *>(lse + lo)) : make_float4(0.f, 0.f, 0.f, 0.f);
           p.lse[0] = l4.x;
           p.lse[1] = l4.y;
           p.lse[2] = l4.z;
@@ -229,7 +229,7 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
         } else {
           const float *lrow = lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 ? __ldg(lrow + p.src[j]) : 0.f;
+          for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 && in_bounds((lrow - lse) + p.src[j], 1, (int64_t)g.batch * g.heads * g.tokens, ctl.status) ? __ldg(lrow + p.src[j]) : 0.f;
         }
       }
     };
@@ -388,15 +388,15 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
       if (land) {
         if (run4 && (lt & 3) == 0) {
           p.lvec = true;
-          p.land[0] = __ldg(reinterpret_cast<const unsigned int *>(land + lt));
+          p.land[0] = in_bounds(lt, 4, (int64_t)g.batch * g.tokens, ctl.status) ? __ldg(reinterpret_cast<const unsigned int *>(land + lt)) : 0u;
         } else {
 #pragma unroll
-          for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 ? __ldg(land + tok0 + p.src[j]) : 0u;
+          for (int j = 0; j < 4; ++j) p.land[j] = p.src[j] >= 0 && in_bounds(tok0 + p.src[j], 1, (int64_t)g.batch * g.tokens, ctl.status) ? __ldg(land + tok0 + p.src[j]) : 0u;
         }
       }
       if (lse && pw == 0) {
         if (run4 && (lo & 3) == 0) {
-          const float4 l4 = __ldg(reinterpret_cast<const float4 *>(lse + lo));
+          const float4 l4 = in_bounds(lo, 4, (int64_t)g.batch * g.heads * g.tokens, ctl.status) ? __ldg(reinterpret_cast<const float4 *>(lse + lo)) : make_float4(0.f, 0.f, 0.f, 0.f);
           p.lse[0] = l4.x;
           p.lse[1] = l4.y;
           p.lse[2] = l4.z;
@@ -404,7 +404,7 @@ __device__ __forceinline__ void gather_role(const Geo &g, const StageLayout &lay
         } else {
           const float *lrow = lse + ((int64_t)cu.b * g.heads + cu.h) * g.tokens;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 ? __ldg(lrow + p.src[j]) : 0.f;
+          for (int j = 0; j < 4; ++j) p.lse[j] = p.src[j] >= 0 && in_bounds((lrow - lse) + p.src[j], 1, (int64_t)g.batch * g.heads * g.tokens, ctl.status) ? __ldg(lrow + p.src[j]) : 0.f;
         }
       }
     };
@@ -732,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld_tied(o2, o3);
       tc_fence_before();
       mbar_arrive_warp(bar(bTFree + wb));
-      const bool store = src >= 0;  // pad rows carry src = -1
+      const bool store = src >= 0 && in_bounds(((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * 32, 32, (int64_t)g.batch * g.tokens * g.C, a.status);  // pad rows carry src = -1
       {
         const float m = two ? fmaxf(m0, m1) : m0;
         const float a0 = ex2(m0 - m), a1 = two ? ex2(m1 - m) : 0.f;
@@ -1117,7 +1117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait_warp(bar(bAccFull), (uint32_t)it & 1u, ctl)) break;
       tc_fence_after();
       // one 32-column accumulator at a time: TMEM -> registers -> bf16 -> grid
-      const bool store = src >= 0;  // pad rows carry src = -1
+      const bool store = src >= 0 && in_bounds(((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * 32, 32, (int64_t)g.batch * g.tokens * g.C, a.status);  // pad rows carry src = -1
       const int64_t off = ((int64_t)x.b * g.tokens + (store ? src : 0)) * g.C + (int64_t)x.h * 32;
       auto drain = [&](uint32_t col, void *base, float mul) {
         uint32_t lo[16], hi[16];
@@ -1211,7 +1211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               sum += acc[qi * kBiasStride + kj];
               if (kPack == 2) sum += acc[(g.offb + qi) * kBiasStride + g.offb + kj];  // the second window
             }
-        a.ws[(int64_t)slot * g.T + t] = sum;
+        if (in_bounds((int64_t)slot * g.T + t, 1, a.ws_slots * g.T, a.status)) a.ws[(int64_t)slot * g.T + t] = sum;
       }
       mbar_arrive_warp(bar(bWsync));
       if (!mbar_wait_warp(bar(bWsync), wsync_phase & 1u, ctl)) return false;

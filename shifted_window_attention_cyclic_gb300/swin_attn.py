@@ -17,7 +17,10 @@ import re
 import numpy as np
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libswin_attn.so")
+# SWIN_ATTN_CHECK_BOUNDS=1 selects the bounds-checked testing build of the
+# same sources (every kernel-addressed global access range-checked).
+CHECK_BOUNDS = os.environ.get("SWIN_ATTN_CHECK_BOUNDS", "0") == "1"
+LIB_PATH = os.path.join(HERE, "libswin_attn_bounds.so" if CHECK_BOUNDS else "libswin_attn.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "swin_attn.h")
 
 SWIN_OK = 0
@@ -66,8 +69,8 @@ def load_library():
     if _lib is not None:
         return _lib
     if not os.path.exists(LIB_PATH):
-        raise RuntimeError("libswin_attn.so is not built (run __graft_entry__.build()); "
-                           "this package has no CPU fallback")
+        raise RuntimeError("%s is not built (run __graft_entry__.build()); "
+                           "this package has no CPU fallback" % os.path.basename(LIB_PATH))
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
     lib.swin_attn_plan.argtypes = [ctypes.POINTER(swin_attn_desc), ctypes.POINTER(vp)]

@@ -104,6 +104,15 @@ def test_plan_rejects_bad_dtype_impl_batch_ndim(lib):
     d = C.make_desc(**base)
     d.ndim = 4
     assert lib.swin_attn_plan(ctypes.byref(d), ctypes.byref(h)) == C.SWIN_ERR_INVALID_ARG
+    # the kernels address the [B*T, C] row view with 32-bit row numbers and
+    # keep the batch in an int: B*T >= 2^31 (or B > INT32_MAX) is refused at plan time
+    d = C.make_desc(grid=(32768, 32768), window=(4, 8), shift=(2, 4), periodic=(0, 1), heads=1, head_dim=16,
+                    batch=2)
+    assert lib.swin_attn_plan(ctypes.byref(d), ctypes.byref(h)) == C.SWIN_ERR_UNSUPPORTED
+    d = C.make_desc(**base)
+    d.batch = 2 ** 31
+    assert lib.swin_attn_plan(ctypes.byref(d), ctypes.byref(h)) == C.SWIN_ERR_UNSUPPORTED
+    assert not h.value
     assert lib.swin_attn_plan(None, ctypes.byref(h)) == C.SWIN_ERR_INVALID_ARG
     assert lib.swin_attn_plan(ctypes.byref(d), None) == C.SWIN_ERR_INVALID_ARG
 

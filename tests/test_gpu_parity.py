@@ -192,12 +192,29 @@ def test_abi_errors_launch_nothing():
     mis = __import__("ctypes").c_void_p(flat.data_ptr() + 2)
     assert lib.swin_attn_fwd(attn.plan.handle, mis, vp(q), vp(q), None, vp(land), vp(o), None, stream) \
         == C.SWIN_ERR_ALIGNMENT
+    # lse off its 16-byte boundary, land off its 4-byte boundary: the kernels
+    # read four slots of either with one load
+    lse = torch.zeros(attn.lse_shape, device=dev)
+    lse_buf = torch.zeros(lse.numel() + 8, device=dev)
+    land_buf = torch.zeros(land.numel() + 8, dtype=torch.uint8, device=dev)
+    lse_mis = __import__("ctypes").c_void_p(lse_buf.data_ptr() + 4)
+    land_mis = __import__("ctypes").c_void_p(land_buf.data_ptr() + 1)
+    assert lib.swin_attn_fwd(attn.plan.handle, vp(q), vp(q), vp(q), None, vp(land), vp(o), lse_mis, stream) \
+        == C.SWIN_ERR_ALIGNMENT
+    assert lib.swin_attn_fwd(attn.plan.handle, vp(q), vp(q), vp(q), None, land_mis, vp(o), vp(lse), stream) \
+        == C.SWIN_ERR_ALIGNMENT
     torch.cuda.synchronize()
     assert torch.all(o == 7.0)
+    assert torch.all(lse == 0.0) and torch.all(lse_buf == 0.0)
     # backward: lse required, workspace checked when dbias is wanted
-    lse = torch.zeros(attn.lse_shape, device=dev)
     dbias = attn.new_bias()
     args = [vp(q)] * 4
+    need0 = C.swin_attn_workspace_bytes(attn.plan)
+    ws0 = torch.empty(need0, dtype=torch.uint8, device=dev)
+    assert lib.swin_attn_bwd(attn.plan.handle, *args, lse_mis, None, vp(land), vp(o), vp(o), vp(o), vp(dbias),
+                             vp(ws0), need0, stream) == C.SWIN_ERR_ALIGNMENT
+    assert lib.swin_attn_bwd(attn.plan.handle, *args, vp(lse), None, land_mis, vp(o), vp(o), vp(o), vp(dbias),
+                             vp(ws0), need0, stream) == C.SWIN_ERR_ALIGNMENT
     assert lib.swin_attn_bwd(attn.plan.handle, *args, None, None, vp(land), vp(o), vp(o), vp(o), None, None, 0,
                              stream) == C.SWIN_ERR_INVALID_ARG
     need = C.swin_attn_workspace_bytes(attn.plan)

@@ -37,6 +37,35 @@ def test_forced_wait_timeout_is_reported_and_recoverable():
     assert_close("O", host(o), o_ref, wl.dtype)
 
 
+def test_forced_wait_timeout_in_backward_is_reported_and_recoverable():
+    """The same failure path in the backward kernel: its softmax warps wait on
+    the barrier nothing arrives at; the gather, MMA and epilogue roles see the
+    abort flag and leave, copies and MMAs in flight drain, TMEM is freed. The
+    plan then runs the backward normally and meets the oracle."""
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    wl = workloads.custom((13, 27), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3), seed_index=92)
+    x = workloads.generate(wl)
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch,
+                               wl.dtype, wl.has_land, "tc")
+    assert attn.info.impl == C.SWIN_IMPL_TC
+    t = to_device(x, wl, torch.device("cuda", 0))
+    _, lse = attn.forward(t["q"], t["k"], t["v"], t["bias"], t["land"])
+    torch.cuda.synchronize()
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK
+    C.swin_attn_plan_set_debug(attn.plan, 5_000_000, 1)  # 5 ms limit, forced wait
+    attn.backward(t["q"], t["k"], t["v"], t["dout"], lse, t["bias"], t["land"])
+    assert C.swin_attn_status(attn.plan) == C.SWIN_ERR_TIMEOUT
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK  # status word was cleared
+    C.swin_attn_plan_set_debug(attn.plan, 1_000_000_000, 0)
+    dq, dk, dv, dbias = attn.backward(t["q"], t["k"], t["v"], t["dout"], lse, t["bias"], t["land"])
+    torch.cuda.synchronize()
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK
+    g = oracle.bwd(problem_of(wl), x["q"], x["k"], x["v"], x["bias"], x["land"], x["dout"])
+    for key, got in (("dq", dq), ("dk", dk), ("dv", dv), ("dbias", dbias)):
+        assert_close(key, host(got), g[key], wl.dtype)
+
+
 def test_debug_hook_rejects_bad_arguments():
     from shifted_window_attention_cyclic_gb300 import swin_attn as C
     from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
