@@ -153,6 +153,62 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
     return res
 
 
+def time_pair(wl, peaks, flush, reps=50, warmup=10):
+    """The W-MSA + SW-MSA block pair on one grid (shift 0, then floor(w/2)),
+    two plans built once: the forward of both layers back to back, then the
+    backward of both (second layer first), each pair of launches timed as one
+    region after an L2 flush; medians over `reps`. Roofline: the sum of both
+    layers' roofline times over the measured time."""
+    import torch
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300 import workloads
+    from shifted_window_attention_cyclic_gb300.functional import SwinBlockPair
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pair = SwinBlockPair(wl.grid, wl.window, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.dtype, wl.has_land)
+    layers = [workloads.custom(wl.grid, wl.window, sh, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.dtype,
+                               wl.land_p, seed_index=wl.index + 40 + i, name=wl.name + ("_wmsa", "_swmsa")[i])
+              for i, sh in enumerate(((0,) * len(wl.grid), pair.shift))]
+    xs = [workloads.generate(lw) for lw in layers]
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    t = [{k_: torch.from_numpy(x[k_]).to(dev).to(tdt) for k_ in ("q", "k", "v", "dout")} for x in xs]
+    for x, d in zip(xs, t):
+        d["bias"] = torch.from_numpy(x["bias"]).to(dev)
+    land = torch.from_numpy(xs[0]["land"]).to(dev) if xs[0]["land"] is not None else None
+    first = (t[0]["q"], t[0]["k"], t[0]["v"], t[0]["bias"])
+    second = (t[1]["q"], t[1]["k"], t[1]["v"], t[1]["bias"])
+    fwd_t, bwd_t = [], []
+    stream = torch.cuda.current_stream()
+    for r in range(warmup + reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.add_(1)
+        ev[0].record(stream)
+        (o1, l1), (o2, l2) = pair.forward(first, second, land)
+        ev[1].record(stream)
+        flush.add_(1)
+        ev[2].record(stream)
+        pair.backward(first, second, t[0]["dout"], t[1]["dout"], l1, l2, land)
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        if r >= warmup:
+            fwd_t.append(ev[0].elapsed_time(ev[1]) * 1e3)
+            bwd_t.append(ev[2].elapsed_time(ev[3]) * 1e3)
+    assert C.swin_attn_status(pair.wmsa.plan) == 0 and C.swin_attn_status(pair.swmsa.plan) == 0
+    f_roof = b_roof = 0.0
+    for lw, x, attn in zip(layers, xs, (pair.wmsa, pair.swmsa)):
+        win_src = C.swin_attn_plan_tables(attn.plan)[0]
+        ff, bf, fb, bb, _ = workload_counts(lw, win_src, x["land"])
+        f_roof += roof_us(ff, fb, peaks)
+        b_roof += roof_us(bf, bb, peaks)
+    tokens = wl.batch * wl.tokens
+    fwd_us, bwd_us = statistics.median(fwd_t), statistics.median(bwd_t)
+    return {"grid": list(wl.grid), "window": list(wl.window), "shifts": [[0] * len(wl.grid), list(pair.shift)],
+            "plans": "two, built once and reused (the shift changes the routing tables)",
+            "l2": "1 GiB written before each pair of launches", "reps": reps, "warmup": warmup,
+            "fwd": {"us": fwd_us, "mtok_s": tokens / fwd_us, "roof_us": f_roof, "roof_frac": f_roof / fwd_us},
+            "bwd": {"us": bwd_us, "roof_us": b_roof, "roof_frac": b_roof / bwd_us},
+            "fwd_bwd_mtok_s": tokens / (fwd_us + bwd_us)}
+
+
 def kernel_source_hash():
     """Hash of the CUDA sources (csrc/*.cu, *.cuh) that the kernels and their
     launch plans compile from; host-only .cpp files are not part of it."""
@@ -591,6 +647,9 @@ def main():
             cx = x if name == wl.name else workloads.generate(cwl)
             configs[name] = time_config(cwl, cx, peaks, flush, reps=args.config_reps, warmup=10)
             configs[name]["config"] = config_of(cwl)["workload"]
+        # the W-MSA + SW-MSA pair on the eddy-resolving ocean grid (TERRA's Wenhai stand-in)
+        configs["block_pair_eddy_ocean"] = time_pair(workloads.WORKLOADS["eddy_ocean"], peaks, flush,
+                                                     reps=args.config_reps, warmup=10)
         configs["clocks"] = csampler.stop()
         configs["peaks"] = {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
                             "source": peak_kind, "which": "burst bf16 peak, measured copy bandwidth"}

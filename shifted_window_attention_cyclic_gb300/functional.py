@@ -138,3 +138,37 @@ class _SwinAttnFn(torch.autograd.Function):
 def swin_window_attention(attn: SwinWindowAttention, q, k, v, bias=None, land=None):
     """Autograd-aware SW-MSA: returns O; gradients flow to q, k, v and bias."""
     return _SwinAttnFn.apply(attn, q, k, v, bias, land)
+
+
+class SwinBlockPair:
+    """The attention of one Swin block pair over a [B, *grid, C] tensor: W-MSA
+    (no shift) in the first block, SW-MSA (the grid rolled by floor(w/2) per
+    dim) in the second, as TERRA's Fig. 4 stacks them and as the BEAST page
+    rolls the domain by half a window between attention layers.
+
+    Two plans, built once and reused for every step: the shift changes the
+    routing tables (window sources, region bits and inverse route); the bias
+    row of a slot pair does not depend on it. Each call is one C-ABI call per
+    layer; the layers' own projections and MLP sit outside this op.
+    """
+
+    def __init__(self, grid, window, periodic, heads, head_dim, batch=1, dtype="bf16", has_land=False,
+                 impl="auto", device=None):
+        shift = tuple(w // 2 if g > w // 2 else 0 for g, w in zip(grid, window))
+        self.shift = shift
+        self.wmsa = SwinWindowAttention(grid, window, (0,) * len(grid), periodic, heads, head_dim, batch, dtype,
+                                        has_land, impl, device)
+        self.swmsa = SwinWindowAttention(grid, window, shift, periodic, heads, head_dim, batch, dtype, has_land,
+                                         impl, device)
+
+    def forward(self, first, second, land=None):
+        """first, second: (q, k, v, bias) of the W-MSA and the SW-MSA layer.
+        Returns ((O, lse) of the first, (O, lse) of the second)."""
+        return self.wmsa.forward(*first, land=land), self.swmsa.forward(*second, land=land)
+
+    def backward(self, first, second, dout_first, dout_second, lse_first, lse_second, land=None):
+        """Gradients (dq, dk, dv, dbias) of both layers, second layer first
+        (the order a training step runs them)."""
+        g2 = self.swmsa.backward(*second[:3], dout_second, lse_second, second[3], land)
+        g1 = self.wmsa.backward(*first[:3], dout_first, lse_first, first[3], land)
+        return g1, g2
