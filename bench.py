@@ -80,7 +80,10 @@ def roof_us(flop, nbytes, peaks):
 # per-config bars: forward >= 50 % and backward >= 35 % of the roofline (bf16)
 TARGETS = {"tiny_fp32": None, "grid1deg": {"fwd": 0.50}, "ragged": {"fwd": 0.50, "bwd": 0.35},
            "eddy_ocean": {"fwd": 0.50, "bwd": 0.35}, "depth3d": {"fwd": 0.50, "bwd": 0.35}}
-NOTES = {"tiny_fp32": "fp32 SIMT path, 512 tokens: launch-bound, parity only",
+# timed beside the five configurations (no bar of its own): the large-window regime
+EXTRA = ["terra_w32"]
+NOTES = {"terra_w32": "windows of 1 024 tokens, head_dim 128: key-tiled tcgen05 kernels; tensor-bound",
+         "tiny_fp32": "fp32 SIMT path, 512 tokens: launch-bound, parity only",
          "grid1deg": "forward only (inference: no LSE written, its bytes not counted)",
          "eddy_ocean": "not ragged: 256 = 32 x 8 rows divide into 8-row windows; irregular through the land mask"}
 FLUSH_BYTES = 1 << 30
@@ -110,13 +113,23 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
     ws = attn.workspace()
     stream = torch.cuda.current_stream()
     fwd_t, bwd_t = [], []
+    backward = wl.backward
+    if backward:
+        try:  # a kernel family without a backward yet is timed forward only
+            C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], bias, land, o, lse, stream)
+            C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, bias, land, dq, dk, dv, dbias, ws,
+                            stream)
+        except C.SwinAttnError as e:
+            if e.code != C.SWIN_ERR_UNSUPPORTED:
+                raise
+            backward = False
     for r in range(warmup + reps):
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         flush.add_(1)
         ev[0].record(stream)
         C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], bias, land, o, lse if wl.backward else None, stream)
         ev[1].record(stream)
-        if wl.backward:
+        if backward:
             flush.add_(1)
             ev[2].record(stream)
             C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, bias, land, dq, dk, dv, dbias, ws,
@@ -125,7 +138,7 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
         torch.cuda.synchronize()
         if r >= warmup:
             fwd_t.append(ev[0].elapsed_time(ev[1]) * 1e3)
-            if wl.backward:
+            if backward:
                 bwd_t.append(ev[2].elapsed_time(ev[3]) * 1e3)
     assert C.swin_attn_status(attn.plan) == 0
     tokens = wl.batch * wl.tokens
@@ -136,13 +149,15 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
            "fwd": {"us": fwd_us, "us_min": min(fwd_t), "mtok_s": tokens / fwd_us, "tflops": fwd_flop / fwd_us / 1e6,
                    "roof_us": f_roof, "roof_frac": f_roof / fwd_us, "alg_bytes": fwd_bytes,
                    "lse_written": bool(wl.backward)}}
-    if wl.backward:
+    if backward:
         bwd_us = statistics.median(bwd_t)
         b_roof = roof_us(bwd_flop, bwd_bytes, peaks)
         res["bwd"] = {"us": bwd_us, "us_min": min(bwd_t), "tflops": bwd_flop / bwd_us / 1e6, "roof_us": b_roof,
                       "roof_frac": b_roof / bwd_us, "alg_bytes": bwd_bytes,
                       "roof_frac_moved": roof_us(bwd_flop, bwd_moved, peaks) / bwd_us, "alg_bytes_moved": bwd_moved}
         res["fwd_bwd_mtok_s"] = tokens / (fwd_us + bwd_us)
+    elif wl.backward:
+        res["bwd"] = "no backward kernel for this configuration yet"
     tgt = TARGETS.get(wl.name)
     res["target"] = tgt
     if tgt:
@@ -642,7 +657,7 @@ def main():
         csampler = ClockSampler(dev.index)
         csampler.start()
         configs = {}
-        for name in TARGETS:
+        for name in list(TARGETS) + EXTRA:
             cwl = workloads.WORKLOADS[name]
             cx = x if name == wl.name else workloads.generate(cwl)
             configs[name] = time_config(cwl, cx, peaks, flush, reps=args.config_reps, warmup=10)

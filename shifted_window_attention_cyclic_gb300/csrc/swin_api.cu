@@ -31,6 +31,7 @@ struct swin_attn_plan_s {
   int *d_head_slot_begin;  // [heads + 1]
   uint64_t wait_limit_ns;  // bound of every in-kernel wait
   int debug_force_timeout;
+  bool large;              // head_dim 128: key-tiled kernels for windows of any size
 };
 
 namespace {
@@ -67,6 +68,9 @@ __global__ void fold_kernel(FoldArgs a) {
   a.dbias[x] = sum;
 }
 
+constexpr int64_t kMaxSlots = 65536;       // slots per window
+constexpr int64_t kMaxRelidxSlots = 2048;  // the plan keeps the [n][n] bias-row table up to this n
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
@@ -85,10 +89,12 @@ int check_desc(const swin_attn_desc *d) {
     if (d->periodic[a] != 0 && d->periodic[a] != 1) return SWIN_ERR_INVALID_ARG;
     tokens *= d->grid[a];
     n *= d->window[a];
-    if (tokens >= (int64_t(1) << 31) || n > 128) return SWIN_ERR_UNSUPPORTED;
+    if (tokens >= (int64_t(1) << 31) || n > kMaxSlots) return SWIN_ERR_UNSUPPORTED;
   }
-  if (n > 128) return SWIN_ERR_UNSUPPORTED;
-  if (d->head_dim != 16 && d->head_dim != 32) return SWIN_ERR_UNSUPPORTED;
+  if (d->head_dim != 16 && d->head_dim != 32 && d->head_dim != 128) return SWIN_ERR_UNSUPPORTED;
+  // windows of more than 128 slots: head_dim 128, bf16 (the key-tiled kernels)
+  if ((n > 128 || d->head_dim == 128) && (d->head_dim != 128 || d->dtype != SWIN_BF16 || d->impl == SWIN_IMPL_SIMT))
+    return SWIN_ERR_UNSUPPORTED;
   // The kernels keep the batch in an int and address the [B*T, C] row view
   // (TMA coordinates, land bytes) with 32-bit row numbers.
   if (d->batch > INT32_MAX || d->batch * tokens >= (int64_t(1) << 31)) return SWIN_ERR_UNSUPPORTED;
@@ -141,6 +147,7 @@ Geo make_geo(const swin_attn_desc *d) {
   }
   g.n = g.w[0] * g.w[1] * g.w[2];
   g.nwin = g.nw[0] * g.nw[1] * g.nw[2];
+  g.nqt = (g.n + 127) / 128;
   g.wstep = window_step(g.nwin);
   g.tokens = g.G[0] * g.G[1] * g.G[2];
   g.rstride[2] = 1;
@@ -217,14 +224,17 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
     return SWIN_ERR_CUDA;
   }
   // kernel family
-  const bool tc_ok = tc_supported(g, desc->dtype);
-  if (desc->impl == SWIN_IMPL_TC && !tc_ok) {
+  p->large = desc->head_dim == 128;
+  const bool tc_ok = p->large ? large_supported(g, desc->dtype) : tc_supported(g, desc->dtype);
+  if ((desc->impl == SWIN_IMPL_TC || p->large) && !tc_ok) {
     free_plan(p);
     return SWIN_ERR_UNSUPPORTED;
   }
   p->impl = desc->impl == SWIN_IMPL_AUTO ? (tc_ok ? SWIN_IMPL_TC : SWIN_IMPL_SIMT) : desc->impl;
-  if (p->impl == SWIN_IMPL_TC && ((g.n + 15) & ~15) + g.n <= 128) set_pack(p->g, 2);
-  p->items = (int64_t)g.heads * g.batch * g.nitem;
+  if (!p->large && p->impl == SWIN_IMPL_TC && ((g.n + 15) & ~15) + g.n <= 128) set_pack(p->g, 2);
+  // work items: (head, image, window group) for the small-window kernels,
+  // (head, image, window, query tile) for the head_dim-128 kernels
+  p->items = p->large ? (int64_t)g.heads * g.batch * g.nwin * g.nqt : (int64_t)g.heads * g.batch * g.nitem;
   int fwd_bps = 1, bwd_bps = 1;
   if (p->impl == SWIN_IMPL_SIMT) {
     if (simt_occupancy(false, g, desc->dtype, &fwd_bps) || simt_occupancy(true, g, desc->dtype, &bwd_bps)) {
@@ -237,7 +247,7 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
   }
   p->fwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, fwd_bps) * p->num_sms);
   p->bwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, bwd_bps) * p->num_sms);
-  if (p->impl == SWIN_IMPL_TC && g.heads <= p->num_sms) {
+  if (p->impl == SWIN_IMPL_TC && !p->large && g.heads <= p->num_sms) {
     // A whole number of CTAs per head: the Eq. (4) split then gives CTA
     // h*k + j the same windows of every head h, so CTAs of adjacent heads
     // run in step and each 128-byte L2 fill (two heads' 64-byte rows of one
@@ -265,7 +275,7 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
   bool ok = cudaMalloc(&p->d_win_src, sizeof(int32_t) * nslots) == cudaSuccess &&
             cudaMalloc(&p->d_region, nslots) == cudaSuccess &&
             cudaMalloc(&p->d_tok_dst, sizeof(int32_t) * g.tokens) == cudaSuccess &&
-            cudaMalloc(&p->d_relidx, sizeof(int32_t) * g.n * g.n) == cudaSuccess &&
+            (g.n > kMaxRelidxSlots || cudaMalloc(&p->d_relidx, sizeof(int32_t) * g.n * g.n) == cudaSuccess) &&
             cudaMalloc(&p->d_status, sizeof(int)) == cudaSuccess &&
             cudaMalloc(&p->d_slot_base, sizeof(int) * p->bwd_ctas) == cudaSuccess &&
             cudaMalloc(&p->d_head_slot_begin, sizeof(int) * (g.heads + 1)) == cudaSuccess;
@@ -276,7 +286,7 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
   if (ok) {
     const int blocks = (int)std::min<int64_t>((nslots + 255) / 256, 4096);
     tables_kernel<<<blocks, 256>>>(g, p->d_win_src, p->d_region, p->d_tok_dst);
-    relidx_kernel<<<(g.n * g.n + 255) / 256, 256>>>(g, p->d_relidx);
+    if (p->d_relidx) relidx_kernel<<<(int)std::min<int64_t>(((int64_t)g.n * g.n + 255) / 256, 65535), 256>>>(g, p->d_relidx);
     ok = cudaGetLastError() == cudaSuccess && cudaDeviceSynchronize() == cudaSuccess;
   }
   if (!ok) {
@@ -309,7 +319,8 @@ int swin_attn_plan_tables(swin_attn_plan_t p, int32_t *win_src, uint8_t *region,
   if (win_src) ok = ok && cudaMemcpy(win_src, p->d_win_src, 4 * nslots, cudaMemcpyDeviceToHost) == cudaSuccess;
   if (region) ok = ok && cudaMemcpy(region, p->d_region, nslots, cudaMemcpyDeviceToHost) == cudaSuccess;
   if (tok_dst) ok = ok && cudaMemcpy(tok_dst, p->d_tok_dst, 4 * (int64_t)p->g.tokens, cudaMemcpyDeviceToHost) == cudaSuccess;
-  if (relidx) ok = ok && cudaMemcpy(relidx, p->d_relidx, 4 * p->g.n * p->g.n, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (relidx && !p->d_relidx) return SWIN_ERR_UNSUPPORTED;  // not kept for windows of more than 2048 slots
+  if (relidx) ok = ok && cudaMemcpy(relidx, p->d_relidx, 4 * (int64_t)p->g.n * p->g.n, cudaMemcpyDeviceToHost) == cudaSuccess;
   return ok ? SWIN_OK : SWIN_ERR_CUDA;
 }
 
@@ -345,6 +356,7 @@ int swin_attn_fwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.scale = 1.0f / sqrtf((float)p->g.hd);
   a.wait_limit_ns = p->wait_limit_ns;
   a.debug_force_timeout = p->debug_force_timeout;
+  if (p->large) return launch_fwd_large(a, stream);
   if (p->impl == SWIN_IMPL_TC) return launch_fwd_tc(a, stream);
   return launch_fwd_simt(a, p->d.dtype, stream);
 }
@@ -387,6 +399,7 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.scale = 1.0f / sqrtf((float)p->g.hd);
   a.wait_limit_ns = p->wait_limit_ns;
   a.debug_force_timeout = p->debug_force_timeout;
+  if (p->large) return SWIN_ERR_UNSUPPORTED;
   rc = p->impl == SWIN_IMPL_TC ? launch_bwd_tc(a, stream) : launch_bwd_simt(a, p->d.dtype, stream);
   if (rc || !dbias) return rc;
   FoldArgs f;

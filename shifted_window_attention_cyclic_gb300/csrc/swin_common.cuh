@@ -30,6 +30,7 @@ struct Geo {
   int pack, nitem;  // nitem = ceil(nwin / pack) items per (head, image) block
   int offb, rows;
   int istep;        // (pack * wstep) mod nwin: window step from one item to the next
+  int nqt;         // query (= key) tiles of 128 slots per window (head_dim-128 kernels)
   int tokens;      // tokens per image
   int T;           // bias rows
   int rstride[3];  // prod_{e>d} (2 w_e - 1)

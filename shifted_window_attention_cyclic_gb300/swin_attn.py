@@ -178,14 +178,18 @@ def swin_attn_plan(desc: swin_attn_desc) -> Plan:
     return Plan(h, desc)
 
 
+RELIDX_MAX_SLOTS = 2048  # the plan keeps the [n][n] bias-row table for windows up to this size
+
+
 def swin_attn_plan_tables(plan: Plan):
-    """(win_src [nwin, n] int32, region [nwin, n] uint8, tok_dst [N] int32, relidx [n, n] int32)."""
+    """(win_src [nwin, n] int32, region [nwin, n] uint8, tok_dst [N] int32, relidx [n, n] int32, or None
+    for windows of more than RELIDX_MAX_SLOTS slots)."""
     nwin, n, N = plan.info.windows_per_image, plan.info.slots, plan.info.tokens_per_image
     win_src = np.empty((nwin, n), np.int32)
     region = np.empty((nwin, n), np.uint8)
     tok_dst = np.empty((N,), np.int32)
-    relidx = np.empty((n, n), np.int32)
-    p = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    relidx = np.empty((n, n), np.int32) if n <= RELIDX_MAX_SLOTS else None
+    p = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
     _check(load_library().swin_attn_plan_tables(plan.handle, p(win_src), p(region), p(tok_dst), p(relidx)),
            "swin_attn_plan_tables")
     return win_src, region, tok_dst, relidx

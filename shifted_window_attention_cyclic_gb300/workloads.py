@@ -15,6 +15,8 @@ Grids (stand-ins for datasets that are not used here):
                    window 8x12, shift (4,6), blocked land mask p=0.3
   * depth3d        16 levels x 192x384, window 2x8x8, shift (1,4,4), land mask
                    whose probability grows from 0.3 (level 0) to 0.6 (level 15)
+  * terra_w32      256x540 with TERRA's large windows: 32x32 (1 024 tokens),
+                   shift (16,16), 8 heads of 128 channels, land p=0.3
 
 Recipe: numpy Generator(PCG64(20260 + index)); draws in the fixed order
 Q, K, V, bias, dO, land-xi. Q/K/V/dO ~ N(0,1), bias ~ N(0, 0.02), drawn in
@@ -69,6 +71,12 @@ WORKLOADS = {
     "eddy_ocean": Workload("eddy_ocean", 3, "bf16", 1, (256, 540), (8, 12), (4, 6), (0, 1), 16, 32, (0.3, 0.3), True),
     "depth3d": Workload("depth3d", 4, "bf16", 1, (16, 192, 384), (2, 8, 8), (1, 4, 4), (0, 0, 1), 8, 32,
                         (0.3, 0.6), True),
+    # TERRA's large-window regime (windows of w = 32 per side, 1 024 tokens,
+    # Nh = 8 heads of d/Nh = 128 channels) on the eddy-resolving stage's
+    # 256 x 540 token grid, shift (16, 16), lon periodic, land p = 0.3:
+    # 283 MB per tensor, larger than L2
+    "terra_w32": Workload("terra_w32", 6, "bf16", 1, (256, 540), (32, 32), (16, 16), (0, 1), 8, 128, (0.3, 0.3),
+                          True),
     # half of depth3d (8 levels, same window/shift/land recipe): the profiling
     # case for ncu captures, still larger than L2 (302 MB per tensor)
     "depth3d_8lvl": Workload("depth3d_8lvl", 5, "bf16", 1, (8, 192, 384), (2, 8, 8), (1, 4, 4), (0, 0, 1), 8, 32,

@@ -1,0 +1,55 @@
+"""Windows of more than 128 slots with head_dim 128 (the key-tiled tcgen05
+kernels) against the oracle, through the C ABI: TERRA's w = 32 windows
+(1 024 tokens, 8 key tiles, d/Nh = 128) on a grid with a periodic seam and
+land, a ragged 3-D case with partial tiles, a window of fewer than 128
+slots, and a window without a bias whose bias table would not fit the
+kernel's column."""
+import numpy as np
+import pytest
+
+import oracle
+from shifted_window_attention_cyclic_gb300 import workloads
+from tests.parity_util import assert_close, host, problem_of, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # grid, window, shift, periodic, heads, batch, land, bias
+    ((64, 64), (32, 32), (16, 16), (0, 1), 2, 1, (0.3, 0.3), True),         # n = 1024, 8 key tiles
+    ((3, 40, 70), (2, 16, 16), (1, 8, 8), (0, 0, 1), 1, 1, (0.2, 0.5), True),  # n = 512, ragged in lat and lon
+    ((21, 45), (8, 12), (4, 6), (0, 1), 2, 2, None, True),                    # n = 96: one partial tile
+    ((60, 200), (30, 100), (15, 50), (0, 1), 1, 1, None, False),              # n = 3000, no bias (59 x 199 rows)
+]
+
+
+def _lse_check(got, ref):
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin)
+    if fin.any():
+        assert np.abs(got[fin] - ref[fin]).max() <= 2e-3
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_large_window_forward_matches_the_oracle(case):
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    grid, window, shift, periodic, heads, batch, land_p, with_bias = case
+    wl = workloads.custom(grid, window, shift, periodic, heads, 128, batch, "bf16", land_p,
+                          seed_index=900 + CASES.index(case))
+    x = workloads.generate(wl)
+    if not with_bias:
+        x["bias"] = np.zeros_like(x["bias"])
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.dtype,
+                               wl.has_land)
+    assert attn.info.impl == C.SWIN_IMPL_TC
+    assert attn.info.work_items == heads * batch * attn.info.windows_per_image * -(-attn.info.slots // 128)
+    t = to_device(x, wl, torch.device("cuda", 0))
+    o, lse = attn.forward(t["q"], t["k"], t["v"], t["bias"] if with_bias else None, t["land"])
+    torch.cuda.synchronize()
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK
+    o_ref, lse_ref = oracle.fwd(problem_of(wl), x["q"], x["k"], x["v"], x["bias"], x["land"])
+    assert_close("O", host(o), o_ref, "bf16")
+    _lse_check(lse.cpu().numpy().astype(np.float64), lse_ref)
+    if x["land"] is not None:
+        assert np.all(host(o)[x["land"].astype(bool)] == 0.0)
