@@ -175,6 +175,14 @@ void free_plan(swin_attn_plan_s *p) {
   delete p;
 }
 
+// head_dim-128 plans keep delta_i = sum_j P_ij dP_ij of every query ([B][heads][tokens]
+// float) at the start of the workspace, ahead of the partial dBias tables.
+size_t delta_bytes(const swin_attn_plan_s *p) {
+  if (!p->large) return 0;
+  const size_t bytes = (size_t)p->g.batch * p->g.heads * p->g.tokens * sizeof(float);
+  return (bytes + 255) & ~size_t(255);
+}
+
 int current_device_matches(const swin_attn_plan_s *p) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return SWIN_ERR_CUDA;
@@ -257,7 +265,7 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
     p->fwd_ctas = p->bwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)k * g.heads);
   }
   // workspace slots: one partial dBias table per (CTA, head it touches)
-  const int64_t per_head = (int64_t)g.batch * g.nitem;
+  const int64_t per_head = p->items / g.heads;
   std::vector<int> slot_base(p->bwd_ctas), slot_head;
   for (int r = 0; r < p->bwd_ctas; ++r) {
     int64_t L, R;
@@ -327,7 +335,7 @@ int swin_attn_plan_tables(swin_attn_plan_t p, int32_t *win_src, uint8_t *region,
 size_t swin_attn_workspace_bytes(swin_attn_plan_t p) {
   if (!p) return 0;
   const size_t bytes = (size_t)p->ws_slots * p->g.T * sizeof(float);
-  return (bytes + 255) & ~size_t(255);
+  return delta_bytes(p) + ((bytes + 255) & ~size_t(255));
 }
 
 int swin_attn_fwd(swin_attn_plan_t p, const void *q, const void *k, const void *v, const float *bias,
@@ -372,7 +380,7 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   if (!aligned16(lse) || (bias && !aligned4(bias)) || (dbias && !aligned4(dbias)) ||
       (p->d.has_land && !aligned4(land)))
     return SWIN_ERR_ALIGNMENT;
-  if (dbias) {
+  if (dbias || p->large) {  // head_dim-128 plans always keep delta in the workspace
     if (!workspace || workspace_bytes < swin_attn_workspace_bytes(p)) return SWIN_ERR_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SWIN_ERR_ALIGNMENT;
   }
@@ -390,7 +398,8 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;
-  a.ws = dbias ? static_cast<float *>(workspace) : nullptr;
+  a.delta = p->large ? static_cast<float *>(workspace) : nullptr;
+  a.ws = dbias ? reinterpret_cast<float *>(static_cast<char *>(workspace) + delta_bytes(p)) : nullptr;
   a.slot_base = p->d_slot_base;
   a.ws_slots = p->ws_slots;
   a.status = p->d_status;
@@ -399,8 +408,8 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.scale = 1.0f / sqrtf((float)p->g.hd);
   a.wait_limit_ns = p->wait_limit_ns;
   a.debug_force_timeout = p->debug_force_timeout;
-  if (p->large) return SWIN_ERR_UNSUPPORTED;
-  rc = p->impl == SWIN_IMPL_TC ? launch_bwd_tc(a, stream) : launch_bwd_simt(a, p->d.dtype, stream);
+  rc = p->large ? launch_bwd_large(a, stream)
+       : p->impl == SWIN_IMPL_TC ? launch_bwd_tc(a, stream) : launch_bwd_simt(a, p->d.dtype, stream);
   if (rc || !dbias) return rc;
   FoldArgs f;
   f.ws = a.ws;

@@ -227,6 +227,7 @@ struct BwdArgs {
   const uint8_t *land;
   void *dq, *dk, *dv;
   float *ws;              // [slots][T] partial dBias tables, or nullptr (dbias not wanted)
+  float *delta;           // head_dim-128 kernels: [B][heads][tokens] delta_i, or nullptr
   int64_t ws_slots;       // slots of ws
   const int *slot_base;   // [ctas] first workspace slot of each CTA
   int *status;

@@ -31,32 +31,14 @@
 //    rows (and the log-sum-exp) at the query slots' tokens.
 // Masked keys (other region, land, pad) get -2^100 from the mask MMA and so
 // exactly zero probability. Every wait is bounded, as in the small kernels.
-#include <cuda.h>
 #include <cuda_bf16.h>
-#include <cuda_runtime.h>
-#include <cudaTypedefs.h>
 
-#include <mutex>
-
-#include "swin_tc.cuh"
-#include "tc_ptx.cuh"
+#include "swin_large.cuh"
 
 namespace swin {
+namespace lg {
 namespace {
 
-using namespace ptx;
-
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-constexpr uint16_t kBf16One = 0x3F80;     // 1.0
-constexpr uint16_t kBf16NegBig = 0xF180;  // -2^100
-
-namespace lg {
-
-constexpr int kHd = 128;
-constexpr int kHalfBytes = 128 * 128;      // 128 rows x 64 bf16 (one channel half), 128-byte swizzle
-constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
-constexpr int kMaskBytes = 128 * 32;        // 128 rows x 16 bf16, 32-byte swizzle
 constexpr int kStages = 2;                  // key/value stages (= S buffers in TMEM)
 constexpr int kQ = 0, kQm = kTileBytes;
 constexpr int kStage0 = kQm + kMaskBytes;   // 36 KB, 1024-aligned
@@ -80,75 +62,8 @@ static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may 
 constexpr int kSoftmaxWarps = 8, kEpilogueWarp0 = 8, kQWarp = 12, kKWarp = 13, kVWarp = 14, kMmaWarp = 15;
 constexpr int kThreads = 16 * 32;
 // TMEM columns: S of key tile t at 128 * (t % 2); O half h at 256 + 128 h
-constexpr uint32_t kTmemCols = 512, kColO = 256;
+constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past 2^8
-
-__device__ __forceinline__ uint32_t sw32(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
-
-// Item = (h, b, window, query tile), query tile fastest.
-struct LItem {
-  int h, b, omega, qt;
-};
-__device__ __forceinline__ LItem decode(const Geo &g, int64_t it) {
-  LItem x;
-  x.qt = (int)(it % g.nqt);
-  int64_t t = it / g.nqt;
-  x.omega = (int)(t % g.nwin);
-  t /= g.nwin;
-  x.b = (int)(t % g.batch);
-  x.h = (int)(t / g.batch);
-  return x;
-}
-
-// Mask row chunk 0 (region codes < 8): query rows carry a one-hot of the
-// region code (live queries), key rows 0 in the column of their code if live
-// and -2^100 elsewhere; columns 8..15 are constant (0 / -2^100).
-__device__ __forceinline__ uint4 mask_chunk(bool live, int reg, bool key) {
-  const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
-  const uint32_t other = key ? nb2 : 0u;
-  const uint32_t hit = !live ? other
-                       : key ? ((reg & 1) ? (uint32_t)kBf16NegBig : (uint32_t)kBf16NegBig << 16)
-                             : ((reg & 1) ? (uint32_t)kBf16One << 16 : (uint32_t)kBf16One);
-  const int t = reg >> 1;
-  return make_uint4(t == 0 ? hit : other, t == 1 ? hit : other, t == 2 ? hit : other, t == 3 ? hit : other);
-}
-
-// Routes of the four slots 4*lane .. 4*lane+3 of tile `tile` of window omega:
-// grid token (or -1 for pads and slots past the window), region bits, and
-// (keys) the key side of the bias row offset.
-struct Quad {
-  int src[4], reg[4], roff[4];
-};
-__device__ __forceinline__ Quad route_quad(const Geo &g, int omega, int tile, int lane) {
-  int wc[3];
-  window_coords(g, omega, wc);
-  Quad q;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int slot = tile * 128 + 4 * lane + j;
-    if (slot < g.n) {
-      const SlotRoute r = slot_route(g, wc, slot);
-      q.src[j] = r.src;
-      q.reg[j] = r.reg;
-      q.roff[j] = r.roff;
-    } else {
-      q.src[j] = -1;
-      q.reg[j] = 0;
-      q.roff[j] = 0;
-    }
-  }
-  return q;
-}
-
-// TMA gather4 of the lane's four rows (both 64-channel halves of head h) of
-// one [B*T, C] tensor into a 128-row tile; pads read token 0 of the image.
-__device__ __forceinline__ void gather_rows(uint32_t dst_tile, const CUtensorMap *rows, const Quad &q, int b,
-                                            int tokens, int h, int lane, uint32_t bar) {
-  const int r0 = b * tokens;
-  const int r[4] = {r0 + max(q.src[0], 0), r0 + max(q.src[1], 0), r0 + max(q.src[2], 0), r0 + max(q.src[3], 0)};
-  tma_gather4(dst_tile + 512u * lane, rows, h * kHd, r[0], r[1], r[2], r[3], bar);
-  tma_gather4(dst_tile + kHalfBytes + 512u * lane, rows, h * kHd + 64, r[0], r[1], r[2], r[3], bar);
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_large_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -214,9 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const LItem x = decode(g, L + it);
       const Quad q = route_quad(g, x.omega, x.qt, lane);
       bool live[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        live[j] = q.src[j] >= 0 && (!a.land || __ldg(a.land + (int64_t)x.b * g.tokens + q.src[j]) == 0);
+      quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
       if (it > 0 && !mbar_wait_warp(bar(bQFree), (uint32_t)(it - 1) & 1u, ctl)) break;
       const int rows = min(128, g.n - x.qt * 128), nq4 = (rows + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(bQFull), (uint32_t)nq4 * 4u * 256u);
@@ -238,11 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kt = (int)(t % nkt);
       const Quad q = route_quad(g, x.omega, kt, lane);
       bool live[4];
-      if (kw) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          live[j] = q.src[j] >= 0 && (!a.land || __ldg(a.land + (int64_t)x.b * g.tokens + q.src[j]) == 0);
-      }
+      if (kw) quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
       if (t >= kStages && !mbar_wait_warp(bar(bEmpty + s), (uint32_t)((t / kStages) - 1) & 1u, ctl)) break;
       const uint32_t st = sbase + kStage0 + s * kStageBytes;
       uint8_t *sp = smem + kStage0 + s * kStageBytes;
@@ -279,11 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kt == 0 && !mbar_wait(bar(bQFull), (uint32_t)it & 1u, ctl)) return false;
         tc_fence_after();
         const uint32_t st = sbase + kStage0 + s * kStageBytes, d = tmem + 128u * s;
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kHalfBytes + 32u * (kk & 3);
-          mma_ss(d, smem_desc(sbase + kQ + off, 16, 1024, kSwizzle128B), smem_desc(st + kK + off, 16, 1024, kSwizzle128B),
-                 idesc_s, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(d, kmajor_desc(sbase + kQ, kk), kmajor_desc(st + kK, kk), idesc_s, kk > 0 ? 1u : 0u);
         mma_ss(d, smem_desc(sbase + kQm, 16, 256, kSwizzle32B), smem_desc(st + kKm, 16, 256, kSwizzle32B), idesc_s, 1);
         mma_commit(bar(bSFull + s));
         if (kt == nkt - 1) mma_commit(bar(bQFree));
@@ -299,10 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int h = 0; h < 2; ++h)
           for (int kk = 0; kk < 4; ++kk) {
             // keys 64h + 16kk ..: P from TMEM, V rows from the stage (channels = N, MN-major)
-            const uint32_t vrow = (uint32_t)(64 * h + 16 * kk) * 128u;
-            mma_ts(tmem + kColO + 128u * h, tmem + 128u * s + 64u * h + 16u * kk,
-                   smem_desc(st + kV + vrow, kHalfBytes, 1024, kSwizzle128B), idesc_pv,
-                   (kt > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + kColO + 128u * h, tmem + 128u * s + 64u * h + 16u * kk, nmajor_desc(st + kV, 64 * h + 16 * kk),
+                   idesc_pv, (kt > 0 || kk > 0) ? 1u : 0u);
           }
         mma_commit(bar(bEmpty + s));
         if (kt == nkt - 1) mma_commit(bar(bOFull));
@@ -516,38 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point.
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  });
-  return fn;
-}
-
-// Row view [B*T, C] of a bf16 tensor for TMA gather4: box one row high and 64
-// channels (128 bytes) wide, 128-byte swizzle (the layout of the operand
-// tile halves).
-bool rows128_map(CUtensorMap *m, const void *base, const Geo &g) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)g.C, (cuuint64_t)g.batch * (cuuint64_t)g.tokens};
-  cuuint64_t strides[1] = {dims[0] * 2};
-  cuuint32_t box[2] = {64u, 1u};
-  cuuint32_t es[2] = {1u, 1u};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-}  // namespace lg
 }  // namespace
+}  // namespace lg
 
 bool large_supported(const Geo &g, int dtype) {
   return dtype == SWIN_BF16 && g.hd == lg::kHd && (int64_t)g.batch * g.tokens <= INT32_MAX;

@@ -1,0 +1,147 @@
+// swin_large.cuh -- shared pieces of the head_dim-128 kernels (windows of any
+// size, key-tiled): tile layouts, work-item decoding, slot routing of a
+// 128-slot tile, TMA row gathers and the mask rows.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "swin_tc.cuh"
+#include "tc_ptx.cuh"
+
+namespace swin {
+namespace lg {
+
+using namespace ptx;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr uint16_t kBf16One = 0x3F80;     // 1.0
+constexpr uint16_t kBf16NegBig = 0xF180;  // -2^100
+
+constexpr int kHd = 128;
+constexpr int kHalfBytes = 128 * 128;      // 128 rows x 64 bf16 (one channel half), 128-byte swizzle
+constexpr int kTileBytes = 2 * kHalfBytes;  // 128 rows x 128 bf16
+constexpr int kMaskBytes = 128 * 32;        // 128 rows x 16 bf16, 32-byte swizzle
+constexpr uint32_t kTmemCols = 512;
+
+__device__ __forceinline__ uint32_t sw32(int r, int c) { return r * 32 + ((c ^ ((r >> 2) & 1)) << 4); }
+
+// Item = (h, b, window, tile), tile fastest.
+struct LItem {
+  int h, b, omega, qt;
+};
+__device__ __forceinline__ LItem decode(const Geo &g, int64_t it) {
+  LItem x;
+  x.qt = (int)(it % g.nqt);
+  int64_t t = it / g.nqt;
+  x.omega = (int)(t % g.nwin);
+  t /= g.nwin;
+  x.b = (int)(t % g.batch);
+  x.h = (int)(t / g.batch);
+  return x;
+}
+
+// Mask row chunk 0 (region codes < 8): query rows carry a one-hot of the
+// region code (live queries), key rows 0 in the column of their code if live
+// and -2^100 elsewhere; columns 8..15 are constant (0 / -2^100).
+__device__ __forceinline__ uint4 mask_chunk(bool live, int reg, bool key) {
+  const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
+  const uint32_t other = key ? nb2 : 0u;
+  const uint32_t hit = !live ? other
+                       : key ? ((reg & 1) ? (uint32_t)kBf16NegBig : (uint32_t)kBf16NegBig << 16)
+                             : ((reg & 1) ? (uint32_t)kBf16One << 16 : (uint32_t)kBf16One);
+  const int t = reg >> 1;
+  return make_uint4(t == 0 ? hit : other, t == 1 ? hit : other, t == 2 ? hit : other, t == 3 ? hit : other);
+}
+
+// Routes of the four slots 4*lane .. 4*lane+3 of tile `tile` of window omega:
+// grid token (or -1 for pads and slots past the window), region bits, and
+// the query and key sides of the bias row offset.
+struct Quad {
+  int src[4], reg[4], roff[4], rbase[4];
+};
+__device__ __forceinline__ Quad route_quad(const Geo &g, int omega, int tile, int lane) {
+  int wc[3];
+  window_coords(g, omega, wc);
+  Quad q;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int slot = tile * 128 + 4 * lane + j;
+    if (slot < g.n) {
+      const SlotRoute r = slot_route(g, wc, slot);
+      q.src[j] = r.src;
+      q.reg[j] = r.reg;
+      q.roff[j] = r.roff;
+      q.rbase[j] = r.rbase;
+    } else {
+      q.src[j] = -1;
+      q.reg[j] = 0;
+      q.roff[j] = 0;
+      q.rbase[j] = g.T - 1;  // keeps rbase - roff inside the bias column
+    }
+  }
+  return q;
+}
+
+// Land test of the quad's live slots (land may be null).
+__device__ __forceinline__ void quad_live(const Quad &q, const uint8_t *land, int64_t tok0, bool (&live)[4]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) live[j] = q.src[j] >= 0 && (!land || __ldg(land + tok0 + q.src[j]) == 0);
+}
+
+// TMA gather4 of the lane's four rows (both 64-channel halves of head h) of
+// one [B*T, C] tensor into a 128-row tile; pads read token 0 of the image.
+__device__ __forceinline__ void gather_rows(uint32_t dst_tile, const CUtensorMap *rows, const Quad &q, int b,
+                                            int tokens, int h, int lane, uint32_t bar) {
+  const int r0 = b * tokens;
+  const int r[4] = {r0 + max(q.src[0], 0), r0 + max(q.src[1], 0), r0 + max(q.src[2], 0), r0 + max(q.src[3], 0)};
+  tma_gather4(dst_tile + 512u * lane, rows, h * kHd, r[0], r[1], r[2], r[3], bar);
+  tma_gather4(dst_tile + kHalfBytes + 512u * lane, rows, h * kHd + 64, r[0], r[1], r[2], r[3], bar);
+}
+
+// K-major 128B-swizzled descriptor of k-step kk (16 channels) of a 128-row
+// tile held as two 64-channel halves.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+  return smem_desc(tile + (uint32_t)(kk >> 2) * kHalfBytes + 32u * (kk & 3), 16, 1024, kSwizzle128B);
+}
+// MN-major (channels = N) descriptor of the 16 rows starting at `row` of such
+// a tile, as the B operand of a product over the rows (N = 128 channels).
+__device__ __forceinline__ uint64_t nmajor_desc(uint32_t tile, int row) {
+  return smem_desc(tile + (uint32_t)row * 128u, kHalfBytes, 1024, kSwizzle128B);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// Row view [B*T, C] of a bf16 tensor for TMA gather4: box one row high and 64
+// channels (128 bytes) wide, 128-byte swizzle (the layout of the operand
+// tile halves).
+inline bool rows128_map(CUtensorMap *m, const void *base, const Geo &g) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)g.C, (cuuint64_t)g.batch * (cuuint64_t)g.tokens};
+  cuuint64_t strides[1] = {dims[0] * 2};
+  cuuint32_t box[2] = {64u, 1u};
+  cuuint32_t es[2] = {1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace lg
+}  // namespace swin

@@ -16,5 +16,7 @@ int launch_bwd_tc(const BwdArgs &a, void *stream);
 bool large_supported(const Geo &g, int dtype);
 int large_max_bias_rows();
 int launch_fwd_large(const FwdArgs &a, void *stream);
+int large_bwd_max_bias_rows();
+int launch_bwd_large(const BwdArgs &a, void *stream);
 
 }  // namespace swin

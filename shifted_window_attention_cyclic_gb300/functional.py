@@ -112,7 +112,7 @@ class SwinWindowAttention:
         dv = torch.empty_like(v) if dv is None else dv
         if dbias is None and want_dbias:
             dbias = self.new_bias()
-        ws = self.workspace() if dbias is not None else None
+        ws = self.workspace()  # dBias partial tables; for head_dim 128 also delta
         C.swin_attn_bwd(self.plan, q, k, v, dout, lse, bias, land if self.has_land else None, dq, dk, dv, dbias,
                         ws, stream)
         return dq, dk, dv, dbias

@@ -1,9 +1,9 @@
 """Windows of more than 128 slots with head_dim 128 (the key-tiled tcgen05
-kernels) against the oracle, through the C ABI: TERRA's w = 32 windows
-(1 024 tokens, 8 key tiles, d/Nh = 128) on a grid with a periodic seam and
-land, a ragged 3-D case with partial tiles, a window of fewer than 128
-slots, and a window without a bias whose bias table would not fit the
-kernel's column."""
+kernels) against the oracle, through the C ABI, forward and backward:
+TERRA's w = 32 windows (1 024 tokens, 8 key tiles, d/Nh = 128) on a grid
+with a periodic seam and land, a ragged 3-D case with partial tiles, a
+window of fewer than 128 slots, and a window without a bias whose bias table
+would not fit the kernels' column (no dBias there)."""
 import numpy as np
 import pytest
 
@@ -53,3 +53,32 @@ def test_large_window_forward_matches_the_oracle(case):
     _lse_check(lse.cpu().numpy().astype(np.float64), lse_ref)
     if x["land"] is not None:
         assert np.all(host(o)[x["land"].astype(bool)] == 0.0)
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_large_window_backward_matches_the_oracle(case):
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    grid, window, shift, periodic, heads, batch, land_p, with_bias = case
+    wl = workloads.custom(grid, window, shift, periodic, heads, 128, batch, "bf16", land_p,
+                          seed_index=900 + CASES.index(case))
+    x = workloads.generate(wl)
+    if not with_bias:
+        x["bias"] = np.zeros_like(x["bias"])
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch, wl.dtype,
+                               wl.has_land)
+    t = to_device(x, wl, torch.device("cuda", 0))
+    bias = t["bias"] if with_bias else None
+    _, lse = attn.forward(t["q"], t["k"], t["v"], bias, t["land"])
+    dq, dk, dv, dbias = attn.backward(t["q"], t["k"], t["v"], t["dout"], lse, bias, t["land"], want_dbias=with_bias)
+    torch.cuda.synchronize()
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK
+    g = oracle.bwd(problem_of(wl), x["q"], x["k"], x["v"], x["bias"], x["land"], x["dout"])
+    for key, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        assert_close(key, host(got), g[key], "bf16")
+    if with_bias:
+        assert_close("dbias", host(dbias), g["dbias"], "bf16")
+    if x["land"] is not None:
+        land = x["land"].astype(bool)
+        for got in (dq, dk, dv):
+            assert np.all(host(got)[land] == 0.0)
