@@ -57,7 +57,7 @@ extern "C" {
 /* Status codes. */
 #define SWIN_OK 0
 #define SWIN_ERR_INVALID_ARG (-1) /* NULL/inconsistent argument or descriptor */
-#define SWIN_ERR_UNSUPPORTED (-2) /* window > 128 slots, head_dim not 16/32, ... */
+#define SWIN_ERR_UNSUPPORTED (-2) /* head_dim not 16/32/128, window too large for head_dim, ... */
 #define SWIN_ERR_ALIGNMENT (-3)   /* a pointer breaks its alignment rule (see Conventions) */
 #define SWIN_ERR_WORKSPACE (-4)   /* workspace NULL or smaller than required */
 #define SWIN_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
@@ -68,10 +68,11 @@ extern "C" {
 #define SWIN_F32 0
 #define SWIN_BF16 1
 
-/* Kernel family. AUTO picks the tensor-core path for bf16 with head_dim 32. */
+/* Kernel family. AUTO picks the tensor-core path for bf16 with head_dim 32 or 128. */
 #define SWIN_IMPL_AUTO 0
-#define SWIN_IMPL_SIMT 1   /* fp32 FFMA kernels (any supported dtype) */
-#define SWIN_IMPL_TC 2     /* tcgen05/TMEM kernels (bf16, head_dim 32) */
+#define SWIN_IMPL_SIMT 1   /* fp32 FFMA kernels (head_dim 16/32, windows up to 128 slots) */
+#define SWIN_IMPL_TC 2     /* tcgen05/TMEM kernels (bf16; head_dim 32 with windows up to 128
+                              slots, or head_dim 128 with windows of any size) */
 
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st *swin_stream_t;
@@ -84,11 +85,12 @@ typedef struct {
   int32_t impl;        /* SWIN_IMPL_* */
   int64_t batch;       /* B >= 1 */
   int32_t grid[3];     /* G_d >= 1, outermost first; batch * prod(G) < 2^31 */
-  int32_t window[3];   /* w_d >= 1; prod(w) <= 128 */
+  int32_t window[3];   /* w_d >= 1; prod(w) <= 128, or <= 65536 with head_dim 128 */
   int32_t shift[3];    /* 0 <= s_d < w_d, s_d < G_d (or 0); all zero = W-MSA */
   int32_t periodic[3]; /* 1 = cyclic neighbour (no region bit), 0 = region-masked */
   int32_t heads;       /* >= 1 */
-  int32_t head_dim;    /* 16 or 32 */
+  int32_t head_dim;    /* 16 or 32; or 128 (bf16, tensor cores): windows of any size, split
+                          into 128-slot query and key tiles with an online softmax */
   int32_t dtype;       /* SWIN_F32 or SWIN_BF16 */
   int32_t has_land;    /* 1 = a land mask is passed to fwd/bwd */
 } swin_attn_desc;
@@ -113,7 +115,8 @@ typedef struct {
  * routing function the kernels use, and the work partition is fixed.
  * Synchronous; allocates device memory owned by the plan.
  * Errors: INVALID_ARG (NULL, bad sizes, shift >= window), UNSUPPORTED
- * (slots > 128, head_dim, dtype, impl not available for the dtype), CUDA. */
+ * (slots > 128 without head_dim 128, slots > 65536, head_dim, dtype, impl not
+ * available for the dtype or head_dim), CUDA. */
 int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out);
 
 /* Copy `plan`'s sizes into *info (host). Errors: INVALID_ARG. */
@@ -123,18 +126,21 @@ int swin_attn_plan_get_info(swin_attn_plan_t plan, swin_attn_plan_info *info);
  *   win_src [nwin][n] int32: grid token feeding slot s of window w, -1 = pad;
  *   region  [nwin][n] uint8: region bits of that token (bit d for dim d), 0 for pads;
  *   tok_dst [N] int32: w*n + s of every token (the inverse route);
- *   relidx  [n][n] int32: bias row of the slot pair (query i, key j).
- * Synchronous. Errors: INVALID_ARG, CUDA. */
+ *   relidx  [n][n] int32: bias row of the slot pair (query i, key j); kept by
+ *           the plan for windows of up to 2048 slots only (UNSUPPORTED above).
+ * Synchronous. Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 int swin_attn_plan_tables(swin_attn_plan_t plan, int32_t *win_src, uint8_t *region,
                           int32_t *tok_dst, int32_t *relidx);
 
-/* Bytes of device workspace swin_attn_bwd needs (partial dBias tables). */
+/* Bytes of device workspace swin_attn_bwd needs: the partial dBias tables,
+ * and for head_dim 128 also delta_i = sum_j P_ij dP_ij of every query. */
 size_t swin_attn_workspace_bytes(swin_attn_plan_t plan);
 
 /* Forward. q, k, v, o as above; bias may be NULL (zero bias); land required
  * iff desc.has_land; lse may be NULL (inference) else receives the float32
  * log-sum-exp. Pad slots write nothing; every grid token is written once.
- * Errors: INVALID_ARG, ALIGNMENT, CUDA (launch). */
+ * head_dim 128: a non-NULL bias needs at most 8192 bias rows (UNSUPPORTED).
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA (launch). */
 int swin_attn_fwd(swin_attn_plan_t plan, const void *q, const void *k, const void *v,
                   const float *bias, const uint8_t *land, void *o, float *lse,
                   swin_stream_t stream);
@@ -144,9 +150,14 @@ int swin_attn_fwd(swin_attn_plan_t plan, const void *q, const void *k, const voi
  * for the same inputs (required). delta_i = sum_j P_ij dP_ij is recomputed
  * in-kernel, so O is not an input. workspace: device, >=
  * swin_attn_workspace_bytes(plan) bytes, 256-byte aligned, contents ignored
- * (not needed when dbias is NULL: pass NULL, 0). When swin_attn_status then
- * reports SWIN_ERR_TIMEOUT, every output of the call is undefined.
- * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, CUDA. */
+ * (not needed when dbias is NULL, except with head_dim 128, whose backward
+ * keeps delta there). head_dim 128: a non-NULL bias needs at most 4096 bias
+ * rows and a non-NULL dbias at most 8192 (UNSUPPORTED); its dBias is summed
+ * per CTA with shared-memory atomic adds, so it may differ between calls in
+ * the last bits (the other outputs, and dBias of head_dim 16/32, do not).
+ * When swin_attn_status then reports SWIN_ERR_TIMEOUT, every output of the
+ * call is undefined.
+ * Errors: INVALID_ARG, ALIGNMENT, WORKSPACE, UNSUPPORTED, CUDA. */
 int swin_attn_bwd(swin_attn_plan_t plan, const void *q, const void *k, const void *v,
                   const void *dout, const float *lse, const float *bias,
                   const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,

@@ -197,7 +197,7 @@ const char *swin_attn_strerror(int status) {
   switch (status) {
     case SWIN_OK: return "ok";
     case SWIN_ERR_INVALID_ARG: return "invalid argument";
-    case SWIN_ERR_UNSUPPORTED: return "unsupported problem (slots > 128, head_dim not 16/32, dtype or impl)";
+    case SWIN_ERR_UNSUPPORTED: return "unsupported problem (window size for the head_dim, head_dim, dtype, impl, bias rows)";
     case SWIN_ERR_ALIGNMENT: return "pointer misaligned (16 bytes; 4 for bias, dbias and land; 256 for workspace)";
     case SWIN_ERR_WORKSPACE: return "workspace missing or too small";
     case SWIN_ERR_CUDA: return "CUDA runtime error";
