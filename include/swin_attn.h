@@ -139,7 +139,7 @@ size_t swin_attn_workspace_bytes(swin_attn_plan_t plan);
 /* Forward. q, k, v, o as above; bias may be NULL (zero bias); land required
  * iff desc.has_land; lse may be NULL (inference) else receives the float32
  * log-sum-exp. Pad slots write nothing; every grid token is written once.
- * head_dim 128: a non-NULL bias needs at most 8192 bias rows (UNSUPPORTED).
+ * head_dim 128: a non-NULL bias needs at most 4096 bias rows (UNSUPPORTED).
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA (launch). */
 int swin_attn_fwd(swin_attn_plan_t plan, const void *q, const void *k, const void *v,
                   const float *bias, const uint8_t *land, void *o, float *lse,

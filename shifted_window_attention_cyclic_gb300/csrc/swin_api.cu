@@ -20,7 +20,8 @@ struct swin_attn_plan_s {
   int num_sms;
   int impl;
   int fwd_ctas, bwd_ctas;
-  int64_t items;
+  int64_t items;           // work items of the backward (and of the forward, but for head_dim 128)
+  int64_t fwd_items;       // work items of the forward
   int64_t ws_slots;
   int32_t *d_win_src;
   uint8_t *d_region;
@@ -253,7 +254,8 @@ int swin_attn_plan(const swin_attn_desc *desc, swin_attn_plan_t *out) {
     fwd_bps = tc_fwd_ctas_per_sm(g);
     bwd_bps = tc_bwd_ctas_per_sm(g);
   }
-  p->fwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, fwd_bps) * p->num_sms);
+  p->fwd_items = p->large ? large_fwd_items(g) : p->items;
+  p->fwd_ctas = (int)std::min<int64_t>(p->fwd_items, (int64_t)std::max(1, fwd_bps) * p->num_sms);
   p->bwd_ctas = (int)std::min<int64_t>(p->items, (int64_t)std::max(1, bwd_bps) * p->num_sms);
   if (p->impl == SWIN_IMPL_TC && !p->large && g.heads <= p->num_sms) {
     // A whole number of CTAs per head: the Eq. (4) split then gives CTA
@@ -359,7 +361,7 @@ int swin_attn_fwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.o = o;
   a.lse = lse;
   a.status = p->d_status;
-  a.items = p->items;
+  a.items = p->fwd_items;
   a.ctas = p->fwd_ctas;
   a.scale = 1.0f / sqrtf((float)p->g.hd);
   a.wait_limit_ns = p->wait_limit_ns;

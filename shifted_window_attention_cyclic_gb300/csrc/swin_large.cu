@@ -11,24 +11,27 @@
 // window and in-window coordinates, Q, K and V rows are gathered straight from
 // the [B, grid, C] tensors by TMA, and O rows are stored at their tokens.
 //
-// Work item = (head, image, window, query tile of 128 slots); each CTA takes a
-// contiguous range of items (TERRA Eq. (4)). Per item the CTA keeps the Q tile
-// in shared memory and streams the window's key tiles through two stages:
-//  * warp 12 loads the Q tile (TMA gather4, two 64-channel halves) and writes
-//    the query mask rows Qm; warp 13 loads K and writes the key mask rows Km
-//    and the key side of the bias offsets; warp 14 loads V;
-//  * warp 15 issues S = Q K^T + Qm Km^T (8 + 1 MMAs, K = 16 each) and
-//    O_h += P_h V (4 MMAs per half h);
-//  * softmax warpgroup h (warps 4h .. 4h+3, thread = query row) takes keys
-//    [64h, 64h + 64) of every key tile: x = S*scale*log2e + bias*log2e, a
-//    running row max m_h and sum l_h, P_h = exp2(x - m_h) in bf16 over S. The
-//    running max is only raised when a tile's max exceeds it by more than 8
-//    (a factor 256): P stays below 256 and O_h (in TMEM) is rescaled rarely;
-//    the final normalisation uses the same max, so the result is exact in
-//    real arithmetic;
-//  * epilogue warps 8-11 combine the halves, O = (a_0 O_0 + a_1 O_1) /
-//    (a_0 l_0 + a_1 l_1) with a_h = exp2(m_h - max(m_0, m_1)), and store the
-//    rows (and the log-sum-exp) at the query slots' tokens.
+// Work item = (head, image, window, pair of query tiles of 128 slots); each
+// CTA takes a contiguous range of items (TERRA Eq. (4)). Both query tiles stay
+// in shared memory and every key tile of the window, streamed through two
+// stages, serves both (half the key/value loads per FLOP of one tile per item):
+//  * warp 12 loads the two Q tiles (TMA gather4, two 64-channel halves each)
+//    and writes their query mask rows; warp 13 loads K and writes the key mask
+//    rows and the key side of the bias offsets; warp 14 loads V;
+//  * warp 15 issues, per key tile, S_A and S_B = Q K^T + Qm Km^T (8 + 1 MMAs
+//    each, N = 128) into one TMEM buffer per query tile and O_A, O_B += P V
+//    (8 MMAs each), in the order PV_A, S_A of the next tile, PV_B, S_B of the
+//    next tile, so that the two query tiles' chains interleave on the
+//    tensor pipe;
+//  * softmax warpgroup X (warps 4X .. 4X+3, thread = query row of tile X)
+//    takes full rows of 128 keys: a first pass over S gives an upper bound of
+//    the tile's row max (max S * scale*log2e + the head's largest bias); the
+//    running max m is raised to it only when it exceeds m by more than 8 (a
+//    factor 256), O (in TMEM) then rescaled, which is rare; the second pass
+//    forms x = S*scale*log2e + bias*log2e, P = exp2(x - m) <= 256 in bf16
+//    over S and the running sum l. The final O / l uses the same m, so the
+//    result is exact in real arithmetic. After the item's last key tile the
+//    warpgroup itself stores O / l (and the log-sum-exp) at the query tokens.
 // Masked keys (other region, land, pad) get -2^100 from the mask MMA and so
 // exactly zero probability. Every wait is bounded, as in the small kernels.
 #include <cuda_bf16.h>
@@ -39,31 +42,45 @@ namespace swin {
 namespace lg {
 namespace {
 
-constexpr int kStages = 2;                  // key/value stages (= S buffers in TMEM)
-constexpr int kQ = 0, kQm = kTileBytes;
-constexpr int kStage0 = kQm + kMaskBytes;   // 36 KB, 1024-aligned
-constexpr int kK = 0, kV = kTileBytes, kKm = 2 * kTileBytes, kRoff = kKm + kMaskBytes;  // inside a stage
-constexpr int kStageBytes = 69 * 1024;      // K, V, Km and int roff[128]
-constexpr int kBcol = kStage0 + kStages * kStageBytes;  // bias column of the current head (bias*log2e)
-constexpr int kMaxBiasRows = 8192;
-constexpr int kXchg = kBcol + kMaxBiasRows * 4;  // float [2 items][2 halves][m, l][128]
-constexpr int kBarOff = kXchg + 2 * 2 * 2 * 128 * 4;
+constexpr int kStages = 2;  // key/value stages
+constexpr int kQA = 0, kQB = kTileBytes, kQmA = 2 * kTileBytes, kQmB = kQmA + kMaskBytes;
+constexpr int kStage0 = kQmB + kMaskBytes;  // 72 KB, 1024-aligned
+constexpr int kK = 0, kV = kTileBytes, kKm = 2 * kTileBytes;  // inside a stage
+constexpr int kStageBytes = 68 * 1024;
+constexpr int kRoff = kStage0 + kStages * kStageBytes;  // int [stage][128]: key side of the bias offsets
+constexpr int kBcol = kRoff + kStages * 512;            // bias column of the current head (bias*log2e)
+constexpr int kMaxBiasRows = 4096;
+constexpr int kBmax = kBcol + kMaxBiasRows * 4;         // float [8]: per-warp maxima of the column
+constexpr int kBarOff = kBmax + 64;
+// per query tile X (0 = A, 1 = B): bSFull + X, bPFull + X, bPVDone + X
 constexpr int bQFull = 0, bQFree = 1, bFull = 2, bEmpty = bFull + kStages, bSFull = bEmpty + kStages,
-              bPFull = bSFull + kStages, bOFull = bPFull + kStages, bTFree = bOFull + 1, bNever = bTFree + 1,
-              bDrain = bNever + 1, bBsync = bDrain + 1, kNumBars = bBsync + 1;
+              bPFull = bSFull + 2, bPVDone = bPFull + 2, bNever = bPVDone + 2, bDrain = bNever + 1,
+              bBsync = bDrain + 1, kNumBars = bBsync + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;  // + alignment slack
-static_assert(kStage0 % 1024 == 0 && kStageBytes % 1024 == 0, "operand tiles need 1024-byte alignment");
-static_assert(kRoff + 512 <= kStageBytes, "stage layout");
+static_assert(kStage0 % 1024 == 0 && kStageBytes % 1024 == 0 && kKm + kMaskBytes <= kStageBytes, "layout");
 static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
 
-// warps 0-7: softmax (warpgroup h = warp / 4 takes key columns [64h, 64h+64));
-// 8-11: epilogue; 12: Q; 13: K (+ key masks, bias offsets); 14: V; 15: MMA
-constexpr int kSoftmaxWarps = 8, kEpilogueWarp0 = 8, kQWarp = 12, kKWarp = 13, kVWarp = 14, kMmaWarp = 15;
+// warps 0-7: softmax (warpgroup X = warp / 4 owns query tile X of the item);
+// 12: Q; 13: K (+ key masks, bias offsets); 14: V; 15: MMA (warps 8-11 idle)
+constexpr int kSoftmaxWarps = 8, kQWarp = 12, kKWarp = 13, kVWarp = 14, kMmaWarp = 15;
 constexpr int kThreads = 16 * 32;
-// TMEM columns: S of key tile t at 128 * (t % 2); O half h at 256 + 128 h
+// TMEM columns: S of query tile X at 128 X; O of query tile X at 256 + 128 X
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past 2^8
+
+// Item = (h, b, window, pair of query tiles 2p and 2p+1), pair fastest.
+__device__ __forceinline__ LItem decode_pair(const Geo &g, int64_t it) {
+  const int nqp = (g.nqt + 1) >> 1;
+  LItem x;
+  x.qt = 2 * (int)(it % nqp);
+  int64_t t = it / nqp;
+  x.omega = (int)(t % g.nwin);
+  t /= g.nwin;
+  x.b = (int)(t % g.batch);
+  x.h = (int)(t / g.batch);
+  return x;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_large_kernel(const FwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -78,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const Geo &g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkt = g.nqt;  // key tiles per window = query tiles per window
+  const int nkt = g.nqt;  // key tiles per window
   int64_t L, R;
   eq4_range(a.items, a.ctas, blockIdx.x, L, R);
   const int64_t count = R - L;
@@ -89,13 +106,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bQFull), 1);
     mbar_init(bar(bQFree), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bFull + s), 2);    // K warp, V warp
-      mbar_init(bar(bEmpty + s), 1);   // MMA commit after PV of the tile
-      mbar_init(bar(bSFull + s), 1);
-      mbar_init(bar(bPFull + s), kSoftmaxWarps);
+      mbar_init(bar(bFull + s), 2);   // K warp, V warp
+      mbar_init(bar(bEmpty + s), 1);  // MMA commit after both PVs of the tile
     }
-    mbar_init(bar(bOFull), 1);
-    mbar_init(bar(bTFree), 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(bSFull + x), 1);
+      mbar_init(bar(bPFull + x), 4);
+      mbar_init(bar(bPVDone + x), 1);
+    }
     mbar_init(bar(bNever), 1);
     mbar_init(bar(bDrain), 1);
     mbar_init(bar(bBsync), kSoftmaxWarps);
@@ -105,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // operand tiles start zeroed (rows past the window stay finite); the
   // constant halves of the mask rows: Qm columns 8-15 = 0, Km columns 8-15 =
   // -2^100
-  for (int z = threadIdx.x; z < kBcol / 16; z += blockDim.x) reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
+  for (int z = threadIdx.x; z < kRoff / 16; z += blockDim.x) reinterpret_cast<uint4 *>(smem)[z] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
   {
     const uint32_t nb2 = (uint32_t)kBf16NegBig | ((uint32_t)kBf16NegBig << 16);
@@ -124,20 +142,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == kQWarp) {
-    // ------------------------------------------------------------ Q tile ---
+    // ----------------------------------------------------------- Q tiles ---
     for (int64_t it = 0; it < count; ++it) {
-      const LItem x = decode(g, L + it);
-      const Quad q = route_quad(g, x.omega, x.qt, lane);
-      bool live[4];
-      quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
+      const LItem x = decode_pair(g, L + it);
+      const bool has_b = x.qt + 1 < g.nqt;
+      const Quad qa = route_quad(g, x.omega, x.qt, lane);
+      const Quad qb = route_quad(g, x.omega, has_b ? x.qt + 1 : x.qt, lane);
+      bool la[4], lb[4];
+      quad_live(qa, a.land, (int64_t)x.b * g.tokens, la);
+      quad_live(qb, a.land, (int64_t)x.b * g.tokens, lb);
       if (it > 0 && !mbar_wait_warp(bar(bQFree), (uint32_t)(it - 1) & 1u, ctl)) break;
-      const int rows = min(128, g.n - x.qt * 128), nq4 = (rows + 3) >> 2;
-      if (lane == 0) mbar_expect_tx(bar(bQFull), (uint32_t)nq4 * 4u * 256u);
+      const int rows_a = min(128, g.n - x.qt * 128), nqa = (rows_a + 3) >> 2;
+      const int rows_b = has_b ? min(128, g.n - (x.qt + 1) * 128) : 0, nqb = (rows_b + 3) >> 2;
+      if (lane == 0) mbar_expect_tx(bar(bQFull), (uint32_t)(nqa + nqb) * 1024u);
       __syncwarp();
-      if (lane < nq4) gather_rows(sbase + kQ, &tmq, q, x.b, g.tokens, x.h, lane, bar(bQFull));
+      if (lane < nqa) gather_rows(sbase + kQA, &tmq, qa, x.b, g.tokens, x.h, lane, bar(bQFull));
+      if (lane < nqb) gather_rows(sbase + kQB, &tmq, qb, x.b, g.tokens, x.h, lane, bar(bQFull));
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4 *>(smem + kQm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], false);
+      for (int j = 0; j < 4; ++j) {
+        *reinterpret_cast<uint4 *>(smem + kQmA + sw32(4 * lane + j, 0)) = mask_chunk(la[j], qa.reg[j], false);
+        *reinterpret_cast<uint4 *>(smem + kQmB + sw32(4 * lane + j, 0)) = mask_chunk(has_b && lb[j], qb.reg[j], false);
+      }
       fence_proxy_async_smem();
       mbar_arrive_warp(bar(bQFull));
     }
@@ -147,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t t = 0;
     for (; t < ntiles; ++t) {
       const int s = (int)(t % kStages);
-      const LItem x = decode(g, L + t / nkt);
+      const LItem x = decode_pair(g, L + t / nkt);
       const int kt = (int)(t % nkt);
       const Quad q = route_quad(g, x.omega, kt, lane);
       bool live[4];
@@ -156,14 +181,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t st = sbase + kStage0 + s * kStageBytes;
       uint8_t *sp = smem + kStage0 + s * kStageBytes;
       const int rows = min(128, g.n - kt * 128), nq4 = (rows + 3) >> 2;
-      if (lane == 0) mbar_expect_tx(bar(bFull + s), (uint32_t)nq4 * 4u * 256u);
+      if (lane == 0) mbar_expect_tx(bar(bFull + s), (uint32_t)nq4 * 1024u);
       __syncwarp();
       if (lane < nq4) gather_rows(st + (kw ? kK : kV), kw ? &tmk : &tmv, q, x.b, g.tokens, x.h, lane, bar(bFull + s));
       if (kw) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           *reinterpret_cast<uint4 *>(sp + kKm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], true);
-        *reinterpret_cast<int4 *>(sp + kRoff + 16 * lane) = make_int4(q.roff[0], q.roff[1], q.roff[2], q.roff[3]);
+        *reinterpret_cast<int4 *>(smem + kRoff + s * 512 + 16 * lane) = make_int4(q.roff[0], q.roff[1], q.roff[2], q.roff[3]);
         fence_proxy_async_smem();
       }
       mbar_arrive_warp(bar(bFull + s));
@@ -175,49 +200,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_warp(bar(bFull + (int)(k % kStages)), (uint32_t)(k / kStages) & 1u, dctl);
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
-    // Order: S(0); then for every key tile t: S(t+1) (if it belongs to the
-    // same item), PV(t), and at an item's last tile PV(t) before S(t+1), so
-    // that the next item's Q tile (loaded once S(t) has freed the buffer)
-    // lands while PV(t) runs.
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0), idesc_pv = idesc_bf16(128, 128, 0, 1);
-      auto issue_s = [&](int64_t t) -> bool {
+      uint32_t ns[2] = {0u, 0u};  // S of query tile X issued so far (the phase of its barriers)
+      // S_X(t) = Q_X K^T + mask into S buffer X
+      auto issue_s = [&](int xq, int64_t t) -> bool {
         const int s = (int)(t % kStages), kt = (int)(t % nkt);
         const int64_t it = t / nkt;
-        if (!mbar_wait(bar(bFull + s), (uint32_t)(t / kStages) & 1u, ctl)) return false;
-        if (kt == 0 && !mbar_wait(bar(bQFull), (uint32_t)it & 1u, ctl)) return false;
-        tc_fence_after();
-        const uint32_t st = sbase + kStage0 + s * kStageBytes, d = tmem + 128u * s;
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(d, kmajor_desc(sbase + kQ, kk), kmajor_desc(st + kK, kk), idesc_s, kk > 0 ? 1u : 0u);
-        mma_ss(d, smem_desc(sbase + kQm, 16, 256, kSwizzle32B), smem_desc(st + kKm, 16, 256, kSwizzle32B), idesc_s, 1);
-        mma_commit(bar(bSFull + s));
-        if (kt == nkt - 1) mma_commit(bar(bQFree));
+        if (xq == 0) {
+          if (!mbar_wait(bar(bFull + s), (uint32_t)(t / kStages) & 1u, ctl)) return false;
+          if (kt == 0 && !mbar_wait(bar(bQFull), (uint32_t)it & 1u, ctl)) return false;
+          tc_fence_after();
+        }
+        const uint32_t st = sbase + kStage0 + s * kStageBytes, d = tmem + 128u * xq;
+        const uint32_t qt = sbase + (xq ? kQB : kQA), qm = sbase + (xq ? kQmB : kQmA);
+        for (int kk = 0; kk < 8; ++kk) mma_ss(d, kmajor_desc(qt, kk), kmajor_desc(st + kK, kk), idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss(d, smem_desc(qm, 16, 256, kSwizzle32B), smem_desc(st + kKm, 16, 256, kSwizzle32B), idesc_s, 1);
+        mma_commit(bar(bSFull + xq));
+        ++ns[xq];
         return true;
       };
-      auto issue_pv = [&](int64_t t) -> bool {
+      // O_X += P_X V once P_X(t) is written
+      auto issue_pv = [&](int xq, int64_t t, uint32_t n) -> bool {
         const int s = (int)(t % kStages), kt = (int)(t % nkt);
-        const int64_t it = t / nkt;
-        if (!mbar_wait(bar(bPFull + s), (uint32_t)(t / kStages) & 1u, ctl)) return false;
-        if (kt == 0 && it > 0 && !mbar_wait(bar(bTFree), (uint32_t)(it - 1) & 1u, ctl)) return false;
+        if (!mbar_wait(bar(bPFull + xq), (n - 1) & 1u, ctl)) return false;
         tc_fence_after();
         const uint32_t st = sbase + kStage0 + s * kStageBytes;
-        for (int h = 0; h < 2; ++h)
-          for (int kk = 0; kk < 4; ++kk) {
-            // keys 64h + 16kk ..: P from TMEM, V rows from the stage (channels = N, MN-major)
-            mma_ts(tmem + kColO + 128u * h, tmem + 128u * s + 64u * h + 16u * kk, nmajor_desc(st + kV, 64 * h + 16 * kk),
-                   idesc_pv, (kt > 0 || kk > 0) ? 1u : 0u);
-          }
-        mma_commit(bar(bEmpty + s));
-        if (kt == nkt - 1) mma_commit(bar(bOFull));
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + kColO + 128u * xq, tmem + 128u * xq + 16u * kk, nmajor_desc(st + kV, 16 * kk), idesc_pv,
+                 (kt > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(bar(bPVDone + xq));
         return true;
       };
-      bool ok = ntiles > 0 && issue_s(0);
+      bool ok = true;
       for (int64_t t = 0; ok && t < ntiles; ++t) {
-        const bool last = (t % nkt) == nkt - 1;
-        if (!last && t + 1 < ntiles) ok = issue_s(t + 1);
-        ok = ok && issue_pv(t);
-        if (ok && last && t + 1 < ntiles) ok = issue_s(t + 1);
+        const int kt = (int)(t % nkt);
+        const LItem x = decode_pair(g, L + t / nkt);
+        const bool has_b = x.qt + 1 < g.nqt;
+        if (kt == 0) {  // the item's first S's (its Q tiles came in after the previous item's last S's)
+          ok = issue_s(0, t) && (!has_b || issue_s(1, t));
+          if (!ok) break;
+          if (kt == nkt - 1) mma_commit(bar(bQFree));
+        }
+        // PV_A(t), S_A(t+1), PV_B(t), S_B(t+1): S of the next tile of the same item
+        // is issued as soon as its query tile's P of this tile has been read
+        const bool next = kt + 1 < nkt;
+        ok = issue_pv(0, t, ns[0]) && (!next || issue_s(0, t + 1));
+        if (ok && has_b) ok = issue_pv(1, t, ns[1]) && (!next || issue_s(1, t + 1));
+        if (!ok) break;
+        if (next && kt + 1 == nkt - 1) mma_commit(bar(bQFree));  // the item's last reads of its Q tiles
+        mma_commit(bar(bEmpty + (int)(t % kStages)));
       }
       mma_commit(bar(bDrain));
       volatile int no_abort = 0;
@@ -225,152 +257,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(bDrain), 0, drain_ctl);
     }
     __syncwarp();
-  } else if (warp >= kEpilogueWarp0) {
-    // ---------------------------------------------------------- epilogue ---
-    const int q4 = warp & 3, i = q4 * 32 + lane;
-    const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
-    const float *xc = reinterpret_cast<const float *>(smem + kXchg);
-    for (int64_t it = 0; it < count; ++it) {
-      const LItem x = decode(g, L + it);
-      const int slot = x.qt * 128 + i;
-      int wc[3];
-      window_coords(g, x.omega, wc);
-      const int src = slot < g.n ? slot_route(g, wc, slot).src : -1;
-      const bool live = src >= 0 && (!a.land || __ldg(a.land + (int64_t)x.b * g.tokens + src) == 0);
-      if (!mbar_wait_warp(bar(bOFull), (uint32_t)it & 1u, ctl)) break;
-      tc_fence_after();
-      const float *xs = xc + (int)(it & 1) * 512;
-      const float m0 = xs[i], l0 = xs[128 + i], m1 = xs[256 + i], l1 = xs[384 + i];
-      const float m = fmaxf(m0, m1);
-      const float a0 = l0 > 0.f ? ex2(m0 - m) : 0.f, a1 = l1 > 0.f ? ex2(m1 - m) : 0.f;
-      const float l = fmaf(a0, l0, a1 * l1);
-      const float inv = live && l > 0.f ? __frcp_rn(l) : 0.f;
-      const float c0 = a0 * inv, c1 = a1 * inv;
-      const bool store = src >= 0 && in_bounds(((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * kHd, kHd,
-                                                (int64_t)g.batch * g.tokens * g.C, a.status);
-      uint4 *dst = store ? reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) +
-                                                     ((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * kHd)
-                         : nullptr;
-#pragma unroll 1
-      for (int c = 0; c < 8; c += 2) {  // 32 channels per TMEM round trip
-        uint32_t o0[16], o1[16], p0[16], p1[16];
-        tmem_ld16(tmem + lane_addr + kColO + 16u * c, o0);
-        tmem_ld16(tmem + lane_addr + kColO + 16u * (c + 1), o1);
-        tmem_ld16(tmem + lane_addr + kColO + 128u + 16u * c, p0);
-        tmem_ld16(tmem + lane_addr + kColO + 128u + 16u * (c + 1), p1);
-        tmem_wait_ld_tied(o0, o1);
-        tmem_tie(p0, p1);
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const uint32_t *h0 = e < 16 ? o0 : o1;
-          const uint32_t *h1 = e < 16 ? p0 : p1;
-          const int o = e & 15;
-          const float v0 = fmaf(__uint_as_float(h1[o]), c1, __uint_as_float(h0[o]) * c0);
-          const float v1 = fmaf(__uint_as_float(h1[o + 1]), c1, __uint_as_float(h0[o + 1]) * c0);
-          w[e >> 1] = pack_bf16(v0, v1);
-        }
-        if (store) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) dst[2 * c + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive_warp(bar(bTFree));
-      if (store && a.lse)
-        a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m + __log2f(l)) * kLn2 : -INFINITY;
-    }
-    tmem_wait_ld();
-  } else {
+  } else if (warp < kSoftmaxWarps) {
     // ----------------------------------------------------------- softmax ---
-    const int grp = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane;
+    const int xq = warp >> 2, q4 = warp & 3, i = q4 * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tS = tmem + lane_addr + 128u * xq, tO = tmem + lane_addr + kColO + 128u * xq;
     float *bcol = reinterpret_cast<float *>(smem + kBcol);
-    float *xc = reinterpret_cast<float *>(smem + kXchg);
+    float *bmx = reinterpret_cast<float *>(smem + kBmax);
     const float cs = a.scale * kLog2e;
-    const float2 cs2 = make_float2(cs, cs);
-    const bool has_bias = a.bias != nullptr;  // the column is read only with a bias (it holds at most kMaxBiasRows)
-    int cur_h = -1, rbase = 0;
-    uint32_t bs_phase = 0;
-    float m_run = -INFINITY, l_run = 0.f;
+    const bool has_bias = a.bias != nullptr;
+    int cur_h = -1, rbase = 0, src = -1;
+    bool live = false, mine = false;
+    float bmax2 = 0.f, m_run = -INFINITY, l_run = 0.f;
+    uint32_t bs_phase = 0, nt = 0;  // key tiles of this warpgroup's query tiles so far (barrier phases)
     bool ok = true;
-    if (a.debug_force_timeout && grp == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
+    auto bsync = [&]() -> bool {
+      mbar_arrive_warp(bar(bBsync));
+      const bool r = mbar_wait_warp(bar(bBsync), bs_phase & 1u, ctl);
+      ++bs_phase;
+      return r;
+    };
+    if (a.debug_force_timeout && xq == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
     for (int64_t t = 0; ok && t < ntiles; ++t) {
-      const int s = (int)(t % kStages), kt = (int)(t % nkt);
-      const int64_t it = t / nkt;
+      const int kt = (int)(t % nkt);
+      const LItem x = decode_pair(g, L + t / nkt);
       if (kt == 0) {
-        const LItem x = decode(g, L + it);
         if (has_bias && x.h != cur_h) {
-          // the head's bias column (bias * log2e) in shared memory; everyone
-          // is done with the previous one first
-          if (cur_h >= 0) {
-            mbar_arrive_warp(bar(bBsync));
-            if (!mbar_wait_warp(bar(bBsync), bs_phase & 1u, ctl)) break;
-            ++bs_phase;
+          // the head's bias column (bias * log2e) and its largest value
+          if (cur_h >= 0 && !bsync()) break;
+          float mx = -INFINITY;
+          for (int r = xq * 128 + i; r < g.T; r += 256) {
+            const float b = __ldg(a.bias + (int64_t)r * g.heads + x.h) * kLog2e;
+            bcol[r] = b;
+            mx = fmaxf(mx, b);
           }
-          for (int r = grp * 128 + i; r < g.T; r += 256) bcol[r] = __ldg(a.bias + (int64_t)r * g.heads + x.h) * kLog2e;
-          mbar_arrive_warp(bar(bBsync));
-          if (!mbar_wait_warp(bar(bBsync), bs_phase & 1u, ctl)) break;
-          ++bs_phase;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          if (lane == 0) bmx[warp] = mx;
+          if (!bsync()) break;
+          bmax2 = bmx[0];
+#pragma unroll
+          for (int w = 1; w < 8; ++w) bmax2 = fmaxf(bmax2, bmx[w]);
           cur_h = x.h;
         }
-        const int wc0[3] = {0, 0, 0};
-        const int slot = x.qt * 128 + i;
-        // a row past the window takes the largest query-side offset, so that
-        // rbase - roff stays inside the column for every key (its output is
-        // never stored)
-        rbase = slot < g.n ? slot_route(g, wc0, slot).rbase : g.T - 1;
+        const int qt = x.qt + xq;
+        mine = qt < g.nqt;  // warpgroup B has no tile in the last pair of an odd tile count
+        const int slot = qt * 128 + i;
+        int wc[3];
+        window_coords(g, x.omega, wc);
+        const SlotRoute r = slot_route(g, wc, mine && slot < g.n ? slot : 0);
+        src = mine && slot < g.n ? r.src : -1;
+        rbase = mine && slot < g.n ? r.rbase : g.T - 1;
+        live = src >= 0 && (!a.land || __ldg(a.land + (int64_t)x.b * g.tokens + src) == 0);
         m_run = -INFINITY;
         l_run = 0.f;
       }
-      const uint32_t tS = tmem + lane_addr + 128u * s + 64u * grp;
-      if (!mbar_wait_warp(bar(bSFull + s), (uint32_t)(t / kStages) & 1u, ctl)) break;
+      if (!mine) continue;
+      if (!mbar_wait_warp(bar(bSFull + xq), nt & 1u, ctl)) break;
       tc_fence_after();
-      uint32_t sv[4][16];
+      const int *roff = reinterpret_cast<const int *>(smem + kRoff + (int)(t % kStages) * 512);
+      // pass 1: an upper bound of the tile's row max from S alone
+      float ms = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[4][16];
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) tmem_ld16(tS + 16u * k4, sv[k4]);
-      const int *roff = reinterpret_cast<const int *>(smem + kStage0 + s * kStageBytes + kRoff) + 64 * grp;
-      tmem_wait_ld_tied(sv[0], sv[1]);
-      tmem_wait_ld_tied(sv[2], sv[3]);
-      // x = S*cs + bias2, tile max
-      float mp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        for (int k4 = 0; k4 < 4; ++k4) tmem_ld16(tS + 64u * c + 16u * k4, sv[k4]);
+        tmem_wait_ld_tied(sv[0], sv[1]);
+        tmem_wait_ld_tied(sv[2], sv[3]);
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
+        for (int k4 = 0; k4 < 4; ++k4)
 #pragma unroll
-        for (int e4 = 0; e4 < 16; e4 += 4) {
-          float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f;
-          if (has_bias) {
-            const int4 r4 = *reinterpret_cast<const int4 *>(roff + 16 * k4 + e4);
-            b0 = bcol[rbase - r4.x];
-            b1 = bcol[rbase - r4.y];
-            b2 = bcol[rbase - r4.z];
-            b3 = bcol[rbase - r4.w];
-          }
-          const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e4]), __uint_as_float(sv[k4][e4 + 1])), cs2,
-                                       make_float2(b0, b1));
-          const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e4 + 2]), __uint_as_float(sv[k4][e4 + 3])),
-                                       cs2, make_float2(b2, b3));
-          sv[k4][e4] = __float_as_uint(x0.x);
-          sv[k4][e4 + 1] = __float_as_uint(x0.y);
-          sv[k4][e4 + 2] = __float_as_uint(x1.x);
-          sv[k4][e4 + 3] = __float_as_uint(x1.y);
-          mp[e4 >> 2] = max3(mp[e4 >> 2], max3(x0.x, x0.y, x1.x), x1.y);
-        }
+          for (int e = 0; e < 16; e += 2)
+            ms = max3(ms, __uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1]));
       }
-      const float mt = fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3]));
-      // a tile whose keys are all masked for this row (about -2^100 after the
-      // mask step) adds nothing; otherwise raise the running max only past 2^8
-      const bool any = mt > -1e29f;
+      // keys all masked for this row (about -2^100 after the mask step): no contribution
+      const bool any = ms > -1e29f;
+      const float mt = ms * cs + bmax2;
       float m_new = m_run;
       if (any && (l_run == 0.f || mt > m_run + kRescaleLog2)) m_new = mt;
       const bool rescale = any && l_run > 0.f && m_new != m_run;
       if (__any_sync(0xffffffffu, rescale)) {
-        // O half grp of this row is scaled by exp2(m_run - m_new) once the PV of
-        // the previous tile (same item) has completed
-        if (!mbar_wait_warp(bar(bEmpty + (int)((t - 1) % kStages)), (uint32_t)((t - 1) / kStages) & 1u, ctl)) break;
+        // O of this row is scaled by exp2(m_run - m_new) once the PV of the
+        // previous tile has completed
+        if (!mbar_wait_warp(bar(bPVDone + xq), (nt - 1) & 1u, ctl)) break;
         tc_fence_after();
         const float f = rescale ? ex2(m_run - m_new) : 1.f;
-        const uint32_t tO = tmem + lane_addr + kColO + 128u * grp;
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           uint32_t ov[16];
@@ -384,31 +356,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run *= f;
       }
       m_run = m_new;
+      // pass 2: x = S*cs + bias2, P = exp2(x - m) over S, row sum
       const float msub = any ? m_run : 0.f;
-      const float2 negm = make_float2(-msub, -msub);
-      float2 sp2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+      float2 sp2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[4][16];
 #pragma unroll
-      for (int k4 = 0; k4 < 4; ++k4) {
-        uint32_t pv[8];
+        for (int k4 = 0; k4 < 4; ++k4) tmem_ld16(tS + 64u * c + 16u * k4, sv[k4]);
+        tmem_wait_ld_tied(sv[0], sv[1]);
+        tmem_wait_ld_tied(sv[2], sv[3]);
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          const float2 xs2 = __fadd2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), negm);
-          const float2 p = any ? make_float2(ex2(xs2.x), ex2(xs2.y)) : make_float2(0.f, 0.f);
-          sp2[(e >> 1) & 3] = __fadd2_rn(sp2[(e >> 1) & 3], p);
-          pv[e >> 1] = pack_bf16(p.x, p.y);
+        for (int k4 = 0; k4 < 4; ++k4) {
+          uint32_t pv[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            float b[4] = {0.f, 0.f, 0.f, 0.f};
+            if (has_bias) {
+              const int4 r4 = *reinterpret_cast<const int4 *>(roff + 64 * c + 16 * k4 + e);
+              b[0] = bcol[rbase - r4.x];
+              b[1] = bcol[rbase - r4.y];
+              b[2] = bcol[rbase - r4.z];
+              b[3] = bcol[rbase - r4.w];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; u += 2) {
+              const float x0 = fmaf(__uint_as_float(sv[k4][e + u]), cs, b[u]) - msub;
+              const float x1 = fmaf(__uint_as_float(sv[k4][e + u + 1]), cs, b[u + 1]) - msub;
+              const float2 p = any ? make_float2(ex2(x0), ex2(x1)) : make_float2(0.f, 0.f);
+              sp2[u >> 1] = __fadd2_rn(sp2[u >> 1], p);
+              pv[(e + u) >> 1] = pack_bf16(p.x, p.y);
+            }
+          }
+          tmem_st8(tS + 64u * c + 16u * k4, pv);
         }
-        tmem_st8(tS + 16u * k4, pv);
       }
-      const float2 sum2 = __fadd2_rn(__fadd2_rn(sp2[0], sp2[1]), __fadd2_rn(sp2[2], sp2[3]));
+      const float2 sum2 = __fadd2_rn(sp2[0], sp2[1]);
       l_run += sum2.x + sum2.y;
-      if (kt == nkt - 1) {
-        float *xs = xc + (int)(it & 1) * 512 + grp * 256;
-        xs[i] = m_run;
-        xs[128 + i] = l_run;
-      }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive_warp(bar(bPFull + s));
+      mbar_arrive_warp(bar(bPFull + xq));
+      ++nt;
+      if (kt == nkt - 1) {
+        // epilogue of the item: O / l at the query tokens, the log-sum-exp
+        if (!mbar_wait_warp(bar(bPVDone + xq), (nt - 1) & 1u, ctl)) break;
+        tc_fence_after();
+        const float inv = live && l_run > 0.f ? __frcp_rn(l_run) : 0.f;
+        const bool store = src >= 0 && in_bounds(((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * kHd, kHd,
+                                                  (int64_t)g.batch * g.tokens * g.C, a.status);
+        uint4 *dst = store ? reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.o) +
+                                                       ((int64_t)x.b * g.tokens + src) * g.C + (int64_t)x.h * kHd)
+                           : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < 8; c += 2) {
+          uint32_t o0[16], o1[16];
+          tmem_ld16(tO + 16u * c, o0);
+          tmem_ld16(tO + 16u * (c + 1), o1);
+          tmem_wait_ld_tied(o0, o1);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            w[e >> 1] = pack_bf16(__uint_as_float(o0[e]) * inv, __uint_as_float(o0[e + 1]) * inv);
+            w[8 + (e >> 1)] = pack_bf16(__uint_as_float(o1[e]) * inv, __uint_as_float(o1[e + 1]) * inv);
+          }
+          if (store) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[2 * c + q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          }
+        }
+        if (store && a.lse)
+          a.lse[((int64_t)x.b * g.heads + x.h) * g.tokens + src] = live ? (m_run + __log2f(l_run)) * kLn2 : -INFINITY;
+      }
     }
     tmem_wait_st();
     tmem_wait_ld();
@@ -427,6 +445,7 @@ bool large_supported(const Geo &g, int dtype) {
   return dtype == SWIN_BF16 && g.hd == lg::kHd && (int64_t)g.batch * g.tokens <= INT32_MAX;
 }
 int large_max_bias_rows() { return lg::kMaxBiasRows; }
+int64_t large_fwd_items(const Geo &g) { return (int64_t)g.heads * g.batch * g.nwin * ((g.nqt + 1) / 2); }
 
 int launch_fwd_large(const FwdArgs &a, void *stream) {
   if (a.bias && a.g.T > lg::kMaxBiasRows) return SWIN_ERR_UNSUPPORTED;

@@ -15,6 +15,7 @@ int launch_bwd_tc(const BwdArgs &a, void *stream);
 // Kernels for head_dim 128 and windows of any size (KV-tiled online softmax).
 bool large_supported(const Geo &g, int dtype);
 int large_max_bias_rows();
+int64_t large_fwd_items(const Geo &g);  // (head, image, window, pair of query tiles)
 int launch_fwd_large(const FwdArgs &a, void *stream);
 int large_bwd_max_bias_rows();
 int launch_bwd_large(const BwdArgs &a, void *stream);
