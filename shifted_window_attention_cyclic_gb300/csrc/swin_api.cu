@@ -149,6 +149,20 @@ Geo make_geo(const swin_attn_desc *d) {
   g.n = g.w[0] * g.w[1] * g.w[2];
   g.nwin = g.nw[0] * g.nw[1] * g.nw[2];
   g.nqt = (g.n + 127) / 128;
+  // a 128-slot tile is a box of the grid when it is made of whole rows of the
+  // window's last dim: w2 x tb1 rows (tb1 dividing w1), or w2 x w1 x tb0 (tb0
+  // dividing w0)
+  g.tb1 = g.tb0 = 0;
+  if (128 % g.w[2] == 0) {
+    const int r = 128 / g.w[2];
+    if (r <= g.w[1] && g.w[1] % r == 0) {
+      g.tb1 = r;
+      g.tb0 = 1;
+    } else if (r % g.w[1] == 0 && r / g.w[1] <= g.w[0] && g.w[0] % (r / g.w[1]) == 0) {
+      g.tb1 = g.w[1];
+      g.tb0 = r / g.w[1];
+    }
+  }
   g.wstep = window_step(g.nwin);
   g.tokens = g.G[0] * g.G[1] * g.G[2];
   g.rstride[2] = 1;

@@ -31,6 +31,8 @@ struct Geo {
   int offb, rows;
   int istep;        // (pack * wstep) mod nwin: window step from one item to the next
   int nqt;         // query (= key) tiles of 128 slots per window (head_dim-128 kernels)
+  int tb1, tb0;    // extents in dims 1 and 0 of a 128-slot tile that is a grid box (w2 x tb1 x tb0
+                   // = 128 slots of whole window rows); 0 when the window's tiles are never boxes
   int tokens;      // tokens per image
   int T;           // bias rows
   int rstride[3];  // prod_{e>d} (2 w_e - 1)

@@ -102,6 +102,46 @@ __device__ __forceinline__ void gather_rows(uint32_t dst_tile, const CUtensorMap
   tma_gather4(dst_tile + kHalfBytes + 512u * lane, rows, h * kHd + 64, r[0], r[1], r[2], r[3], bar);
 }
 
+// The two TMA views of one [B, G0, G1, G2, C] bf16 tensor: 128-slot tile
+// boxes (64 channels x w2 x tb1 x tb0) and the [B*T, C] row view for gather4.
+struct TileMaps {
+  CUtensorMap box, rows;
+};
+
+// Grid coordinates of the first slot of tile `tile` of window omega when the
+// tile is a box of the grid (whole window rows that neither wrap nor pad).
+__device__ __forceinline__ bool tile_box(const Geo &g, int omega, int tile, int (&c)[3]) {
+  if (g.tb1 == 0 || (tile + 1) * 128 > g.n) return false;
+  int wc[3];
+  window_coords(g, omega, wc);
+  const int s0 = tile * 128;
+  const int o[3] = {s0 / (g.w[1] * g.w[2]), (s0 / g.w[2]) % g.w[1], 0};
+  const int ext[3] = {g.tb0, g.tb1, g.w[2]};
+  bool box = true;
+#pragma unroll
+  for (int d = 0; d < 3; ++d) {
+    c[d] = wc[d] * g.w[d] + g.s[d] + o[d];
+    box = box && c[d] + ext[d] <= g.G[d];
+  }
+  return box;
+}
+
+// One 128-slot tile of head h into `dst` (two 64-channel halves): two box
+// copies from lane 0 when the tile is a box, else the lanes' row gathers.
+// Returns nothing; completion is counted on `bar` (32 KB either way for a
+// full tile).
+__device__ __forceinline__ void load_tile(uint32_t dst, const TileMaps *m, bool box, const int (&c)[3], const Quad &q,
+                                          int b, int tokens, int h, int lane, int nq4, uint32_t bar) {
+  if (box) {
+    if (lane == 0) {
+      tma_load_5d(dst, &m->box, h * kHd, c[2], c[1], c[0], b, bar);
+      tma_load_5d(dst + kHalfBytes, &m->box, h * kHd + 64, c[2], c[1], c[0], b, bar);
+    }
+  } else if (lane < nq4) {
+    gather_rows(dst, &m->rows, q, b, tokens, h, lane, bar);
+  }
+}
+
 // K-major 128B-swizzled descriptor of k-step kk (16 channels) of a 128-row
 // tile held as two 64-channel halves.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
@@ -141,6 +181,29 @@ inline bool rows128_map(CUtensorMap *m, const void *base, const Geo &g) {
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Box view of the same tensor: (64 channels, w2, tb1, tb0, 1) per copy.
+inline bool box128_map(CUtensorMap *m, const void *base, const Geo &g) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  if (g.tb1 == 0) {  // tiles are never boxes: a valid map of the row view stands in (never used)
+    return rows128_map(m, base, g);
+  }
+  const cuuint64_t e = 2;
+  cuuint64_t dims[5] = {(cuuint64_t)g.C, (cuuint64_t)g.G[2], (cuuint64_t)g.G[1], (cuuint64_t)g.G[0],
+                        (cuuint64_t)g.batch};
+  cuuint64_t strides[4] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e,
+                           dims[0] * dims[1] * dims[2] * dims[3] * e};
+  cuuint32_t box[5] = {64u, (cuuint32_t)g.w[2], (cuuint32_t)g.tb1, (cuuint32_t)g.tb0, 1u};
+  cuuint32_t es[5] = {1u, 1u, 1u, 1u, 1u};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline bool tile_maps(TileMaps *t, const void *base, const Geo &g) {
+  return box128_map(&t->box, base, g) && rows128_map(&t->rows, base, g);
 }
 
 }  // namespace lg

@@ -52,8 +52,8 @@ constexpr int kQWarp = 12, kKWarp = 13, kVWarp = 14;
 constexpr uint32_t kColS = 0, kColdP = 128, kColdQ = 256;
 
 __global__ void __launch_bounds__(kThreads, 1)
-    bwdq_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
+    bwdq_kernel(const BwdArgs a, const __grid_constant__ TileMaps tmq, const __grid_constant__ TileMaps tmk,
+                const __grid_constant__ TileMaps tmv, const __grid_constant__ TileMaps tmdo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -115,10 +115,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = min(128, g.n - x.qt * 128), nq4 = (rows + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(bQFull), (uint32_t)nq4 * 2u * 1024u);
       __syncwarp();
-      if (lane < nq4) {
-        gather_rows(sbase + kQ, &tmq, q, x.b, g.tokens, x.h, lane, bar(bQFull));
-        gather_rows(sbase + kdO, &tmdo, q, x.b, g.tokens, x.h, lane, bar(bQFull));
-      }
+      int c[3];
+      const bool box = tile_box(g, x.omega, x.qt, c);
+      load_tile(sbase + kQ, &tmq, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bQFull));
+      load_tile(sbase + kdO, &tmdo, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bQFull));
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         *reinterpret_cast<uint4 *>(smem + kQm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], false);
@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = min(128, g.n - kt * 128), nq4 = (rows + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(bFull + s), (uint32_t)nq4 * 1024u);
       __syncwarp();
-      if (lane < nq4) gather_rows(st + (kw ? kK : kV), kw ? &tmk : &tmv, q, x.b, g.tokens, x.h, lane, bar(bFull + s));
+      int c[3];
+      const bool box = tile_box(g, x.omega, kt, c);
+      load_tile(st + (kw ? kK : kV), kw ? &tmk : &tmv, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bFull + s));
       if (kw) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -368,8 +370,8 @@ constexpr int kKVWarp = 12, kQWarp = 13, kdOWarp = 14;
 constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 384;
 
 __global__ void __launch_bounds__(kThreads, 1)
-    bwdkv_kernel(const BwdArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                 const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmdo) {
+    bwdkv_kernel(const BwdArgs a, const __grid_constant__ TileMaps tmq, const __grid_constant__ TileMaps tmk,
+                 const __grid_constant__ TileMaps tmv, const __grid_constant__ TileMaps tmdo) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -428,10 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = min(128, g.n - x.qt * 128), nq4 = (rows + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(bKVFull), (uint32_t)nq4 * 2u * 1024u);
       __syncwarp();
-      if (lane < nq4) {
-        gather_rows(sbase + kK, &tmk, q, x.b, g.tokens, x.h, lane, bar(bKVFull));
-        gather_rows(sbase + kV, &tmv, q, x.b, g.tokens, x.h, lane, bar(bKVFull));
-      }
+      int c[3];
+      const bool box = tile_box(g, x.omega, x.qt, c);
+      load_tile(sbase + kK, &tmk, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bKVFull));
+      load_tile(sbase + kV, &tmv, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bKVFull));
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         *reinterpret_cast<uint4 *>(smem + kKm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], true);
@@ -463,7 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = min(128, g.n - qt * 128), nq4 = (rows + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(bFull), (uint32_t)nq4 * 1024u);
       __syncwarp();
-      if (lane < nq4) gather_rows(sbase + kStage + (qw ? kQ : kdO), qw ? &tmq : &tmdo, q, x.b, g.tokens, x.h, lane, bar(bFull));
+      int c[3];
+      const bool box = tile_box(g, x.omega, qt, c);
+      load_tile(sbase + kStage + (qw ? kQ : kdO), qw ? &tmq : &tmdo, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bFull));
       if (qw) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -677,9 +681,9 @@ int large_bwd_max_bias_rows() { return lg::bq::kMaxBiasRows; }
 
 int launch_bwd_large(const BwdArgs &a, void *stream) {
   if ((a.bias && a.g.T > lg::bq::kMaxBiasRows) || (a.ws && a.g.T > lg::bkv::kMaxBiasRows)) return SWIN_ERR_UNSUPPORTED;
-  CUtensorMap mq, mk, mv, mdo;
-  if (!lg::rows128_map(&mq, a.q, a.g) || !lg::rows128_map(&mk, a.k, a.g) || !lg::rows128_map(&mv, a.v, a.g) ||
-      !lg::rows128_map(&mdo, a.dout, a.g))
+  lg::TileMaps mq, mk, mv, mdo;
+  if (!lg::tile_maps(&mq, a.q, a.g) || !lg::tile_maps(&mk, a.k, a.g) || !lg::tile_maps(&mv, a.v, a.g) ||
+      !lg::tile_maps(&mdo, a.dout, a.g))
     return SWIN_ERR_CUDA;
   if (cudaFuncSetAttribute(lg::bq::bwdq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lg::bq::kSmemBytes) !=
           cudaSuccess ||
