@@ -62,8 +62,10 @@ static_assert(kStage0 % 1024 == 0 && kStageBytes % 1024 == 0 && kKm + kMaskBytes
 static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
 
 // warps 0-7: softmax (warpgroup X = warp / 4 owns query tile X of the item);
-// 12: Q; 13: K (+ key masks, bias offsets); 14: V; 15: MMA (warps 8-11 idle)
-constexpr int kSoftmaxWarps = 8, kQWarp = 12, kKWarp = 13, kVWarp = 14, kMmaWarp = 15;
+// 12: Q; 13 and 8: K (channels 0-63, + key masks and bias offsets; 64-127);
+// 14 and 9: V (the same halves); 15: MMA. Four warps issue the key/value row
+// gathers: one warp's gather issue alone took longer than the item's MMAs.
+constexpr int kSoftmaxWarps = 8, kQWarp = 12, kKWarp = 13, kVWarp = 14, kKWarp2 = 8, kVWarp2 = 9, kMmaWarp = 15;
 constexpr int kThreads = 16 * 32;
 // TMEM columns: S of query tile X at 128 X; O of query tile X at 256 + 128 X
 constexpr uint32_t kColO = 256;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bQFull), 1);
     mbar_init(bar(bQFree), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bFull + s), 2);   // K warp, V warp
+      mbar_init(bar(bFull + s), 4);   // the four key/value gather warps
       mbar_init(bar(bEmpty + s), 1);  // MMA commit after both PVs of the tile
     }
     for (int x = 0; x < 2; ++x) {
@@ -168,26 +170,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive_warp(bar(bQFull));
     }
-  } else if (warp == kKWarp || warp == kVWarp) {
+  } else if (warp == kKWarp || warp == kVWarp || warp == kKWarp2 || warp == kVWarp2) {
     // -------------------------------------------------------- K, V tiles ---
-    const bool kw = warp == kKWarp;
+    const bool kw = warp == kKWarp || warp == kKWarp2;
+    const int half = (warp == kKWarp2 || warp == kVWarp2) ? 1 : 0;  // channel half this warp loads
     int64_t t = 0;
     for (; t < ntiles; ++t) {
       const int s = (int)(t % kStages);
       const LItem x = decode_pair(g, L + t / nkt);
       const int kt = (int)(t % nkt);
       const Quad q = route_quad(g, x.omega, kt, lane);
+      const bool meta = warp == kKWarp;  // writes the key mask rows and bias offsets
       bool live[4];
-      if (kw) quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
+      if (meta) quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
       if (t >= kStages && !mbar_wait_warp(bar(bEmpty + s), (uint32_t)((t / kStages) - 1) & 1u, ctl)) break;
       const uint32_t st = sbase + kStage0 + s * kStageBytes;
       uint8_t *sp = smem + kStage0 + s * kStageBytes;
       const int rows = min(128, g.n - kt * 128), nq4 = (rows + 3) >> 2;
-      if (lane == 0) mbar_expect_tx(bar(bFull + s), (uint32_t)nq4 * 1024u);
+      if (lane == 0) mbar_expect_tx(bar(bFull + s), (uint32_t)nq4 * 512u);
       __syncwarp();
-      const int cz[3] = {0, 0, 0};
-      load_tile(st + (kw ? kK : kV), kw ? &tmk : &tmv, false, cz, q, x.b, g.tokens, x.h, lane, nq4, bar(bFull + s));
-      if (kw) {
+      if (lane < nq4) {
+        // rows 4*lane .. 4*lane+3 of this warp's channel half (pads read token 0 of the image)
+        const CUtensorMap *m = kw ? &tmk.rows : &tmv.rows;
+        const int r0 = x.b * g.tokens;
+        tma_gather4(st + (kw ? kK : kV) + half * kHalfBytes + 512u * lane, m, x.h * kHd + 64 * half,
+                    r0 + max(q.src[0], 0), r0 + max(q.src[1], 0), r0 + max(q.src[2], 0), r0 + max(q.src[3], 0),
+                    bar(bFull + s));
+      }
+      if (meta) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           *reinterpret_cast<uint4 *>(sp + kKm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], true);
@@ -369,27 +379,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k4 = 0; k4 < 4; ++k4) tmem_ld16(tS + 64u * c + 16u * k4, sv[k4]);
         tmem_wait_ld_tied(sv[0], sv[1]);
         tmem_wait_ld_tied(sv[2], sv[3]);
+        // x - m = S*cs + (bias2 - m) for the 64 keys, in place: the shared-memory
+        // bias reads run back to back (no TMEM store between them)
+        const float2 cs2 = make_float2(cs, cs);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+          for (int e = 0; e < 16; e += 4) {
+            float b[4] = {-msub, -msub, -msub, -msub};
+            if (has_bias) {
+              const int4 r4 = *reinterpret_cast<const int4 *>(roff + 64 * c + 16 * k4 + e);
+              b[0] = bcol[rbase - r4.x] - msub;
+              b[1] = bcol[rbase - r4.y] - msub;
+              b[2] = bcol[rbase - r4.z] - msub;
+              b[3] = bcol[rbase - r4.w] - msub;
+            }
+            const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), cs2,
+                                         make_float2(b[0], b[1]));
+            const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e + 2]), __uint_as_float(sv[k4][e + 3])),
+                                         cs2, make_float2(b[2], b[3]));
+            sv[k4][e] = __float_as_uint(x0.x);
+            sv[k4][e + 1] = __float_as_uint(x0.y);
+            sv[k4][e + 2] = __float_as_uint(x1.x);
+            sv[k4][e + 3] = __float_as_uint(x1.y);
+          }
+        }
+        // P = exp2(x - m) in bf16 over S, row sum
 #pragma unroll
         for (int k4 = 0; k4 < 4; ++k4) {
           uint32_t pv[8];
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            float b[4] = {0.f, 0.f, 0.f, 0.f};
-            if (has_bias) {
-              const int4 r4 = *reinterpret_cast<const int4 *>(roff + 64 * c + 16 * k4 + e);
-              b[0] = bcol[rbase - r4.x];
-              b[1] = bcol[rbase - r4.y];
-              b[2] = bcol[rbase - r4.z];
-              b[3] = bcol[rbase - r4.w];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; u += 2) {
-              const float x0 = fmaf(__uint_as_float(sv[k4][e + u]), cs, b[u]) - msub;
-              const float x1 = fmaf(__uint_as_float(sv[k4][e + u + 1]), cs, b[u + 1]) - msub;
-              const float2 p = any ? make_float2(ex2(x0), ex2(x1)) : make_float2(0.f, 0.f);
-              sp2[u >> 1] = __fadd2_rn(sp2[u >> 1], p);
-              pv[(e + u) >> 1] = pack_bf16(p.x, p.y);
-            }
+          for (int e = 0; e < 16; e += 2) {
+            const float2 p = any ? make_float2(ex2(__uint_as_float(sv[k4][e])), ex2(__uint_as_float(sv[k4][e + 1])))
+                                 : make_float2(0.f, 0.f);
+            sp2[(e >> 1) & 1] = __fadd2_rn(sp2[(e >> 1) & 1], p);
+            pv[e >> 1] = pack_bf16(p.x, p.y);
           }
           tmem_st8(tS + 64u * c + 16u * k4, pv);
         }
