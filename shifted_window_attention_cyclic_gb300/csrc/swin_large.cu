@@ -201,7 +201,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           *reinterpret_cast<uint4 *>(sp + kKm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], true);
-        *reinterpret_cast<int4 *>(smem + kRoff + s * 512 + 16 * lane) = make_int4(q.roff[0], q.roff[1], q.roff[2], q.roff[3]);
+        // key side of the bias offsets as negated byte offsets into the column.
+        // A 16-key chunk (lanes 4c .. 4c+3) whose keys are all slots of the
+        // window with offsets stepping by one is marked regular by bit 0 of its
+        // first entry: the softmax then reads its 16 bias values at fixed
+        // distances from one address.
+        const bool lane_reg = kt * 128 + 4 * lane + 3 < g.n && q.roff[1] == q.roff[0] + 1 &&
+                              q.roff[2] == q.roff[0] + 2 && q.roff[3] == q.roff[0] + 3;
+        const int lead = __shfl_sync(0xffffffffu, q.roff[0], lane & ~3);
+        const uint32_t bal = __ballot_sync(0xffffffffu, lane_reg && q.roff[0] == lead + 4 * (lane & 3));
+        const int flag = (lane & 3) == 0 && ((bal >> (lane & ~3)) & 0xFu) == 0xFu ? 1 : 0;
+        *reinterpret_cast<int4 *>(smem + kRoff + s * 512 + 16 * lane) =
+            make_int4((-4 * q.roff[0]) | flag, -4 * q.roff[1], -4 * q.roff[2], -4 * q.roff[3]);
         fence_proxy_async_smem();
       }
       mbar_arrive_warp(bar(bFull + s));
@@ -276,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_addr + 128u * xq, tO = tmem + lane_addr + kColO + 128u * xq;
     float *bcol = reinterpret_cast<float *>(smem + kBcol);
+    const uint32_t bcol_u32 = sbase + kBcol;
     float *bmx = reinterpret_cast<float *>(smem + kBmax);
     const float cs = a.scale * kLog2e;
     const bool has_bias = a.bias != nullptr;
@@ -381,27 +393,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld_tied(sv[2], sv[3]);
         // x - m = S*cs + (bias2 - m) for the 64 keys, in place: the shared-memory
         // bias reads run back to back (no TMEM store between them)
-        const float2 cs2 = make_float2(cs, cs);
+        const float2 cs2 = make_float2(cs, cs), nm2 = make_float2(-msub, -msub);
+        if (has_bias) {
+          const uint32_t brow = bcol_u32 + 4u * (uint32_t)rbase;  // this row's end of the column
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int v = roff[64 * c + 16 * k4];  // the same word for every lane
+            if (v & 1) {
+              // regular chunk: key e's value sits 4e bytes below the first key's
+              float bv[16];
+              lds_f32_desc16(brow + (uint32_t)(v - 1) - 60u, bv);
 #pragma unroll
-          for (int e = 0; e < 16; e += 4) {
-            float b[4] = {-msub, -msub, -msub, -msub};
-            if (has_bias) {
-              const int4 r4 = *reinterpret_cast<const int4 *>(roff + 64 * c + 16 * k4 + e);
-              b[0] = bcol[rbase - r4.x] - msub;
-              b[1] = bcol[rbase - r4.y] - msub;
-              b[2] = bcol[rbase - r4.z] - msub;
-              b[3] = bcol[rbase - r4.w] - msub;
+              for (int e = 0; e < 16; e += 2) {
+                const float2 x = __fadd2_rn(
+                    __ffma2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), cs2,
+                               make_float2(bv[e], bv[e + 1])),
+                    nm2);
+                sv[k4][e] = __float_as_uint(x.x);
+                sv[k4][e + 1] = __float_as_uint(x.y);
+              }
+              continue;
             }
-            const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), cs2,
-                                         make_float2(b[0], b[1]));
-            const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(sv[k4][e + 2]), __uint_as_float(sv[k4][e + 3])),
-                                         cs2, make_float2(b[2], b[3]));
-            sv[k4][e] = __float_as_uint(x0.x);
-            sv[k4][e + 1] = __float_as_uint(x0.y);
-            sv[k4][e + 2] = __float_as_uint(x1.x);
-            sv[k4][e + 3] = __float_as_uint(x1.y);
+#pragma unroll
+            for (int e = 0; e < 16; e += 4) {
+              const int4 r4 = *reinterpret_cast<const int4 *>(roff + 64 * c + 16 * k4 + e);
+              const float2 b01 = make_float2(lds_f32(brow + r4.x), lds_f32(brow + r4.y));
+              const float2 b23 = make_float2(lds_f32(brow + r4.z), lds_f32(brow + r4.w));
+              const float2 x0 = __fadd2_rn(
+                  __ffma2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), cs2, b01), nm2);
+              const float2 x1 = __fadd2_rn(
+                  __ffma2_rn(make_float2(__uint_as_float(sv[k4][e + 2]), __uint_as_float(sv[k4][e + 3])), cs2, b23),
+                  nm2);
+              sv[k4][e] = __float_as_uint(x0.x);
+              sv[k4][e + 1] = __float_as_uint(x0.y);
+              sv[k4][e + 2] = __float_as_uint(x1.x);
+              sv[k4][e + 3] = __float_as_uint(x1.y);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+              const float2 x =
+                  __ffma2_rn(make_float2(__uint_as_float(sv[k4][e]), __uint_as_float(sv[k4][e + 1])), cs2, nm2);
+              sv[k4][e] = __float_as_uint(x.x);
+              sv[k4][e + 1] = __float_as_uint(x.y);
+            }
           }
         }
         // P = exp2(x - m) in bf16 over S, row sum

@@ -11,6 +11,33 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// One float from a shared-memory address (32-bit, no generic-pointer arithmetic).
+// Not volatile and no memory clobber, so the compiler may batch these loads: the
+// caller must derive `addr` from a value read after the barrier that orders the
+// writes of the location.
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// Sixteen floats at descending addresses: out[e] = *(base + 60 - 4e), one
+// base register with immediate offsets (same ordering contract as lds_f32).
+__device__ __forceinline__ void lds_f32_desc16(uint32_t base, float (&out)[16]) {
+  asm("ld.shared.f32 %0, [%16+60];\n\tld.shared.f32 %1, [%16+56];\n\t"
+      "ld.shared.f32 %2, [%16+52];\n\tld.shared.f32 %3, [%16+48];\n\t"
+      "ld.shared.f32 %4, [%16+44];\n\tld.shared.f32 %5, [%16+40];\n\t"
+      "ld.shared.f32 %6, [%16+36];\n\tld.shared.f32 %7, [%16+32];\n\t"
+      "ld.shared.f32 %8, [%16+28];\n\tld.shared.f32 %9, [%16+24];\n\t"
+      "ld.shared.f32 %10, [%16+20];\n\tld.shared.f32 %11, [%16+16];\n\t"
+      "ld.shared.f32 %12, [%16+12];\n\tld.shared.f32 %13, [%16+8];\n\t"
+      "ld.shared.f32 %14, [%16+4];\n\tld.shared.f32 %15, [%16];"
+      : "=f"(out[0]), "=f"(out[1]), "=f"(out[2]), "=f"(out[3]), "=f"(out[4]), "=f"(out[5]), "=f"(out[6]),
+        "=f"(out[7]), "=f"(out[8]), "=f"(out[9]), "=f"(out[10]), "=f"(out[11]), "=f"(out[12]), "=f"(out[13]),
+        "=f"(out[14]), "=f"(out[15])
+      : "r"(base));
+}
+
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
