@@ -47,13 +47,21 @@ constexpr int kQA = 0, kQB = kTileBytes, kQmA = 2 * kTileBytes, kQmB = kQmA + kM
 constexpr int kStage0 = kQmB + kMaskBytes;  // 72 KB, 1024-aligned
 constexpr int kK = 0, kV = kTileBytes, kKm = 2 * kTileBytes;  // inside a stage
 constexpr int kStageBytes = 68 * 1024;
-constexpr int kRoff = kStage0 + kStages * kStageBytes;  // int [stage][128]: key side of the bias offsets
-constexpr int kBcol = kRoff + kStages * 512;            // bias column of the current head (bias*log2e)
+// key side of the bias offsets, int16 [kRoffSlots][128], a ring written with
+// the key tiles: slot t mod 4 is rewritten with key tile t + 4, which cannot
+// start before the softmax of tile t has finished (see the barriers below)
+constexpr int kRoffSlots = 4;
+constexpr int kRoff = kStage0 + kStages * kStageBytes;
+constexpr int kBcol = kRoff + kRoffSlots * 256;  // bias column of the current head (bias*log2e)
 constexpr int kMaxBiasRows = 4096;
 constexpr int kBmax = kBcol + kMaxBiasRows * 4;         // float [8]: per-warp maxima of the column
 constexpr int kBarOff = kBmax + 64;
 // per query tile X (0 = A, 1 = B): bSFull + X, bPFull + X, bPVDone + X
-constexpr int bQFull = 0, bQFree = 1, bFull = 2, bEmpty = bFull + kStages, bSFull = bEmpty + kStages,
+// stage s: bKFull/bKEmpty for its key tile (+ key mask rows), bVFull/bVEmpty
+// for its value tile; the key half is released after the last S of the tile,
+// the value half after the last PV
+constexpr int bQFull = 0, bQFree = 1, bKFull = 2, bVFull = bKFull + kStages, bKEmpty = bVFull + kStages,
+              bVEmpty = bKEmpty + kStages, bSFull = bVEmpty + kStages,
               bPFull = bSFull + 2, bPVDone = bPFull + 2, bNever = bPVDone + 2, bDrain = bNever + 1,
               bBsync = bDrain + 1, kNumBars = bBsync + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot (u32), abort flag (int)
@@ -108,8 +116,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(bQFull), 1);
     mbar_init(bar(bQFree), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(bFull + s), 4);   // the four key/value gather warps
-      mbar_init(bar(bEmpty + s), 1);  // MMA commit after both PVs of the tile
+      mbar_init(bar(bKFull + s), 2);   // the two key gather warps
+      mbar_init(bar(bVFull + s), 2);   // the two value gather warps
+      mbar_init(bar(bKEmpty + s), 1);  // MMA commit after the tile's last S
+      mbar_init(bar(bVEmpty + s), 1);  // MMA commit after the tile's last PV
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(bSFull + x), 1);
@@ -174,6 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------- K, V tiles ---
     const bool kw = warp == kKWarp || warp == kKWarp2;
     const int half = (warp == kKWarp2 || warp == kVWarp2) ? 1 : 0;  // channel half this warp loads
+    const int full_b = kw ? bKFull : bVFull, empty_b = kw ? bKEmpty : bVEmpty;
     int64_t t = 0;
     for (; t < ntiles; ++t) {
       const int s = (int)(t % kStages);
@@ -183,11 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool meta = warp == kKWarp;  // writes the key mask rows and bias offsets
       bool live[4];
       if (meta) quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
-      if (t >= kStages && !mbar_wait_warp(bar(bEmpty + s), (uint32_t)((t / kStages) - 1) & 1u, ctl)) break;
+      if (t >= kStages && !mbar_wait_warp(bar(empty_b + s), (uint32_t)((t / kStages) - 1) & 1u, ctl)) break;
       const uint32_t st = sbase + kStage0 + s * kStageBytes;
       uint8_t *sp = smem + kStage0 + s * kStageBytes;
       const int rows = min(128, g.n - kt * 128), nq4 = (rows + 3) >> 2;
-      if (lane == 0) mbar_expect_tx(bar(bFull + s), (uint32_t)nq4 * 512u);
+      if (lane == 0) mbar_expect_tx(bar(full_b + s), (uint32_t)nq4 * 512u);
       __syncwarp();
       if (lane < nq4) {
         // rows 4*lane .. 4*lane+3 of this warp's channel half (pads read token 0 of the image)
@@ -195,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r0 = x.b * g.tokens;
         tma_gather4(st + (kw ? kK : kV) + half * kHalfBytes + 512u * lane, m, x.h * kHd + 64 * half,
                     r0 + max(q.src[0], 0), r0 + max(q.src[1], 0), r0 + max(q.src[2], 0), r0 + max(q.src[3], 0),
-                    bar(bFull + s));
+                    bar(full_b + s));
       }
       if (meta) {
 #pragma unroll
@@ -211,17 +222,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lead = __shfl_sync(0xffffffffu, q.roff[0], lane & ~3);
         const uint32_t bal = __ballot_sync(0xffffffffu, lane_reg && q.roff[0] == lead + 4 * (lane & 3));
         const int flag = (lane & 3) == 0 && ((bal >> (lane & ~3)) & 0xFu) == 0xFu ? 1 : 0;
-        *reinterpret_cast<int4 *>(smem + kRoff + s * 512 + 16 * lane) =
-            make_int4((-4 * q.roff[0]) | flag, -4 * q.roff[1], -4 * q.roff[2], -4 * q.roff[3]);
+        auto h16 = [](int v) { return (uint32_t)v & 0xFFFFu; };
+        *reinterpret_cast<uint2 *>(smem + kRoff + (int)(t % kRoffSlots) * 256 + 8 * lane) =
+            make_uint2(h16((-4 * q.roff[0]) | flag) | (h16(-4 * q.roff[1]) << 16),
+                       h16(-4 * q.roff[2]) | (h16(-4 * q.roff[3]) << 16));
         fence_proxy_async_smem();
       }
-      mbar_arrive_warp(bar(bFull + s));
+      mbar_arrive_warp(bar(full_b + s));
     }
     // copies still in flight must land before the CTA exits
     volatile int no_abort = 0;
     const WaitCtl dctl{&no_abort, ctl.status, ctl.limit_ns < 50000000ull ? ctl.limit_ns : 50000000ull};
     for (int64_t k = t > kStages ? t - kStages : 0; k < t; ++k)
-      mbar_wait_warp(bar(bFull + (int)(k % kStages)), (uint32_t)(k / kStages) & 1u, dctl);
+      mbar_wait_warp(bar(full_b + (int)(k % kStages)), (uint32_t)(k / kStages) & 1u, dctl);
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
@@ -232,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = (int)(t % kStages), kt = (int)(t % nkt);
         const int64_t it = t / nkt;
         if (xq == 0) {
-          if (!mbar_wait(bar(bFull + s), (uint32_t)(t / kStages) & 1u, ctl)) return false;
+          if (!mbar_wait(bar(bKFull + s), (uint32_t)(t / kStages) & 1u, ctl)) return false;
           if (kt == 0 && !mbar_wait(bar(bQFull), (uint32_t)it & 1u, ctl)) return false;
           tc_fence_after();
         }
@@ -248,6 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_pv = [&](int xq, int64_t t, uint32_t n) -> bool {
         const int s = (int)(t % kStages), kt = (int)(t % nkt);
         if (!mbar_wait(bar(bPFull + xq), (n - 1) & 1u, ctl)) return false;
+        if (xq == 0 && !mbar_wait(bar(bVFull + s), (uint32_t)(t / kStages) & 1u, ctl)) return false;
         tc_fence_after();
         const uint32_t st = sbase + kStage0 + s * kStageBytes;
         for (int kk = 0; kk < 8; ++kk)
@@ -264,16 +278,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kt == 0) {  // the item's first S's (its Q tiles came in after the previous item's last S's)
           ok = issue_s(0, t) && (!has_b || issue_s(1, t));
           if (!ok) break;
+          mma_commit(bar(bKEmpty + (int)(t % kStages)));
           if (kt == nkt - 1) mma_commit(bar(bQFree));
         }
         // PV_A(t), S_A(t+1), PV_B(t), S_B(t+1): S of the next tile of the same item
         // is issued as soon as its query tile's P of this tile has been read
         const bool next = kt + 1 < nkt;
         ok = issue_pv(0, t, ns[0]) && (!next || issue_s(0, t + 1));
-        if (ok && has_b) ok = issue_pv(1, t, ns[1]) && (!next || issue_s(1, t + 1));
+        if (ok && has_b) ok = issue_pv(1, t, ns[1]);
         if (!ok) break;
-        if (next && kt + 1 == nkt - 1) mma_commit(bar(bQFree));  // the item's last reads of its Q tiles
-        mma_commit(bar(bEmpty + (int)(t % kStages)));
+        mma_commit(bar(bVEmpty + (int)(t % kStages)));
+        if (next) {
+          if (has_b && !issue_s(1, t + 1)) break;
+          mma_commit(bar(bKEmpty + (int)((t + 1) % kStages)));
+          if (kt + 1 == nkt - 1) mma_commit(bar(bQFree));  // the item's last reads of its Q tiles
+        }
       }
       mma_commit(bar(bDrain));
       volatile int no_abort = 0;
@@ -340,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mine) continue;
       if (!mbar_wait_warp(bar(bSFull + xq), nt & 1u, ctl)) break;
       tc_fence_after();
-      const int *roff = reinterpret_cast<const int *>(smem + kRoff + (int)(t % kStages) * 512);
+      const int16_t *roff = reinterpret_cast<const int16_t *>(smem + kRoff + (int)(t % kRoffSlots) * 256);
       // pass 1: an upper bound of the tile's row max from S alone
       float ms = -INFINITY;
 #pragma unroll 1
@@ -398,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t brow = bcol_u32 + 4u * (uint32_t)rbase;  // this row's end of the column
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            const int v = roff[64 * c + 16 * k4];  // the same word for every lane
+            const int v = roff[64 * c + 16 * k4];  // the same entry for every lane
             if (v & 1) {
               // regular chunk: key e's value sits 4e bytes below the first key's
               float bv[16];
@@ -416,7 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #pragma unroll
             for (int e = 0; e < 16; e += 4) {
-              const int4 r4 = *reinterpret_cast<const int4 *>(roff + 64 * c + 16 * k4 + e);
+              const uint2 w = *reinterpret_cast<const uint2 *>(roff + 64 * c + 16 * k4 + e);
+              const int4 r4 = make_int4((int)(int16_t)(w.x & 0xFFFFu), (int)w.x >> 16, (int)(int16_t)(w.y & 0xFFFFu),
+                                        (int)w.y >> 16);
               const float2 b01 = make_float2(lds_f32(brow + r4.x), lds_f32(brow + r4.y));
               const float2 b23 = make_float2(lds_f32(brow + r4.z), lds_f32(brow + r4.w));
               const float2 x0 = __fadd2_rn(
