@@ -224,15 +224,31 @@ def time_pair(wl, peaks, flush, reps=50, warmup=10):
             "fwd_bwd_mtok_s": tokens / (fwd_us + bwd_us)}
 
 
-def kernel_source_hash():
-    """Hash of the CUDA sources (csrc/*.cu, *.cuh) that the kernels and their
-    launch plans compile from; host-only .cpp files are not part of it."""
-    h = hashlib.sha256()
+KERNEL_UNITS = {"tcgen05": "swin_tc.cu", "simt": "swin_simt.cu"}
+
+
+def kernel_source_hash(kernels="tcgen05"):
+    """Hash of the CUDA sources a kernel family compiles from: its translation
+    unit (swin_tc.cu or swin_simt.cu), the launch plans (swin_api.cu), and the
+    headers either includes, followed transitively. Changes to other kernels
+    (the head_dim-128 ones) leave it alone."""
     csrc = os.path.join(ROOT, "shifted_window_attention_cyclic_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    todo = [os.path.join(csrc, KERNEL_UNITS[kernels]), os.path.join(csrc, "swin_api.cu")]
+    seen = []
+    while todo:
+        path = os.path.normpath(todo.pop(0))
+        if path in seen or not os.path.exists(path):
+            continue
+        seen.append(path)
+        with open(path) as f:
+            for line in f:
+                line = line.strip()
+                if line.startswith('#include "'):
+                    todo.append(os.path.join(os.path.dirname(path), line.split('"')[1]))
+    h = hashlib.sha256()
+    for path in sorted(seen):
+        with open(path, "rb") as f:
+            h.update(os.path.relpath(path, ROOT).encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -583,7 +599,7 @@ def main():
     fwd_roof_us = roof_us(fwd_flop, fwd_bytes, peaks)
     bwd_roof_us = roof_us(bwd_flop, bwd_bytes, peaks)
     bwd_gbs = bwd_bytes / (bwd_avg * 1e-3) / 1e9
-    khash = kernel_source_hash()
+    khash = kernel_source_hash({1: "simt", 2: "tcgen05"}[attn.info.impl])
 
     # end to end through the public API with host buffers: H2D inputs, fwd, bwd, D2H results
     host_out = {k_: torch.empty(attn.shape, dtype=tdt).pin_memory() for k_ in ("o", "dq", "dk", "dv")}

@@ -13,12 +13,19 @@ import bench  # noqa: E402
 
 def test_committed_traffic_matches_current_sources():
     # the committed ncu traffic belongs to the kernel sources in the tree
-    khash = bench.kernel_source_hash()
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         t = json.load(f)
+    khash = bench.kernel_source_hash(t["kernels"])
     if t["kernel_source_hash"] != khash:
         pytest.skip("kernel sources changed since the committed ncu capture")
     assert bench.profiled_traffic(khash, t["workload"], t["kernels"]) == t["bwd_dram_bytes_per_launch"]
+
+
+def test_source_hash_covers_the_kernel_unit_and_its_headers():
+    # the tcgen05 hash follows swin_tc.cu's includes (tc_ptx.cuh, swin_common.cuh,
+    # the public header) and the launch plans; it differs from the SIMT one
+    a, b = bench.kernel_source_hash("tcgen05"), bench.kernel_source_hash("simt")
+    assert a != b and len(a) == 16 and a == bench.kernel_source_hash("tcgen05")
 
 
 def test_traffic_only_for_its_workload_kernels_and_sources(tmp_path):
