@@ -190,6 +190,31 @@ int swin_attn_bwd_noalloc(swin_attn_plan_t plan, const void *q, const void *k, c
                           const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,
                           swin_stream_t stream);
 
+/* The attention half of a Swin block in one kernel: LayerNorm and the QKV
+ * projection as its prologue, SW-MSA as above, the out-projection and the
+ * residual add as its epilogue, so that Q, K, V and O never go to device
+ * memory (TERRA, Fig. 4 "Layernorm ... Window Attention ... MLP" and Sec. III;
+ * BEAST page, "Model Architecture"). Per token t of image b:
+ *   Xn = (x - mean) / sqrt(var + ln_eps) * ln_gamma + ln_beta
+ *        (mean and biased variance over the C channels of x),
+ *   [q | k | v] = bf16(Xn) W_qkv^T + b_qkv, each rounded to bf16,
+ *   o = SW-MSA(q, k, v; bias, land) of the plan's geometry, rounded to bf16,
+ *   y = x + o W_o^T + b_o, rounded to bf16.
+ * x, y: bf16 [B, grid..., C], 16-byte aligned, y must not overlap x; every
+ * grid token is written once. w_qkv: bf16 [3C][C] row-major (rows 0..C-1
+ * give q, C..2C-1 k, 2C..3C-1 v; head h owns rows h*32..h*32+31 of each);
+ * w_o: bf16 [C][C] row-major (row = output channel); both 16-byte aligned.
+ * ln_gamma, ln_beta, b_o: float32 [C]; b_qkv: float32 [3C]; bias as above
+ * (may be NULL); all 4-byte aligned. ln_eps > 0 and finite.
+ * Supported plans: bf16, head_dim 32, at most 128 slots per window, C a
+ * multiple of 64 up to 256, heads * bias rows <= 8192 (else UNSUPPORTED).
+ * Forward only (no autograd through the projections here).
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED, CUDA (launch). */
+int swin_attn_block_fwd(swin_attn_plan_t plan, const void *x, const float *ln_gamma, const float *ln_beta,
+                        float ln_eps, const void *w_qkv, const float *b_qkv, const void *w_o,
+                        const float *b_o, const float *bias, const uint8_t *land, void *y,
+                        swin_stream_t stream);
+
 /* Testing hook for the failure path of the tensor-core kernels. Every wait
  * inside those kernels gives up after `wait_limit_ns` (default 1 s) and then
  * records SWIN_ERR_TIMEOUT in the status word. force_timeout = 1 makes one

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -436,6 +437,42 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   const int total = f.T * f.heads;
   fold_kernel<<<(total + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(f);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
+}
+
+int swin_attn_block_fwd(swin_attn_plan_t p, const void *x, const float *ln_gamma, const float *ln_beta,
+                        float ln_eps, const void *w_qkv, const float *b_qkv, const void *w_o, const float *b_o,
+                        const float *bias, const uint8_t *land, void *y, swin_stream_t stream) {
+  if (!p || !x || !ln_gamma || !ln_beta || !w_qkv || !b_qkv || !w_o || !b_o || !y) return SWIN_ERR_INVALID_ARG;
+  if (p->d.has_land && !land) return SWIN_ERR_INVALID_ARG;
+  if (!(ln_eps > 0.f) || !std::isfinite(ln_eps)) return SWIN_ERR_INVALID_ARG;
+  const int64_t bytes = (int64_t)p->g.batch * p->g.tokens * p->g.C * 2;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+  if (xa < ya + (uintptr_t)bytes && ya < xa + (uintptr_t)bytes) return SWIN_ERR_INVALID_ARG;  // y overlaps x
+  if (!aligned16(x) || !aligned16(y) || !aligned16(w_qkv) || !aligned16(w_o)) return SWIN_ERR_ALIGNMENT;
+  if (!aligned4(ln_gamma) || !aligned4(ln_beta) || !aligned4(b_qkv) || !aligned4(b_o) || (bias && !aligned4(bias)) ||
+      (p->d.has_land && !aligned4(land)))
+    return SWIN_ERR_ALIGNMENT;
+  if (p->d.dtype != SWIN_BF16 || p->impl != SWIN_IMPL_TC || p->large) return SWIN_ERR_UNSUPPORTED;
+  int rc = current_device_matches(p);
+  if (rc) return rc;
+  BlockArgs a;
+  a.g = p->g;
+  a.x = x;
+  a.y = y;
+  a.gamma = ln_gamma;
+  a.beta = ln_beta;
+  a.b_qkv = b_qkv;
+  a.b_o = b_o;
+  a.bias = bias;
+  a.land = p->d.has_land ? land : nullptr;
+  a.eps = ln_eps;
+  a.scale = 1.0f / sqrtf((float)p->g.hd);
+  a.status = p->d_status;
+  a.items = (int64_t)p->g.batch * p->g.nwin;
+  a.ctas = (int)std::min<int64_t>(a.items, (int64_t)p->num_sms);
+  a.wait_limit_ns = p->wait_limit_ns;
+  if (a.items == 0) return SWIN_OK;
+  return launch_block_fwd(a, w_qkv, w_o, stream);
 }
 
 int swin_attn_plan_set_debug(swin_attn_plan_t p, uint64_t wait_limit_ns, int force_timeout) {

@@ -247,8 +247,24 @@ struct FoldArgs {
   int T, heads;
 };
 
+// The attention half of a Swin block (swin_block.cu): LayerNorm + QKV
+// projection, SW-MSA, out-projection + residual.
+struct BlockArgs {
+  Geo g;
+  const void *x;
+  void *y;
+  const float *gamma, *beta, *b_qkv, *b_o, *bias;
+  const uint8_t *land;
+  float eps, scale;
+  int *status;
+  int64_t items;  // windows (batch * nwin)
+  int ctas;
+  uint64_t wait_limit_ns;
+};
+
 // Launchers implemented in the kernel translation units.
 int launch_fwd_simt(const FwdArgs &a, int dtype, void *stream);
+int launch_block_fwd(const BlockArgs &a, const void *w_qkv, const void *w_o, void *stream);
 int launch_bwd_simt(const BwdArgs &a, int dtype, void *stream);
 int simt_fwd_smem(const Geo &g);
 int simt_bwd_smem(const Geo &g);

@@ -118,6 +118,25 @@ class SwinWindowAttention:
         return dq, dk, dv, dbias
 
 
+    def block_forward(self, x, ln_gamma, ln_beta, w_qkv, b_qkv, w_o, b_o, bias=None, land=None, ln_eps=1e-5,
+                      y=None, stream=None):
+        """The attention half of a Swin block in one launch: y = x + SW-MSA(
+        LayerNorm(x) W_qkv^T + b_qkv) W_o^T + b_o (bf16 x, y, W_qkv [3C, C],
+        W_o [C, C]; float32 LayerNorm and bias vectors). Forward only."""
+        self._check(x=x, bias=bias, land=land, y=y)
+        c = self.shape[-1]
+        for name, t, shape, dt in (("ln_gamma", ln_gamma, (c,), torch.float32), ("ln_beta", ln_beta, (c,), torch.float32),
+                                   ("w_qkv", w_qkv, (3 * c, c), torch.bfloat16), ("b_qkv", b_qkv, (3 * c,), torch.float32),
+                                   ("w_o", w_o, (c, c), torch.bfloat16), ("b_o", b_o, (c,), torch.float32)):
+            if tuple(t.shape) != shape or t.dtype != dt or t.device != self.device or not t.is_contiguous():
+                raise ValueError("%s: want a contiguous %s %s on %s" % (name, dt, shape, self.device))
+        if y is None:
+            y = torch.empty(self.shape, dtype=self.torch_dtype, device=self.device)
+        C.swin_attn_block_fwd(self.plan, x, ln_gamma, ln_beta, ln_eps, w_qkv, b_qkv, w_o, b_o, bias,
+                              land if self.has_land else None, y, stream)
+        return y
+
+
 class _SwinAttnFn(torch.autograd.Function):
     @staticmethod
     def forward(ctx, attn, q, k, v, bias, land):

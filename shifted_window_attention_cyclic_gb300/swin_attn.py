@@ -87,6 +87,8 @@ def load_library():
     lib.swin_attn_bwd.restype = ctypes.c_int
     lib.swin_attn_bwd_noalloc.argtypes = [vp] * 13
     lib.swin_attn_bwd_noalloc.restype = ctypes.c_int
+    lib.swin_attn_block_fwd.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.swin_attn_block_fwd.restype = ctypes.c_int
     lib.swin_attn_plan_set_debug.argtypes = [vp, ctypes.c_uint64, ctypes.c_int]
     lib.swin_attn_plan_set_debug.restype = ctypes.c_int
     lib.swin_attn_status.argtypes = [vp, vp]
@@ -247,6 +249,18 @@ def swin_attn_bwd_noalloc(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv
     _check(load_library().swin_attn_bwd_noalloc(plan.handle, pq, pk, pv, pdo, plse, _ptr(bias, 4, "bias"),
                                                 _ptr(land, 4, "land"), pdq, pdk, pdv, _ptr(dbias, 4, "dbias"),
                                                 _stream(stream)), "swin_attn_bwd_noalloc")
+
+
+def swin_attn_block_fwd(plan: Plan, x, ln_gamma, ln_beta, ln_eps, w_qkv, b_qkv, w_o, b_o, bias, land, y,
+                        stream=None) -> None:
+    """LayerNorm + QKV projection, SW-MSA, out-projection + residual in one
+    launch (see include/swin_attn.h); y must not overlap x."""
+    px, py, pwq, pwo = _acts(("x", x), ("y", y), ("w_qkv", w_qkv), ("w_o", w_o))
+    _check(load_library().swin_attn_block_fwd(plan.handle, px, _ptr(ln_gamma, 4, "ln_gamma"),
+                                              _ptr(ln_beta, 4, "ln_beta"), float(ln_eps), pwq,
+                                              _ptr(b_qkv, 4, "b_qkv"), pwo, _ptr(b_o, 4, "b_o"),
+                                              _ptr(bias, 4, "bias"), _ptr(land, 4, "land"), py, _stream(stream)),
+           "swin_attn_block_fwd")
 
 
 def swin_attn_status(plan: Plan, stream=None) -> int:

@@ -146,3 +146,25 @@ def generate(wl: Workload, with_dout: bool = True):
         xi = rng.random((wl.batch, -(-lat // 8), -(-lon // 8)))
         land = land_mask(wl, xi)
     return {"q": q, "k": k, "v": v, "bias": bias, "dout": dout, "land": land}
+
+
+def generate_block(wl: Workload):
+    """Seeded host inputs of the block forward (LayerNorm + QKV projection +
+    SW-MSA + out-projection + residual) on a workload's geometry: x [B, *grid,
+    C] ~ N(0, 1) in bf16, LayerNorm gamma ~ 1 + N(0, 0.1^2) and beta ~ N(0,
+    0.1^2), W_qkv [3C, C] and W_o [C, C] ~ N(0, 1/C) in bf16 (the usual fan-in
+    scale), b_qkv [3C] and b_o [C] ~ N(0, 0.1^2); bias and land as in
+    generate(). Seeded from the workload's seed + 7, drawn in that order."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed + 7))
+    c = wl.channels
+    x = round_bf16(rng.standard_normal((wl.batch,) + tuple(wl.grid) + (c,), dtype=np.float32))
+    gamma = (1.0 + 0.1 * rng.standard_normal(c)).astype(np.float32)
+    beta = (0.1 * rng.standard_normal(c)).astype(np.float32)
+    w_qkv = round_bf16((rng.standard_normal((3 * c, c)) / np.sqrt(c)).astype(np.float32))
+    b_qkv = (0.1 * rng.standard_normal(3 * c)).astype(np.float32)
+    w_o = round_bf16((rng.standard_normal((c, c)) / np.sqrt(c)).astype(np.float32))
+    b_o = (0.1 * rng.standard_normal(c)).astype(np.float32)
+    base = generate(wl, with_dout=False)
+    return {"x": x, "gamma": gamma, "beta": beta, "w_qkv": w_qkv, "b_qkv": b_qkv, "w_o": w_o, "b_o": b_o,
+            "bias": base["bias"], "land": base["land"]}
+
