@@ -359,7 +359,9 @@ constexpr int kStageBytes = 70 * 1024;
 constexpr int kBcol = kStage + kStageBytes;
 constexpr int kMaxBiasRows = 8192;
 constexpr int kBacc = kBcol + kMaxBiasRows * 4;  // float dBias accumulator of the current head
-constexpr int kBarOff = kBacc + kMaxBiasRows * 4;
+// float [8 warps][32 keys][17]: one warp's dS of 16 queries, staged for the diagonal sums
+constexpr int kDiag = kBacc + kMaxBiasRows * 4;
+constexpr int kBarOff = kDiag + 8 * 32 * 17 * 4;
 constexpr int bKVFull = 0, bKVFree = 1, bFull = 2, bEmpty = 3, bSFull = 4, bPFull = 5, bDKVFull = 6, bTFree = 7,
               bNever = 8, bDrain = 9, bBsync = 10, kNumBars = 11;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -572,6 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // thread = key row j; warpgroup grp takes queries [64 grp, 64 grp + 64)
     // of every query tile
     const int grp = warp >> 2, q4 = warp & 3, j = q4 * 32 + lane, tid = grp * 128 + j;
+    float *diag = reinterpret_cast<float *>(smem + kDiag) + warp * (32 * 17);
+    bool keys_run = false;  // this warp's 32 keys are window slots whose bias offsets step by one
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     float *bcol = reinterpret_cast<float *>(smem + kBcol);
     float *bacc = reinterpret_cast<float *>(smem + kBacc);
@@ -615,6 +619,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = x.qt * 128 + j;
         const int wc0[3] = {0, 0, 0};
         roff = slot < g.n ? slot_route(g, wc0, slot).roff : 0;
+        // (the shuffle runs on every lane: a full-mask shuffle that some lanes
+        // skip never completes)
+        const int roff0 = __shfl_sync(0xffffffffu, roff, 0);
+        keys_run = __all_sync(0xffffffffu, slot < g.n && roff == roff0 + lane);
       }
       if (!mbar_wait_warp(bar(bSFull), (uint32_t)t & 1u, ctl)) break;
       tc_fence_after();
@@ -636,10 +644,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hh = 0; hh < 2; ++hh) {
           const uint32_t *sv = hh ? sv1 : sv0;
           const uint32_t *dv = hh ? dv1 : dv0;
+          const int c0 = 32 * c2 + 16 * hh;  // first query column of these 16, within this warpgroup's half
+          // 16 queries whose bias offsets step by one, against a warp of such
+          // keys: the 512 dS values fall on 47 bias rows, one per diagonal
+          // (query - key); they are staged and summed per diagonal, so each
+          // lane adds two sums instead of 16 values
+          const int rq = rb[c0 + (lane & 15)];
+          const bool diag_sum = want_db && keys_run && __all_sync(0xffffffffu, rq == rb[c0] + (lane & 15));
           uint32_t pk[8], dk8[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
-            const int c = 32 * c2 + 16 * hh + e;  // query column within this warpgroup's half
+            const int c = c0 + e;  // query column within this warpgroup's half
             const float2 l2 = *reinterpret_cast<const float2 *>(lse2 + c);
             const float2 d2 = *reinterpret_cast<const float2 *>(dl + c);
             const int2 r2 = *reinterpret_cast<const int2 *>(rb + c);
@@ -647,12 +662,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float p0 = ex2(fmaf(__uint_as_float(sv[e]), cs, b0) - l2.x);
             const float p1 = ex2(fmaf(__uint_as_float(sv[e + 1]), cs, b1) - l2.y);
             const float ds0 = p0 * (__uint_as_float(dv[e]) - d2.x), ds1 = p1 * (__uint_as_float(dv[e + 1]) - d2.y);
-            if (want_db) {
+            if (diag_sum) {
+              diag[lane * 17 + e] = ds0;
+              diag[lane * 17 + e + 1] = ds1;
+            } else if (want_db) {
               if (ds0 != 0.f) atomicAdd(bacc + (r2.x - roff), ds0);
               if (ds1 != 0.f) atomicAdd(bacc + (r2.y - roff), ds1);
             }
             pk[e >> 1] = pack_bf16(p0, p1);
             dk8[e >> 1] = pack_bf16(ds0, ds1);
+          }
+          if (diag_sum) {
+            // lane t: diagonal t - 31 (queries i <= t, key i + 31 - t) and
+            // diagonal t + 1 (queries i > t, key i - t - 1); one of the two per i
+            __syncwarp();
+            float sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const bool lo = i <= lane;
+              const float v = diag[(lo ? i + 31 - lane : i - lane - 1) * 17 + i];
+              if (lo) sa += v;
+              else sb += v;
+            }
+            const int base = rb[c0] - (roff - lane);  // bias row of query c0 against this warp's first key
+            if (sa != 0.f) atomicAdd(bacc + base + lane - 31, sa);
+            if (lane < 15 && sb != 0.f) atomicAdd(bacc + base + lane + 1, sb);
+            __syncwarp();
           }
           tmem_st8(tmem + lane_addr + kColS + col + 16u * hh, pk);    // P^T over S^T
           tmem_st8(tmem + lane_addr + kColdP + col + 16u * hh, dk8);  // dS^T over dP^T
