@@ -224,6 +224,79 @@ def time_pair(wl, peaks, flush, reps=50, warmup=10):
             "fwd_bwd_mtok_s": tokens / (fwd_us + bwd_us)}
 
 
+def block_counts(wl, win_src, land):
+    """Algorithmic FLOPs and bytes of the attention half of a Swin block in one
+    launch: LayerNorm + QKV projection (2 N C 3C), the window attention (the
+    forward's 4 B sum n^2 C) and the out-projection (2 N C C); bytes: x in and
+    y out (2 N C e), the weights (4 C^2 e) and the LayerNorm and bias vectors,
+    land and the bias table. Q, K, V and O stay on chip, so they cost nothing."""
+    fwd_flop, _, _, _, _ = workload_counts(wl, win_src, land, lse_written=False)
+    N, C, e = wl.batch * wl.tokens, wl.channels, 2
+    rows = int(np.prod([2 * w - 1 for w in wl.window]))
+    flop = 2.0 * N * C * 3 * C + fwd_flop + 2.0 * N * C * C
+    nbytes = 2 * N * C * e + 4 * C * C * e + 4 * (6 * C) + (N if land is not None else 0) + rows * wl.heads * 4
+    return flop, nbytes
+
+
+def time_block(wl, peaks, flush, reps=50, warmup=10):
+    """The attention half of a Swin block (LayerNorm + QKV projection, SW-MSA,
+    out-projection + residual) in one launch of swin_attn_block_fwd, timed
+    launch by launch after an L2 flush (medians over `reps`); beside it, for
+    context, the same block unfused: torch layer_norm and linear (cuBLAS)
+    around this library's attention forward, timed as one region."""
+    import torch
+    import torch.nn.functional as F
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300 import workloads
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    dev = torch.device("cuda", torch.cuda.current_device())
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch, "bf16",
+                               wl.has_land)
+    h = workloads.generate_block(wl)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf = lambda a: f32(a).to(torch.bfloat16)
+    x, w_qkv, w_o = bf(h["x"]), bf(h["w_qkv"]), bf(h["w_o"])
+    gamma, beta, b_qkv, b_o, bias = f32(h["gamma"]), f32(h["beta"]), f32(h["b_qkv"]), f32(h["b_o"]), f32(h["bias"])
+    land = f32(h["land"]) if h["land"] is not None else None
+    y = torch.empty_like(x)
+    c = wl.channels
+
+    def unfused():
+        xn = F.layer_norm(x, (c,), gamma.to(torch.bfloat16), beta.to(torch.bfloat16), 1e-5)
+        q, k, v = (t.contiguous() for t in F.linear(xn, w_qkv, b_qkv.to(torch.bfloat16)).split(c, dim=-1))
+        o, _ = attn.forward(q, k, v, bias, land, need_lse=False)
+        return x + F.linear(o, w_o, b_o.to(torch.bfloat16))
+
+    stream = torch.cuda.current_stream()
+    times = {"fused": [], "unfused": []}
+    for r in range(warmup + reps):
+        for key in times:
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            flush.add_(1)
+            ev[0].record(stream)
+            if key == "fused":
+                attn.block_forward(x, gamma, beta, w_qkv, b_qkv, w_o, b_o, bias, land, 1e-5, y=y)
+            else:
+                unfused()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            if r >= warmup:
+                times[key].append(ev[0].elapsed_time(ev[1]) * 1e3)
+    assert C.swin_attn_status(attn.plan) == 0
+    win_src = C.swin_attn_plan_tables(attn.plan)[0]
+    flop, nbytes = block_counts(wl, win_src, h["land"])
+    fused_us, unfused_us = statistics.median(times["fused"]), statistics.median(times["unfused"])
+    roof = roof_us(flop, nbytes, peaks)
+    tokens = wl.batch * wl.tokens
+    return {"grid": list(wl.grid), "window": list(wl.window), "channels": c,
+            "l2": "1 GiB written before each launch", "reps": reps, "warmup": warmup,
+            "fwd": {"us": fused_us, "mtok_s": tokens / fused_us, "roof_us": roof, "roof_frac": roof / fused_us,
+                    "tflops": flop / fused_us / 1e6, "bound": "tensor" if flop / (peaks["bf16_tflops"] * 1e12) >
+                    nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"},
+            "unfused_us": unfused_us,
+            "unfused": "torch layer_norm + linear (cuBLAS) around swin_attn_fwd, for context"}
+
+
 KERNEL_UNITS = {"tcgen05": "swin_tc.cu", "simt": "swin_simt.cu"}
 
 
@@ -681,6 +754,10 @@ def main():
         # the W-MSA + SW-MSA pair on the eddy-resolving ocean grid (TERRA's Wenhai stand-in)
         configs["block_pair_eddy_ocean"] = time_pair(workloads.WORKLOADS["eddy_ocean"], peaks, flush,
                                                      reps=args.config_reps, warmup=10)
+        # the attention half of a Swin block in one launch (LayerNorm + QKV, SW-MSA, out-projection)
+        for name in ("depth3d", "grid1deg"):
+            configs["block_fused_" + name] = time_block(workloads.WORKLOADS[name], peaks, flush,
+                                                        reps=args.config_reps, warmup=10)
         configs["clocks"] = csampler.stop()
         configs["peaks"] = {"hbm_gbs": peaks["hbm_gbs"], "bf16_tflops": peaks["bf16_tflops"],
                             "source": peak_kind, "which": "burst bf16 peak, measured copy bandwidth"}

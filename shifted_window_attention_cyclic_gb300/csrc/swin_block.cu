@@ -57,7 +57,9 @@ constexpr int kQm = kO + 8192, kKm = kQm + 4096;  // [128][16] SW32
 constexpr int kBcol = kKm + 4096;             // float [heads][T]: bias * log2e
 constexpr int kRoff = kBcol + kMaxBias * 4;   // int [128]: key side of the bias offsets
 constexpr int kSrc = kRoff + 512;             // int [128]: source token of each slot, -1 for pads
-constexpr int kPar = kSrc + 512;              // float gamma[256], beta[256], b_o[256], b_qkv[768]
+constexpr int kRb = kSrc + 512;               // int [128]: query side of the bias offsets
+constexpr int kXch = kRb + 512;               // float [2][128]: second warpgroup's row max and sum
+constexpr int kPar = kXch + 1024;             // float gamma[256], beta[256], b_o[256], b_qkv[768]
 constexpr int kBarOff = kPar + (3 * kMaxC + 3 * kMaxC) * 4;
 constexpr int bW = 0, bWo = 1, bQKV = 2, bS = 3, bO = 4, bY = 5, bDrain = 6, kNumBars = 7;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
@@ -65,8 +67,9 @@ constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
 static_assert(kWqkv % 1024 == 0 && kWo % 1024 == 0 && kQ % 1024 == 0 && kQm % 1024 == 0, "layout");
 
-// TMEM columns: QKV (96) at 0, O (32) at 96, S (128) at 128, Y (C) at 256
-constexpr uint32_t kColQKV = 0, kColO = 96, kColS = 128, kColY = 256;
+// TMEM columns: QKV (96) at 0, O (32) at 96, S (128) at 128, Y (C) at 256;
+// the second key half's O at 64 (the V columns, read before the PV product)
+constexpr uint32_t kColQKV = 0, kColO1 = 64, kColO = 96, kColS = 128, kColY = 256;
 
 // 16-byte chunk c of row r in a 64-byte-row tile with 64-byte swizzle
 __device__ __forceinline__ uint32_t sw64(int r, int c) { return r * 64 + ((c ^ ((r >> 1) & 3)) << 4); }
@@ -104,6 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float *bcol = reinterpret_cast<float *>(smem + kBcol);
   int *roff = reinterpret_cast<int *>(smem + kRoff);
   int *srcs = reinterpret_cast<int *>(smem + kSrc);
+  int *rbs = reinterpret_cast<int *>(smem + kRb);
+  float *xch = reinterpret_cast<float *>(smem + kXch);
   float *gam = reinterpret_cast<float *>(smem + kPar), *bet = gam + kMaxC, *bo = bet + kMaxC, *bqkv = bo + kMaxC;
 
   if (tid == 0) {
@@ -195,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       srcs[tid] = src;
       roff[tid] = ro;
+      rbs[tid] = rbase;
       *reinterpret_cast<uint4 *>(smem + kQm + sw32(tid, 0)) = mask_chunk(live, reg, false);
       *reinterpret_cast<uint4 *>(smem + kKm + sw32(tid, 0)) = mask_chunk(live, reg, true);
     }
@@ -251,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     __syncthreads();
 
-    float l_row = 0.f;
+    float m_own = 0.f, l_own = 0.f;  // this warpgroup's row max and sum over its key half
+    bool any_own = false;
     for (int h = 0; h < H; ++h, ++hc) {
       const uint32_t ph = hc & 1u;
       // ---------------------------------------------- QKV_h = Xn W_qkv,h^T ---
@@ -318,57 +325,71 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       // ------------------------------------------------------------ softmax ---
-      if (warp < 4) {
-        uint32_t sv[8][16];
+      // warpgroup grp takes keys [64 grp, 64 grp + 64) of every row: its own
+      // max m, P = exp2(x - m) in bf16 over its S columns and its sum l; the
+      // O epilogue puts the two halves on one scale
+      {
+        const int grp = warp >> 2, kb0 = 4 * grp, nk = min(ng - kb0, 4);
+        any_own = false;
+        m_own = 0.f;
+        l_own = 0.f;
+        if (nk > 0) {
+          uint32_t sv[4][16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (k < ng) tmem_ld16(tmem + lane_addr + kColS + 16u * k, sv[k]);
-        tmem_wait_ld_tied(sv[0], sv[1]);
-        tmem_tie(sv[2], sv[3]);
-        tmem_tie(sv[4], sv[5]);
-        tmem_tie(sv[6], sv[7]);
-        const float *bc = bcol + h * g.T + rbase;
-        float mx = -INFINITY;
+          for (int k = 0; k < 4; ++k)
+            if (k < nk) tmem_ld16(tmem + lane_addr + kColS + 16u * (kb0 + k), sv[k]);
+          tmem_wait_ld_tied(sv[0], sv[1]);
+          tmem_tie(sv[2], sv[3]);
+          const float *bc = bcol + h * g.T + rbs[row];
+          const int *ro = roff + 16 * kb0;
+          float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k < ng) {
+          for (int k = 0; k < 4; ++k) {
+            if (k < nk) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float x = fmaf(__uint_as_float(sv[k][e]), cs, bc[-roff[16 * k + e]]);
-              sv[k][e] = __float_as_uint(x);
-              mx = fmaxf(mx, x);
+              for (int e = 0; e < 16; ++e) {
+                const float x = fmaf(__uint_as_float(sv[k][e]), cs, bc[-ro[16 * k + e]]);
+                sv[k][e] = __float_as_uint(x);
+                mq[e & 3] = fmaxf(mq[e & 3], x);
+              }
             }
           }
-        }
-        // keys all masked for this row (about -2^100 after the mask step): no weight
-        const bool any = mx > -1e29f;
-        const float m = any ? mx : 0.f;
-        float l = 0.f;
+          const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+          // keys all masked in this half (about -2^100 after the mask step): no weight
+          any_own = mx > -1e29f;
+          m_own = any_own ? mx : 0.f;
+          float lq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (k < ng) {
-            uint32_t pv[8];
+          for (int k = 0; k < 4; ++k) {
+            if (k < nk) {
+              uint32_t pv[8];
 #pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-              const float p0 = any ? ex2(__uint_as_float(sv[k][e]) - m) : 0.f;
-              const float p1 = any ? ex2(__uint_as_float(sv[k][e + 1]) - m) : 0.f;
-              l += p0 + p1;
-              pv[e >> 1] = pack_bf16(p0, p1);
+              for (int e = 0; e < 16; e += 2) {
+                const float p0 = any_own ? ex2(__uint_as_float(sv[k][e]) - m_own) : 0.f;
+                const float p1 = any_own ? ex2(__uint_as_float(sv[k][e + 1]) - m_own) : 0.f;
+                lq[(e >> 1) & 3] += p0 + p1;
+                pv[e >> 1] = pack_bf16(p0, p1);
+              }
+              tmem_st8(tmem + lane_addr + kColS + 16u * (kb0 + k), pv);
             }
-            tmem_st8(tmem + lane_addr + kColS + 16u * k, pv);
           }
+          l_own = (lq[0] + lq[1]) + (lq[2] + lq[3]);
+          tmem_wait_st();
         }
-        l_row = live && l > 0.f ? 1.f / l : 0.f;
-        tmem_wait_st();
+        if (grp == 1) {
+          xch[row] = any_own ? m_own : -INFINITY;
+          xch[128 + row] = l_own;
+        }
       }
       tc_fence_before();
       __syncthreads();
       // ---------------------------------------------------------- O = P V ---
+      // keys 0-63 into O (columns 96..127), keys 64-127 into O1 (64..95)
       if (tid == 0) {
         tc_fence_after();
         for (int kk = 0; kk < ng; ++kk)
-          mma_ts(tmem + kColO, tmem + kColS + 16u * kk, smem_desc(sbase + kV + 1024u * kk, 8192, 512, kSwizzle64B),
-                 idesc_pv, kk > 0 ? 1u : 0u);
+          mma_ts(tmem + (kk < 4 ? kColO : kColO1), tmem + kColS + 16u * kk,
+                 smem_desc(sbase + kV + 1024u * kk, 8192, 512, kSwizzle64B), idesc_pv, (kk & 3) ? 1u : 0u);
         mma_commit(bar(bO));
       }
       ok = cta_wait(bO, ph, true);
@@ -376,15 +397,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // ------------------------------------------------- O / l -> bf16 tile ---
       if (warp < 4) {
-        uint32_t o0[16], o1[16];
+        const float m1 = xch[row], l1 = xch[128 + row];
+        const bool any1 = ng > 4 && m1 != -INFINITY;
+        const float m = any_own ? (any1 ? fmaxf(m_own, m1) : m_own) : (any1 ? m1 : 0.f);
+        const float s0 = any_own ? ex2(m_own - m) : 0.f, s1 = any1 ? ex2(m1 - m) : 0.f;
+        const float lsum = l_own * s0 + l1 * s1;
+        const float inv = live && lsum > 0.f ? 1.f / lsum : 0.f;
+        const float a0 = s0 * inv, a1 = s1 * inv;
+        uint32_t o0[16], o1[16], q0[16], q1[16];
         tmem_ld16(tmem + lane_addr + kColO, o0);
         tmem_ld16(tmem + lane_addr + kColO + 16u, o1);
+        if (ng > 4) {
+          tmem_ld16(tmem + lane_addr + kColO1, q0);
+          tmem_ld16(tmem + lane_addr + kColO1 + 16u, q1);
+        }
         tmem_wait_ld_tied(o0, o1);
+        tmem_tie(q0, q1);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; e += 2) {
-          w[e >> 1] = pack_bf16(__uint_as_float(o0[e]) * l_row, __uint_as_float(o0[e + 1]) * l_row);
-          w[8 + (e >> 1)] = pack_bf16(__uint_as_float(o1[e]) * l_row, __uint_as_float(o1[e + 1]) * l_row);
+          float v0 = __uint_as_float(o0[e]) * a0, v1 = __uint_as_float(o0[e + 1]) * a0;
+          float u0 = __uint_as_float(o1[e]) * a0, u1 = __uint_as_float(o1[e + 1]) * a0;
+          if (ng > 4) {
+            v0 = fmaf(__uint_as_float(q0[e]), a1, v0);
+            v1 = fmaf(__uint_as_float(q0[e + 1]), a1, v1);
+            u0 = fmaf(__uint_as_float(q1[e]), a1, u0);
+            u1 = fmaf(__uint_as_float(q1[e + 1]), a1, u1);
+          }
+          w[e >> 1] = pack_bf16(v0, v1);
+          w[8 + (e >> 1)] = pack_bf16(u0, u1);
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q)
