@@ -112,8 +112,10 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
     dbias = attn.new_bias()
     ws = attn.workspace()
     stream = torch.cuda.current_stream()
-    fwd_t, bwd_t = [], []
+    fwd_t, bwd_t, bwdo_t = [], [], []
     backward = wl.backward
+    # head_dim 128: the backward also given the forward's output (delta = dO . O)
+    with_o = backward and wl.head_dim == 128
     if backward:
         try:  # a kernel family without a backward yet is timed forward only
             C.swin_attn_fwd(attn.plan, d["q"], d["k"], d["v"], bias, land, o, lse, stream)
@@ -135,11 +137,20 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
             C.swin_attn_bwd(attn.plan, d["q"], d["k"], d["v"], d["dout"], lse, bias, land, dq, dk, dv, dbias, ws,
                             stream)
             ev[3].record(stream)
+        if with_o:
+            ev += [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            flush.add_(1)
+            ev[4].record(stream)
+            C.swin_attn_bwd_o(attn.plan, d["q"], d["k"], d["v"], o, d["dout"], lse, bias, land, dq, dk, dv, dbias,
+                              ws, stream)
+            ev[5].record(stream)
         torch.cuda.synchronize()
         if r >= warmup:
             fwd_t.append(ev[0].elapsed_time(ev[1]) * 1e3)
             if backward:
                 bwd_t.append(ev[2].elapsed_time(ev[3]) * 1e3)
+            if with_o:
+                bwdo_t.append(ev[4].elapsed_time(ev[5]) * 1e3)
     assert C.swin_attn_status(attn.plan) == 0
     tokens = wl.batch * wl.tokens
     fwd_us = statistics.median(fwd_t)
@@ -156,6 +167,11 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
                       "roof_frac": b_roof / bwd_us, "alg_bytes": bwd_bytes,
                       "roof_frac_moved": roof_us(bwd_flop, bwd_moved, peaks) / bwd_us, "alg_bytes_moved": bwd_moved}
         res["fwd_bwd_mtok_s"] = tokens / (fwd_us + bwd_us)
+    if with_o and backward:
+        us = statistics.median(bwdo_t)
+        b_roof = roof_us(bwd_flop, bwd_bytes, peaks)
+        res["bwd_o"] = {"us": us, "tflops": bwd_flop / us / 1e6, "roof_us": b_roof, "roof_frac": b_roof / us,
+                        "api": "swin_attn_bwd_o: delta = dO . O from the forward's bf16 output"}
     elif wl.backward:
         res["bwd"] = "no backward kernel for this configuration yet"
     tgt = TARGETS.get(wl.name)

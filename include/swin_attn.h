@@ -163,6 +163,21 @@ int swin_attn_bwd(swin_attn_plan_t plan, const void *q, const void *k, const voi
                   const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,
                   void *workspace, size_t workspace_bytes, swin_stream_t stream);
 
+/* Backward that also receives the forward's output o (same type, layout and
+ * alignment as q; o of the same inputs). With head_dim 128, delta_i is then
+ * sum over the head's channels of dout_ic * o_ic (FlashAttention's form of
+ * the softmax derivative's row sum, which TERRA's FlashAttention backward
+ * uses), computed by a small kernel before the query-tile kernel, which then
+ * sweeps the key tiles once instead of twice. It differs from swin_attn_bwd's
+ * delta by the rounding of o to the storage type. Other head dims ignore o
+ * (their kernels recompute delta in the pass that needs it at no extra cost)
+ * and give swin_attn_bwd's results. Other arguments, results and errors as
+ * swin_attn_bwd; o NULL is INVALID_ARG, misaligned ALIGNMENT. */
+int swin_attn_bwd_o(swin_attn_plan_t plan, const void *q, const void *k, const void *v, const void *o,
+                    const void *dout, const float *lse, const float *bias, const uint8_t *land, void *dq,
+                    void *dk, void *dv, float *dbias, void *workspace, size_t workspace_bytes,
+                    swin_stream_t stream);
+
 /* Backward for callers that cannot allocate device memory. No counterpart on
  * the pages: it exists for callers whose host code has no device allocator
  * of its own (for example a C or Fortran model that only receives tensors),

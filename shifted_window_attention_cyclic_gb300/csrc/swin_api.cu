@@ -386,10 +386,15 @@ int swin_attn_fwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   return launch_fwd_simt(a, p->d.dtype, stream);
 }
 
-int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *v, const void *dout,
-                  const float *lse, const float *bias, const uint8_t *land, void *dq, void *dk, void *dv,
-                  float *dbias, void *workspace, size_t workspace_bytes, swin_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// swin_attn_bwd and swin_attn_bwd_o: o (the forward's output) may be NULL.
+int bwd_impl(swin_attn_plan_t p, const void *q, const void *k, const void *v, const void *o, const void *dout,
+             const float *lse, const float *bias, const uint8_t *land, void *dq, void *dk, void *dv, float *dbias,
+             void *workspace, size_t workspace_bytes, swin_stream_t stream) {
   if (!p || !q || !k || !v || !dout || !lse || !dq || !dk || !dv) return SWIN_ERR_INVALID_ARG;
+  if (o && !aligned16(o)) return SWIN_ERR_ALIGNMENT;
   if (p->d.has_land && !land) return SWIN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) ||
       !aligned16(dv))
@@ -416,6 +421,7 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   a.dk = dk;
   a.dv = dv;
   a.delta = p->large ? static_cast<float *>(workspace) : nullptr;
+  a.o = p->large ? o : nullptr;  // the other kernels recompute delta in the pass that needs it
   a.ws = dbias ? reinterpret_cast<float *>(static_cast<char *>(workspace) + delta_bytes(p)) : nullptr;
   a.slot_base = p->d_slot_base;
   a.ws_slots = p->ws_slots;
@@ -437,6 +443,23 @@ int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *
   const int total = f.T * f.heads;
   fold_kernel<<<(total + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(f);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" {
+
+int swin_attn_bwd(swin_attn_plan_t p, const void *q, const void *k, const void *v, const void *dout,
+                  const float *lse, const float *bias, const uint8_t *land, void *dq, void *dk, void *dv,
+                  float *dbias, void *workspace, size_t workspace_bytes, swin_stream_t stream) {
+  return bwd_impl(p, q, k, v, nullptr, dout, lse, bias, land, dq, dk, dv, dbias, workspace, workspace_bytes,
+                  stream);
+}
+
+int swin_attn_bwd_o(swin_attn_plan_t p, const void *q, const void *k, const void *v, const void *o,
+                    const void *dout, const float *lse, const float *bias, const uint8_t *land, void *dq, void *dk,
+                    void *dv, float *dbias, void *workspace, size_t workspace_bytes, swin_stream_t stream) {
+  if (!o) return SWIN_ERR_INVALID_ARG;
+  return bwd_impl(p, q, k, v, o, dout, lse, bias, land, dq, dk, dv, dbias, workspace, workspace_bytes, stream);
 }
 
 int swin_attn_block_fwd(swin_attn_plan_t p, const void *x, const float *ln_gamma, const float *ln_beta,

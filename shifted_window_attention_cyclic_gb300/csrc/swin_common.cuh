@@ -230,6 +230,7 @@ struct BwdArgs {
   void *dq, *dk, *dv;
   float *ws;              // [slots][T] partial dBias tables, or nullptr (dbias not wanted)
   float *delta;           // head_dim-128 kernels: [B][heads][tokens] delta_i, or nullptr
+  const void *o;          // the forward's output, or nullptr: with head_dim 128, delta = dO . O from it
   int64_t ws_slots;       // slots of ws
   const int *slot_base;   // [ctas] first workspace slot of each CTA
   int *status;

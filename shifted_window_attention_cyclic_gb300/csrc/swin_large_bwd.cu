@@ -63,7 +63,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kMiscOff + 4);
   const Geo &g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkt = g.nqt, per_item = 2 * nkt;  // key tiles of the two sweeps
+  // key tiles per item: two sweeps (delta, then dS and dQ), or one when delta
+  // was computed from the forward's output before this kernel
+  const bool delta_given = a.o != nullptr;
+  const int nkt = g.nqt, per_item = delta_given ? nkt : 2 * nkt;
   int64_t L, R;
   eq4_range(a.items, a.ctas, blockIdx.x, L, R);
   const int64_t count = R - L, ntiles = count * per_item;
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t t = 0; ok && t < ntiles; ++t) {
         const int s = (int)(t % kStages), u = (int)(t % per_item), kt = u % nkt;
         const int64_t it = t / per_item;
-        const bool second = u >= nkt;
+        const bool second = delta_given || u >= nkt;
         ok = mbar_wait(bar(bFull + s), (uint32_t)(t / kStages) & 1u, ctl) &&
              (u != 0 || mbar_wait(bar(bQFull), (uint32_t)it & 1u, ctl)) &&
              (t == 0 || mbar_wait(bar(bPFull), (uint32_t)(t - 1) & 1u, ctl));  // S and dP of t-1 consumed
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t t = 0; ok && t < ntiles; ++t) {
       const int s = (int)(t % kStages), u = (int)(t % per_item), kt = u % nkt;
       const int64_t it = t / per_item;
-      const bool second = u >= nkt;
+      const bool second = delta_given || u >= nkt;
       const LItem x = decode(g, L + it);
       if (u == 0) {
         if (has_bias && x.h != cur_h) {
@@ -283,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         live = src >= 0 && (!a.land || __ldg(a.land + (int64_t)x.b * g.tokens + src) == 0);
         lse2 = live ? __ldg(a.lse + ((int64_t)x.b * g.heads + x.h) * g.tokens + src) * kLog2e : 0.f;
         dpart = 0.f;
+        if (delta_given) delta = live ? __ldcg(a.delta + ((int64_t)x.b * g.heads + x.h) * g.tokens + src) : 0.f;
       }
       if (!mbar_wait_warp(bar(bSFull), (uint32_t)t & 1u, ctl)) break;
       tc_fence_after();
@@ -348,6 +352,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 }  // namespace bq
+
+// ---------------------------------------------------------- delta from O ---
+// delta_i = sum_c dO_ic O_ic over each head's 128 channels (the softmax
+// derivative's row sum, FlashAttention's form): one warp per token, lanes
+// over 16-byte chunks of the token's C channels, 16 lanes per head and pass.
+__global__ void __launch_bounds__(256) delta_kernel(const BwdArgs a) {
+  const Geo &g = a.g;
+  const int64_t tok = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (tok >= (int64_t)g.batch * g.tokens) return;
+  const int64_t b = tok / g.tokens, t = tok % g.tokens;
+  const uint4 *o = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.o) + tok * g.C);
+  const uint4 *d = reinterpret_cast<const uint4 *>(static_cast<const __nv_bfloat16 *>(a.dout) + tok * g.C);
+  const int chunks = g.C >> 3;  // 16-byte chunks per token (16 per head)
+  for (int c0 = 0; c0 < chunks; c0 += 32) {
+    const int c = c0 + lane;
+    float s = 0.f;
+    if (c < chunks) {
+      const uint4 x = __ldg(o + c), y = __ldg(d + c);
+      const uint32_t xa[4] = {x.x, x.y, x.z, x.w}, ya[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s = fmaf(__uint_as_float(xa[e] << 16), __uint_as_float(ya[e] << 16), s);
+        s = fmaf(__uint_as_float(xa[e] & 0xFFFF0000u), __uint_as_float(ya[e] & 0xFFFF0000u), s);
+      }
+    }
+#pragma unroll
+    for (int m = 8; m > 0; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    if ((lane & 15) == 0 && c < chunks) a.delta[(b * g.heads + (c >> 4)) * g.tokens + t] = s;
+  }
+}
 
 // -------------------------------------------------------------- key tiles ---
 namespace bkv {
@@ -726,6 +761,10 @@ int launch_bwd_large(const BwdArgs &a, void *stream) {
           cudaSuccess)
     return SWIN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a.o) {
+    const int64_t toks = (int64_t)a.g.batch * a.g.tokens;
+    lg::delta_kernel<<<(unsigned)((toks + 7) / 8), 256, 0, s>>>(a);
+  }
   lg::bq::bwdq_kernel<<<a.ctas, lg::kThreads, lg::bq::kSmemBytes, s>>>(a, mq, mk, mv, mdo);
   lg::bkv::bwdkv_kernel<<<a.ctas, lg::kThreads, lg::bkv::kSmemBytes, s>>>(a, mq, mk, mv, mdo);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;

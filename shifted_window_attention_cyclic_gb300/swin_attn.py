@@ -85,6 +85,8 @@ def load_library():
     lib.swin_attn_fwd.restype = ctypes.c_int
     lib.swin_attn_bwd.argtypes = [vp] * 13 + [sz, vp]
     lib.swin_attn_bwd.restype = ctypes.c_int
+    lib.swin_attn_bwd_o.argtypes = [vp] * 14 + [sz, vp]
+    lib.swin_attn_bwd_o.restype = ctypes.c_int
     lib.swin_attn_bwd_noalloc.argtypes = [vp] * 13
     lib.swin_attn_bwd_noalloc.restype = ctypes.c_int
     lib.swin_attn_block_fwd.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -239,6 +241,18 @@ def swin_attn_bwd(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv, dbias,
                                         _ptr(land, 4, "land"), pdq, pdk, pdv, _ptr(dbias, 4, "dbias"),
                                         _ptr(workspace, 256, "workspace"), ws_bytes, _stream(stream)),
            "swin_attn_bwd")
+
+
+def swin_attn_bwd_o(plan: Plan, q, k, v, o, dout, lse, bias, land, dq, dk, dv, dbias, workspace,
+                    stream=None) -> None:
+    """Backward given the forward's output o (head_dim 128: delta from dout . o)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    pq, pk, pv, po, pdo, plse, pdq, pdk, pdv = _acts(("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout),
+                                                     ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))
+    _check(load_library().swin_attn_bwd_o(plan.handle, pq, pk, pv, po, pdo, plse, _ptr(bias, 4, "bias"),
+                                          _ptr(land, 4, "land"), pdq, pdk, pdv, _ptr(dbias, 4, "dbias"),
+                                          _ptr(workspace, 256, "workspace"), ws_bytes, _stream(stream)),
+           "swin_attn_bwd_o")
 
 
 def swin_attn_bwd_noalloc(plan: Plan, q, k, v, dout, lse, bias, land, dq, dk, dv, dbias, stream=None) -> None:

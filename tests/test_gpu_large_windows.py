@@ -3,13 +3,15 @@ kernels) against the oracle, through the C ABI, forward and backward:
 TERRA's w = 32 windows (1 024 tokens, 8 key tiles, d/Nh = 128) on a grid
 with a periodic seam and land, a ragged 3-D case with partial tiles, a
 window of fewer than 128 slots, and a window without a bias whose bias table
-would not fit the kernels' column (no dBias there)."""
+would not fit the kernels' column (no dBias there). The backward runs both
+ways: delta recomputed as sum_j P dP (swin_attn_bwd) and delta = dout . O
+from the forward's output (swin_attn_bwd_o)."""
 import numpy as np
 import pytest
 
 import oracle
 from shifted_window_attention_cyclic_gb300 import workloads
-from tests.parity_util import assert_close, host, problem_of, to_device
+from tests.parity_util import BF16_MAX_ABS, BF16_REL_L2, assert_close, host, problem_of, to_device
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -56,7 +58,8 @@ def test_large_window_forward_matches_the_oracle(case):
 
 
 @pytest.mark.parametrize("case", CASES)
-def test_large_window_backward_matches_the_oracle(case):
+@pytest.mark.parametrize("with_o", [False, True], ids=["delta_recomputed", "delta_from_o"])
+def test_large_window_backward_matches_the_oracle(case, with_o):
     from shifted_window_attention_cyclic_gb300 import swin_attn as C
     from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
     grid, window, shift, periodic, heads, batch, land_p, with_bias = case
@@ -69,15 +72,27 @@ def test_large_window_backward_matches_the_oracle(case):
                                wl.has_land)
     t = to_device(x, wl, torch.device("cuda", 0))
     bias = t["bias"] if with_bias else None
-    _, lse = attn.forward(t["q"], t["k"], t["v"], bias, t["land"])
-    dq, dk, dv, dbias = attn.backward(t["q"], t["k"], t["v"], t["dout"], lse, bias, t["land"], want_dbias=with_bias)
+    o, lse = attn.forward(t["q"], t["k"], t["v"], bias, t["land"])
+    # with_o: delta = dout . o (o the forward's bf16 output) instead of sum P dP
+    dq, dk, dv, dbias = attn.backward(t["q"], t["k"], t["v"], t["dout"], lse, bias, t["land"], want_dbias=with_bias,
+                                      o=o if with_o else None)
     torch.cuda.synchronize()
     assert C.swin_attn_status(attn.plan) == C.SWIN_OK
     g = oracle.bwd(problem_of(wl), x["q"], x["k"], x["v"], x["bias"], x["land"], x["dout"])
     for key, got in (("dq", dq), ("dk", dk), ("dv", dv)):
         assert_close(key, host(got), g[key], "bf16")
-    if with_bias:
+    if with_bias and not with_o:
         assert_close("dbias", host(dbias), g["dbias"], "bf16")
+    elif with_bias:
+        # delta = dout . O carries O's bf16 storage rounding (2^-9 relative per
+        # term) into every dS of the query, and dBias adds those dS over every
+        # pair of one offset in every window of the head, with one sign: the
+        # max-abs bar grows by 2^-8 of the largest |dBias|; relative L2 keeps
+        # the bar
+        got, ref = host(dbias), g["dbias"]
+        rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+        bar = BF16_MAX_ABS + 2.0 ** -8 * np.abs(ref).max()
+        assert rel <= BF16_REL_L2 and np.abs(got - ref).max() <= bar, (rel, np.abs(got - ref).max(), bar)
     if x["land"] is not None:
         land = x["land"].astype(bool)
         for got in (dq, dk, dv):
