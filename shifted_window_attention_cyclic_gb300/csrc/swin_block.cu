@@ -84,6 +84,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(dst),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
@@ -148,10 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t n_wqkv = 0, n_wo = 0;  // copies issued (thread 0): the drain waits for the last of each
   auto load_wqkv = [&](int h) {
     ++n_wqkv;
+    // one copy: (64 channels) x (32 rows of head h) x (q, k, v) x (C/64 channel
+    // blocks), landing as [block][q|k|v][row][64 channels], the MMA's B layout
     mbar_expect_tx(bar(bW), (uint32_t)(3 * nkb * 4096));
-    for (int p = 0; p < 3; ++p)
-      for (int kb = 0; kb < nkb; ++kb)
-        tma_load_2d(sbase + kWqkv + kb * 12288 + p * 4096, &wqkv_map, kb * 64, p * C + h * kHdB, bar(bW));
+    tma_load_4d(sbase + kWqkv, &wqkv_map, 0, h * kHdB, 0, 0, bar(bW));
     mbar_arrive(bar(bW));  // the phase completes once this arrival and the bytes are in
   };
   auto load_wo = [&](int h) {
@@ -513,11 +522,13 @@ int launch_block_fwd(const BlockArgs &a, const void *w_qkv, const void *w_o, voi
   if (!enc) return SWIN_ERR_CUDA;
   CUtensorMap mq, mo;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)g.C, (cuuint64_t)(3 * g.C)};
-    cuuint64_t strides[1] = {(cuuint64_t)g.C * 2};
-    cuuint32_t box[2] = {64u, 32u};
-    cuuint32_t es[2] = {1u, 1u};
-    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(w_qkv), dims, strides, box, es,
+    // W_qkv [3C][C] as (channel in block, row in part, part, channel block)
+    const cuuint64_t C2 = (cuuint64_t)g.C * 2;
+    cuuint64_t dims[4] = {64, (cuuint64_t)g.C, 3, (cuuint64_t)(g.C / 64)};
+    cuuint64_t strides[3] = {C2, C2 * (cuuint64_t)g.C, 128};
+    cuuint32_t box[4] = {64u, 32u, 3u, (cuuint32_t)(g.C / 64)};
+    cuuint32_t es[4] = {1u, 1u, 1u, 1u};
+    if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(w_qkv), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SWIN_ERR_CUDA;
