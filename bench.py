@@ -589,6 +589,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config table (all five workloads)")
     ap.add_argument("--config-reps", type=int, default=50)
+    ap.add_argument("--only-block", action="store_true",
+                    help="time only the fused block (LayerNorm + QKV, SW-MSA, out-projection) on --workload")
     ap.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
@@ -599,6 +601,13 @@ def main():
         return oracle_sample_main(args.oracle_sample, wl)
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.only_block:
+        import torch
+        peaks, _ = load_peaks()
+        flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        print(json.dumps({"workload": wl.name, "block_fused": time_block(wl, peaks, flush, reps=args.steps,
+                                                                         warmup=args.warmup)}))
+        return 0
 
     import torch
     rank, world, local = dist_info()
