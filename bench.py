@@ -167,11 +167,10 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
                       "roof_frac": b_roof / bwd_us, "alg_bytes": bwd_bytes,
                       "roof_frac_moved": roof_us(bwd_flop, bwd_moved, peaks) / bwd_us, "alg_bytes_moved": bwd_moved}
         res["fwd_bwd_mtok_s"] = tokens / (fwd_us + bwd_us)
-    if with_o and backward:
-        us = statistics.median(bwdo_t)
-        b_roof = roof_us(bwd_flop, bwd_bytes, peaks)
-        res["bwd_o"] = {"us": us, "tflops": bwd_flop / us / 1e6, "roof_us": b_roof, "roof_frac": b_roof / us,
-                        "api": "swin_attn_bwd_o: delta = dO . O from the forward's bf16 output"}
+        if with_o:
+            us = statistics.median(bwdo_t)
+            res["bwd_o"] = {"us": us, "tflops": bwd_flop / us / 1e6, "roof_us": b_roof, "roof_frac": b_roof / us,
+                            "api": "swin_attn_bwd_o: delta = dO . O from the forward's bf16 output"}
     elif wl.backward:
         res["bwd"] = "no backward kernel for this configuration yet"
     tgt = TARGETS.get(wl.name)
