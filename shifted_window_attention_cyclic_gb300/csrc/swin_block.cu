@@ -61,7 +61,7 @@ constexpr int kRb = kSrc + 512;               // int [128]: query side of the bi
 constexpr int kXch = kRb + 512;               // float [2][128]: second warpgroup's row max and sum
 constexpr int kPar = kXch + 1024;             // float gamma[256], beta[256], b_o[256], b_qkv[768]
 constexpr int kBarOff = kPar + (3 * kMaxC + 3 * kMaxC) * 4;
-constexpr int bW = 0, bWo = 1, bQKV = 2, bS = 3, bO = 4, bY = 5, bDrain = 6, kNumBars = 7;
+constexpr int bW = 0, bWo = 1, bQKV = 2, bS = 3, bO = 4, bY = 5, bDrain = 6, bX = 7, kNumBars = 8;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
@@ -93,12 +93,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
       : "memory");
 }
 
+// TMA box store of shared memory into a 5-D tensor map (bulk group), and the
+// bulk-group waits (.read: the source may be overwritten; plain: complete)
+__device__ __forceinline__ void tma_store_5d(const void *tmap, uint32_t src, int c0, int c1, int c2, int c3, int c4) {
+  asm volatile("cp.async.bulk.tensor.5d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5, %6}], [%1];" ::"l"(tmap),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
 __global__ void __launch_bounds__(kThreads, 1)
     block_kernel(const BlockArgs a, const __grid_constant__ CUtensorMap wqkv_map,
-                 const __grid_constant__ CUtensorMap wo_map) {
+                 const __grid_constant__ CUtensorMap wo_map, const __grid_constant__ CUtensorMap x_map,
+                 const __grid_constant__ CUtensorMap y_map) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -169,6 +181,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_2d(sbase + kWo, &wo_map, h * kHdB, 0, bar(bWo));
     mbar_arrive(bar(bWo));
   };
+  // a window that neither wraps nor pads is a box of the grid: X arrives, and
+  // y leaves, as one 5-D TMA box per 64-channel block (the Xn tile's layout)
+  auto window_box = [&](int omega, int (&c)[3]) -> bool {
+    int wc[3];
+    window_coords(g, omega, wc);
+    bool box = true;
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+      c[d] = wc[d] * g.w[d] + g.s[d];
+      box = box && c[d] + g.w[d] <= g.G[d];
+    }
+    return box;
+  };
+  uint32_t n_x = 0;  // X box loads issued (thread 0; every thread counts the waits alike)
+  auto load_x = [&](const int (&c)[3], int b) {
+    ++n_x;
+    mbar_expect_tx(bar(bX), (uint32_t)(nkb * g.n * 128));
+    for (int kb = 0; kb < nkb; ++kb)
+      tma_load_5d(sbase + kXn + kb * 16384, &x_map, kb * 64, c[2], c[1], c[0], b, bar(bX));
+    mbar_arrive(bar(bX));
+  };
   // every thread waits (bounded), then the CTA agrees on the outcome
   auto cta_wait = [&](int b, uint32_t parity, bool ok) -> bool {
     if (ok) ok = mbar_wait(bar(b), parity, ctl);
@@ -183,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ng = (g.n + 15) >> 4;  // 16-key groups of S
   const uint32_t idesc_s = idesc_bf16(128, (uint32_t)(16 * ng), 0, 0);
   uint32_t hc = 0;  // heads done in this CTA (phase of every per-head barrier)
+  uint32_t xph = 0;  // X box loads waited for so far (phase of bX)
   bool ok = true;
   if (tid == 0 && total_heads > 0) {
     load_wqkv(0);
@@ -191,7 +225,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   for (int64_t it = 0; ok && it < count; ++it) {
     const int64_t item = L + it;
-    const int omega = (int)(item % g.nwin), b = (int)(item / g.nwin);
+    // windows in the plan's spread order (the i-th is (i * wstep) mod nwin):
+    // wrapping and padded windows (row loads) fall evenly over the CTAs
+    const int omega = (int)(((item % g.nwin) * (int64_t)g.wstep) % g.nwin), b = (int)(item / g.nwin);
+    int bc[3];
+    const bool box = window_box(omega, bc);
+    if (tid == 0) {
+      // the previous window's y stores have read the region (before this
+      // window's X box or LayerNorm writes it; the route's barrier orders
+      // the other threads' writes after this wait)
+      bulk_wait_read0();
+      if (box) load_x(bc, b);
+    }
     // ------------------------------------------------------------- route ---
     int rbase = g.T - 1, src = -1;
     bool live = false;
@@ -214,6 +259,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4 *>(smem + kKm + sw32(tid, 0)) = mask_chunk(live, reg, true);
     }
     __syncthreads();
+    if (box) {
+      ok = cta_wait(bX, xph & 1u, true);
+      ++xph;
+      if (!ok) break;
+    }
     // --------------------------------------------------------- LayerNorm ---
     {
       const int r = tid >> 1, half = tid & 1, cw = C >> 1;  // this thread: channels [half*cw, half*cw + cw)
@@ -223,9 +273,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                  ((int64_t)b * g.tokens + s) * C + half * cw)
                                : nullptr;
       float sum = 0.f;
+      // a box window's rows are already in the tile (read in place), others
+      // come from L2/HBM
+      if (box) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c0 = half * cw + 8 * j;
+          xv[j] = (s >= 0 && 8 * j < cw)
+                      ? *reinterpret_cast<const uint4 *>(smem + kXn + (c0 >> 6) * 16384 + sw128(r, (c0 & 63) >> 3))
+                      : make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) xv[j] = (xp && 8 * j < cw) ? __ldg(xp + j) : make_uint4(0u, 0u, 0u, 0u);
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        xv[j] = (xp && 8 * j < cw) ? __ldg(xp + j) : make_uint4(0u, 0u, 0u, 0u);
         sum += bf_lo(xv[j].x) + bf_hi(xv[j].x) + bf_lo(xv[j].y) + bf_hi(xv[j].y) + bf_lo(xv[j].z) +
                bf_hi(xv[j].z) + bf_lo(xv[j].w) + bf_hi(xv[j].w);
       }
@@ -294,6 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // the next head's W_qkv rows (this head's product has read them)
       if (tid == 0 && (int64_t)hc + 1 < total_heads) load_wqkv(h + 1 < H ? h + 1 : 0);
+      // the window's last QKV product has read Xn: X comes back into the
+      // region for the epilogue's residual
+      if (tid == 0 && box && h == H - 1) load_x(bc, b);
       // -------------------------------------- + b_qkv, bf16 Q / K / V tiles ---
       {
         const int part = warp < 4 ? 0 : 2;  // warps 0-3: Q then K; warps 4-7: V
@@ -462,8 +528,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------- Y + b_o + X at the tokens ---
     ok = cta_wait(bY, (hc - 1) & 1u, true);
     if (!ok) break;
+    if (box) {
+      ok = cta_wait(bX, xph & 1u, true);  // X back in the region
+      ++xph;
+      if (!ok) break;
+    }
     tc_fence_after();
-    {
+    if (box) {
+      // y = Y + b_o + X in bf16 over X in the tile (row = slot), then one box
+      // store per 64-channel block
+      const int cw = C >> 1, c0 = (warp < 4 ? 0 : cw);
+      const bool real = row < g.n;
+      for (int k = 0; k < cw / 16; ++k) {
+        uint32_t v[16];
+        tmem_ld16(tmem + lane_addr + kColY + (uint32_t)(c0 + 16 * k), v);
+        tmem_wait_ld_tied(v);
+        if (real) {
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int cc = c0 + 16 * k + 8 * q;  // first channel of this 16-byte chunk
+            uint4 *ptr = reinterpret_cast<uint4 *>(smem + kXn + (cc >> 6) * 16384 + sw128(row, (cc & 63) >> 3));
+            const uint4 xq = *ptr;
+            const uint32_t xw[4] = {xq.x, xq.y, xq.z, xq.w};
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = pack_bf16(__uint_as_float(v[8 * q + 2 * e]) + bo[cc + 2 * e] + bf_lo(xw[e]),
+                               __uint_as_float(v[8 * q + 2 * e + 1]) + bo[cc + 2 * e + 1] + bf_hi(xw[e]));
+            *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        for (int kb = 0; kb < nkb; ++kb) tma_store_5d(&y_map, sbase + kXn + kb * 16384, kb * 64, bc[2], bc[1], bc[0], b);
+        bulk_commit();
+      }
+    } else {
       const int cw = C >> 1, c0 = (warp < 4 ? 0 : cw);  // warps 0-3: first half of the channels
       const int s = srcs[row];
       const bool store = s >= 0 && in_bounds(((int64_t)b * g.tokens + s) * C + c0, cw,
@@ -493,6 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
   }
+  if (tid == 0) bulk_wait0();  // every y box store complete before the CTA leaves
 
   // drain: MMAs in flight, then weight copies still in flight
   if (tid == 0) {
@@ -504,6 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // then the only one not yet waited for); earlier ones were consumed
     if (n_wqkv > 0) mbar_wait(bar(bW), (n_wqkv - 1) & 1u, dctl);
     if (n_wo > 0) mbar_wait(bar(bWo), (n_wo - 1) & 1u, dctl);
+    if (n_x > 0) mbar_wait(bar(bX), (n_x - 1) & 1u, dctl);
   }
   tc_fence_before();
   __syncthreads();
@@ -543,10 +648,26 @@ int launch_block_fwd(const BlockArgs &a, const void *w_qkv, const void *w_o, voi
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SWIN_ERR_CUDA;
   }
+  // x and y as [B, G0, G1, G2, C] boxes of (64 channels, a whole window), 128-byte swizzle
+  CUtensorMap mx, my;
+  {
+    const cuuint64_t e = 2;
+    cuuint64_t dims[5] = {(cuuint64_t)g.C, (cuuint64_t)g.G[2], (cuuint64_t)g.G[1], (cuuint64_t)g.G[0],
+                          (cuuint64_t)g.batch};
+    cuuint64_t strides[4] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e,
+                             dims[0] * dims[1] * dims[2] * dims[3] * e};
+    cuuint32_t box[5] = {64u, (cuuint32_t)g.w[2], (cuuint32_t)g.w[1], (cuuint32_t)g.w[0], 1u};
+    cuuint32_t es[5] = {1u, 1u, 1u, 1u, 1u};
+    for (int t = 0; t < 2; ++t)
+      if (enc(t ? &my : &mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, t ? a.y : const_cast<void *>(a.x), dims, strides,
+              box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return SWIN_ERR_CUDA;
+  }
   if (cudaFuncSetAttribute(blk::block_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, blk::kSmemBytes) !=
       cudaSuccess)
     return SWIN_ERR_CUDA;
-  blk::block_kernel<<<a.ctas, blk::kThreads, blk::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mo);
+  blk::block_kernel<<<a.ctas, blk::kThreads, blk::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mo, mx, my);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
 }
 
