@@ -55,7 +55,7 @@ constexpr int kQ = kWo + kMaxC * 64;          // bf16 [128][32] SW64 each
 constexpr int kK = kQ + 8192, kV = kK + 8192, kO = kV + 8192;
 constexpr int kQm = kO + 8192, kKm = kQm + 4096;  // [128][16] SW32
 constexpr int kBcol = kKm + 4096;             // float [heads][T]: bias * log2e
-constexpr int kRoff = kBcol + kMaxBias * 4;   // int [128]: key side of the bias offsets
+constexpr int kRoff = kBcol + kMaxBias * 4;   // int [128]: key side of the bias offsets, as -4 * offset (bytes)
 constexpr int kSrc = kRoff + 512;             // int [128]: source token of each slot, -1 for pads
 constexpr int kRb = kSrc + 512;               // int [128]: query side of the bias offsets
 constexpr int kXch = kRb + 512;               // float [2][128]: second warpgroup's row max and sum
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         live = src >= 0 && (!a.land || __ldg(a.land + (int64_t)b * g.tokens + src) == 0);
       }
       srcs[tid] = src;
-      roff[tid] = ro;
+      roff[tid] = -4 * ro;  // negated byte offset into a bias column
       rbs[tid] = rbase;
       *reinterpret_cast<uint4 *>(smem + kQm + sw32(tid, 0)) = mask_chunk(live, reg, false);
       *reinterpret_cast<uint4 *>(smem + kKm + sw32(tid, 0)) = mask_chunk(live, reg, true);
@@ -415,7 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k < nk) tmem_ld16(tmem + lane_addr + kColS + 16u * (kb0 + k), sv[k]);
           tmem_wait_ld_tied(sv[0], sv[1]);
           tmem_tie(sv[2], sv[3]);
-          const float *bc = bcol + h * g.T + rbs[row];
+          // the row's end of the head's bias column; keys step back by their offsets
+          const uint32_t brow = sbase + kBcol + 4u * (uint32_t)(h * g.T + rbs[row]);
           const int *ro = roff + 16 * kb0;
           float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
@@ -423,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (k < nk) {
 #pragma unroll
               for (int e = 0; e < 16; ++e) {
-                const float x = fmaf(__uint_as_float(sv[k][e]), cs, bc[-ro[16 * k + e]]);
+                const float x = fmaf(__uint_as_float(sv[k][e]), cs, lds_f32(brow + (uint32_t)ro[16 * k + e]));
                 sv[k][e] = __float_as_uint(x);
                 mq[e & 3] = fmaxf(mq[e & 3], x);
               }
