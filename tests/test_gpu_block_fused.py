@@ -30,6 +30,10 @@ CASES = [
     ((4, 16, 32), (2, 8, 8), (1, 4, 4), (0, 0, 1), 8, 1, (0.3, 0.6)),
     ((15, 22), (7, 7), (0, 0), (0, 0), 6, 1, (0.2, 0.2)),
     ((9, 40), (8, 16), (4, 8), (1, 1), 8, 1, None),
+    # every token land: attention contributes nothing, y = x + b_o
+    ((8, 16), (4, 8), (2, 4), (0, 1), 2, 1, (1.0, 1.0)),
+    # windows of 8 slots: the second softmax warpgroup has no keys
+    ((6, 12), (2, 4), (1, 2), (0, 1), 4, 2, (0.3, 0.3)),
 ]
 
 
