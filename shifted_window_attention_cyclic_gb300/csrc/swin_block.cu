@@ -7,24 +7,29 @@
 // X is read (twice: for the LayerNorm and, from L2, for the residual) and Y
 // written.
 //
-// One CTA per SM takes a contiguous range of windows (TERRA Eq. (4)); per
-// window, all 256 threads run the phases in order:
+// One CTA per SM takes a contiguous range of windows (TERRA Eq. (4)), in the
+// plan's spread order; per window, all 256 threads run the phases in order:
 //  * route: slot -> grid token (cyclic shift, ragged edge, pads), region and
 //    land -> the K = 16 mask rows Qm / Km (one extra MMA step adds -2^100 to
 //    every masked logit, as in the attention kernels), key side of the bias
 //    offsets;
-//  * LayerNorm: each slot's X row (two threads per row, 16-byte loads), mean
-//    and biased variance in fp32 from registers, Xn = (x - mean) * rstd *
-//    gamma + beta in bf16 into a 128-byte-swizzled K-major tile;
+//  * LayerNorm: X of a window that is a box of the grid arrives as 5-D TMA
+//    boxes straight into the tile, other windows' rows by 16-byte loads; two
+//    threads per row, mean and biased variance in fp32 from registers, Xn =
+//    (x - mean) * rstd * gamma + beta in bf16 into a 128-byte-swizzled
+//    K-major tile (in place);
 //  * per head h: [Q|K|V]_h = Xn W_qkv,h^T (tcgen05, N = 96, fp32 in TMEM),
 //    + b_qkv, to bf16 tiles; S = Q K^T + mask; softmax over the slot's keys
-//    with the head's bias column (x = S*scale*log2e + bias*log2e, P =
-//    exp2(x - max) in bf16 over S, row sum l); O = P V (A from TMEM);
+//    by both warpgroups (keys 0-63 and 64-127, each its own max, sum and PV
+//    accumulator) with the head's bias column (x = S*scale*log2e +
+//    bias*log2e, P = exp2(x - max) in bf16 over S); O = P V (A from TMEM);
 //    O / l (0 for dead queries) to a bf16 tile; Y += O W_o,h^T (N = C,
 //    accumulated over the heads in TMEM). The next head's W_qkv rows are
-//    fetched by TMA while this head's attention runs; W_o's columns once
-//    the previous head's out-projection has completed.
-//  * epilogue: Y + b_o + X at the slot's token, in bf16 (pads write nothing).
+//    fetched by one 4-D TMA copy while this head's attention runs; W_o's
+//    columns once the previous head's out-projection has completed.
+//  * epilogue: Y + b_o + X at the slot's token, in bf16 (pads write nothing);
+//    for box windows X is reloaded into the tile during the last head and y
+//    leaves as TMA box stores.
 // Every wait is bounded; on timeout all threads leave together (the result
 // of the wait is agreed with a CTA-wide AND), drain the copies and MMAs in
 // flight, free TMEM, and the status word reports the timeout.

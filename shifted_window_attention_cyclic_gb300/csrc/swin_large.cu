@@ -16,8 +16,11 @@
 // in shared memory and every key tile of the window, streamed through two
 // stages, serves both (half the key/value loads per FLOP of one tile per item):
 //  * warp 12 loads the two Q tiles (TMA gather4, two 64-channel halves each)
-//    and writes their query mask rows; warp 13 loads K and writes the key mask
-//    rows and the key side of the bias offsets; warp 14 loads V;
+//    and writes their query mask rows; warps 13 and 8 load K (one channel
+//    half each; 13 also writes the key mask rows and, into a four-slot int16
+//    ring, the key side of the bias offsets with the 16-key chunks whose
+//    offsets step by one marked), warps 14 and 9 load V. A stage's key half
+//    is released after the tile's last S, its value half after its last PV;
 //  * warp 15 issues, per key tile, S_A and S_B = Q K^T + Qm Km^T (8 + 1 MMAs
 //    each, N = 128) into one TMEM buffer per query tile and O_A, O_B += P V
 //    (8 MMAs each), in the order PV_A, S_A of the next tile, PV_B, S_B of the
@@ -28,8 +31,9 @@
 //    the tile's row max (max S * scale*log2e + the head's largest bias); the
 //    running max m is raised to it only when it exceeds m by more than 8 (a
 //    factor 256), O (in TMEM) then rescaled, which is rare; the second pass
-//    forms x = S*scale*log2e + bias*log2e, P = exp2(x - m) <= 256 in bf16
-//    over S and the running sum l. The final O / l uses the same m, so the
+//    forms x = S*scale*log2e + bias*log2e (a marked chunk reads its 16 bias
+//    values at fixed distances from one address), P = exp2(x - m) <= 256 in
+//    bf16 over S and the running sum l. The final O / l uses the same m, so the
 //    result is exact in real arithmetic. After the item's last key tile the
 //    warpgroup itself stores O / l (and the log-sum-exp) at the query tokens.
 // Masked keys (other region, land, pad) get -2^100 from the mask MMA and so

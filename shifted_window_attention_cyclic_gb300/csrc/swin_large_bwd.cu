@@ -8,17 +8,21 @@
 //    the workspace. Sweep 2 recomputes S and dP, forms dS = P (dP - delta) in
 //    bf16 over S in TMEM and accumulates dQ += dS K on the tensor cores
 //    (A from TMEM); the epilogue stores dQ * hd^-1/2 at the query tokens.
+//    Given the forward's output O, delta_kernel first writes delta_i =
+//    sum_c dO_ic O_ic instead and the kernel runs sweep 2 alone.
 //  * bwdkv_kernel, one key tile per item, one sweep over the window's query
 //    tiles with the keys as the MMA rows: S^T = K Q^T + mask and dP^T = V dO^T,
 //    P^T and dS^T (bf16) over them in TMEM, dV += P^T dO and dK += dS^T Q (A
 //    from TMEM, B the query tiles as MN-major operands); the dBias of the
-//    CTA's head accumulates per bias row in shared memory (atomic adds) and
-//    is written to the CTA's workspace slot at head changes; the epilogue
-//    stores dV and dK * hd^-1/2 at the key tokens.
-// delta is the textbook softmax derivative sum, recomputed here rather than
-// taken from the bf16 O (TERRA's FlashAttention-style backward needs O; this
-// one reads neither O nor an fp32 copy of it). Routing, masks and the bias
-// column are those of the forward.
+//    CTA's head accumulates per bias row in shared memory (atomic adds, or
+//    per-diagonal sums where a warp's keys and 16 queries have bias offsets
+//    stepping by one) and is written to the CTA's workspace slot at head
+//    changes; the epilogue stores dV and dK * hd^-1/2 at the key tokens.
+// By default delta is the textbook softmax derivative sum, recomputed from P
+// and dP, so this backward reads neither O nor an fp32 copy of it; the form
+// from O (TERRA's FlashAttention-style backward) saves sweep 1 and carries
+// O's bf16 rounding. Routing, masks and the bias column are those of the
+// forward; whole-row tiles load as 5-D boxes, others as row gathers.
 #include <cuda_bf16.h>
 
 #include "swin_large.cuh"
