@@ -230,11 +230,12 @@ int swin_attn_block_fwd(swin_attn_plan_t plan, const void *x, const float *ln_ga
                         const float *b_o, const float *bias, const uint8_t *land, void *y,
                         swin_stream_t stream);
 
-/* Testing hook for the failure path of the tensor-core kernels. Every wait
- * inside those kernels gives up after `wait_limit_ns` (default 1 s) and then
- * records SWIN_ERR_TIMEOUT in the status word. force_timeout = 1 makes one
- * role of the next launches wait on a barrier that nothing arrives at, so the
- * bounded wait runs out on purpose (the kernel then drains and exits).
+/* Testing hook for the failure path of the tensor-core kernels (the fused
+ * block's included). Every wait inside those kernels gives up after
+ * `wait_limit_ns` (default 1 s) and then records SWIN_ERR_TIMEOUT in the
+ * status word. force_timeout = 1 makes one role of the next launches wait on
+ * a barrier that nothing arrives at, so the bounded wait runs out on purpose
+ * (the kernel then drains and exits).
  * Errors: INVALID_ARG (NULL plan, zero limit, force_timeout not 0/1). */
 int swin_attn_plan_set_debug(swin_attn_plan_t plan, uint64_t wait_limit_ns, int force_timeout);
 

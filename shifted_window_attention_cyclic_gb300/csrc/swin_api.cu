@@ -494,6 +494,7 @@ int swin_attn_block_fwd(swin_attn_plan_t p, const void *x, const float *ln_gamma
   a.items = (int64_t)p->g.batch * p->g.nwin;
   a.ctas = (int)std::min<int64_t>(a.items, (int64_t)p->num_sms);
   a.wait_limit_ns = p->wait_limit_ns;
+  a.debug_force_timeout = p->debug_force_timeout;
   if (a.items == 0) return SWIN_OK;
   return launch_block_fwd(a, w_qkv, w_o, stream);
 }

@@ -66,7 +66,7 @@ constexpr int kRb = kSrc + 512;               // int [128]: query side of the bi
 constexpr int kXch = kRb + 512;               // float [2][128]: second warpgroup's row max and sum
 constexpr int kPar = kXch + 1024;             // float gamma[256], beta[256], b_o[256], b_qkv[768]
 constexpr int kBarOff = kPar + (3 * kMaxC + 3 * kMaxC) * 4;
-constexpr int bW = 0, bWo = 1, bQKV = 2, bS = 3, bO = 4, bY = 5, bDrain = 6, bX = 7, kNumBars = 8;
+constexpr int bW = 0, bWo = 1, bQKV = 2, bS = 3, bO = 4, bY = 5, bDrain = 6, bX = 7, bNever = 8, kNumBars = 9;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem slot, abort flag
 constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
@@ -228,6 +228,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     load_wo(0);
   }
 
+  // testing hook: the bounded wait runs out on a barrier nothing arrives at
+  if (a.debug_force_timeout) ok = cta_wait(bNever, 0, true);
   for (int64_t it = 0; ok && it < count; ++it) {
     const int64_t item = L + it;
     // windows in the plan's spread order (the i-th is (i * wstep) mod nwin):

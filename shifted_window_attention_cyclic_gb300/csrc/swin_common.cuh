@@ -261,6 +261,7 @@ struct BlockArgs {
   int64_t items;  // windows (batch * nwin)
   int ctas;
   uint64_t wait_limit_ns;
+  int debug_force_timeout;  // testing hook: every thread first waits on a barrier nothing arrives at
 };
 
 // Launchers implemented in the kernel translation units.

@@ -74,3 +74,35 @@ def test_debug_hook_rejects_bad_arguments():
     assert lib.swin_attn_plan_set_debug(attn.plan.handle, 0, 0) == C.SWIN_ERR_INVALID_ARG
     assert lib.swin_attn_plan_set_debug(attn.plan.handle, 10, 2) == C.SWIN_ERR_INVALID_ARG
     assert lib.swin_attn_plan_set_debug(None, 10, 0) == C.SWIN_ERR_INVALID_ARG
+
+
+def test_forced_wait_timeout_in_fused_block_is_reported_and_recoverable():
+    """The fused block kernel (LayerNorm + QKV, SW-MSA, out-projection): every
+    thread waits on the barrier nothing arrives at, the CTA agrees on the
+    failure, drains the weight copies in flight, frees TMEM and exits; the
+    plan then runs the block normally and meets the block oracle."""
+    from oracle import block as oblock
+    from shifted_window_attention_cyclic_gb300 import swin_attn as C
+    from shifted_window_attention_cyclic_gb300.functional import SwinWindowAttention
+    wl = workloads.custom((13, 27), (4, 8), (2, 4), (0, 1), 2, 32, 1, "bf16", (0.3, 0.3), seed_index=93)
+    xb = workloads.generate_block(wl)
+    attn = SwinWindowAttention(wl.grid, wl.window, wl.shift, wl.periodic, wl.heads, wl.head_dim, wl.batch,
+                               wl.dtype, wl.has_land, "tc")
+    dev = torch.device("cuda", 0)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf = lambda a: f32(a).to(torch.bfloat16)
+    args = (bf(xb["x"]), f32(xb["gamma"]), f32(xb["beta"]), bf(xb["w_qkv"]), f32(xb["b_qkv"]), bf(xb["w_o"]),
+            f32(xb["b_o"]), f32(xb["bias"]), f32(xb["land"]))
+    C.swin_attn_plan_set_debug(attn.plan, 5_000_000, 1)  # 5 ms limit, forced wait
+    attn.block_forward(*args)
+    assert C.swin_attn_status(attn.plan) == C.SWIN_ERR_TIMEOUT
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK  # status word was cleared
+    C.swin_attn_plan_set_debug(attn.plan, 1_000_000_000, 0)
+    y = attn.block_forward(*args)
+    torch.cuda.synchronize()
+    assert C.swin_attn_status(attn.plan) == C.SWIN_OK
+    ref, _ = oblock.block_fwd(problem_of(wl), xb["x"], xb["gamma"], xb["beta"], 1e-5, xb["w_qkv"], xb["b_qkv"],
+                              xb["w_o"], xb["b_o"], xb["bias"], xb["land"])
+    got = host(y)
+    assert np.isfinite(got).all()
+    assert (np.abs(got - ref) <= 2e-2 + 2.0 ** -8 * np.abs(ref)).all()
