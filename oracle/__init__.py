@@ -118,6 +118,9 @@ def _load():
                                                                         ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_bwd.argtypes = [P(_Desc)] + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + [ctypes.c_void_p] * 4
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_route.argtypes = [P(_Desc), ctypes.c_void_p, ctypes.c_int64] + [ctypes.c_void_p] * 3
+        lib.oracle_query_rows.argtypes = [P(_Desc)] + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + [ctypes.c_void_p] * 3
+        lib.oracle_key_rows.argtypes = [P(_Desc)] + [ctypes.c_void_p] * 7 + [ctypes.c_int64] + [ctypes.c_void_p] * 2
         _lib = lib
     return _lib
 
@@ -226,3 +229,58 @@ def bwd(pb: Problem, q, k, v, bias, land, dout):
             "dk": scatter_windows(pb, g["dk"], win_src).reshape(shape),
             "dv": scatter_windows(pb, g["dv"], win_src).reshape(shape),
             "dbias": g["dbias"]}
+
+
+# ---- sampled rows: windows too large for the per-window form ----------------
+
+def _tokens(pb, tokens):
+    t = np.ascontiguousarray(tokens, dtype=np.int64).reshape(-1)
+    if t.size and (t.min() < 0 or t.max() >= pb.batch * pb.tokens):
+        raise ValueError("token index out of range")
+    return t
+
+
+def route(pb: Problem, tokens):
+    """Window (global id b*nwin + w), slot and region bits of flat tokens b*N + t."""
+    t = _tokens(pb, tokens)
+    gid = np.empty(t.size, np.int64)
+    slot = np.empty(t.size, np.int32)
+    reg = np.empty(t.size, np.int32)
+    d = pb._c()
+    rc = _load().oracle_route(ctypes.byref(d), _ptr(t), t.size, _ptr(gid), _ptr(slot), _ptr(reg))
+    if rc:
+        raise ValueError("oracle_route failed: %d" % rc)
+    return gid, slot, reg
+
+
+def query_rows(pb: Problem, q, k, v, bias, land, tokens, dout=None):
+    """O [m, C], LSE [m, heads] and, given dout, dQ [m, C] (fp64) of the query
+    tokens listed by flat index b*N + t, each from its whole window; no n x n
+    matrix is formed. Returns (o, lse, dq or None)."""
+    t = _tokens(pb, tokens)
+    o = np.zeros((t.size, pb.channels), np.float64)
+    lse = np.zeros((t.size, pb.heads), np.float64)
+    dq = np.zeros((t.size, pb.channels), np.float64) if dout is not None else None
+    q, k, v, bias, dout = _f32(q), _f32(k), _f32(v), _f32(bias), _f32(dout)
+    d = pb._c()
+    rc = _load().oracle_query_rows(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(_land(pb, land)),
+                                   _ptr(dout), _ptr(t), t.size, _ptr(o), _ptr(lse), _ptr(dq))
+    if rc:
+        raise ValueError("oracle_query_rows failed: %d" % rc)
+    return o, lse, dq
+
+
+def key_rows(pb: Problem, q, k, v, bias, land, dout, tokens):
+    """dK [m, C] and dV [m, C] (fp64) of the tokens listed by flat index as
+    keys. Costs O(n_r^2 hd) per (window, head), n_r the queries of the listed
+    keys' regions in that window."""
+    t = _tokens(pb, tokens)
+    dk = np.zeros((t.size, pb.channels), np.float64)
+    dv = np.zeros((t.size, pb.channels), np.float64)
+    q, k, v, bias, dout = _f32(q), _f32(k), _f32(v), _f32(bias), _f32(dout)
+    d = pb._c()
+    rc = _load().oracle_key_rows(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(_land(pb, land)),
+                                 _ptr(dout), _ptr(t), t.size, _ptr(dk), _ptr(dv))
+    if rc:
+        raise ValueError("oracle_key_rows failed: %d" % rc)
+    return dk, dv

@@ -466,6 +466,267 @@ int oracle_bwd(const oracle_desc *d, const float *q, const float *k,
   return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
 }
 
+/* ---- sampled rows, for windows too large for the per-window form --------
+ * One query's attention depends on its own window alone, so the quantities of
+ * oracle_fwd / oracle_bwd can be had token by token without any n x n
+ * matrix (memory O(n) per thread). Tokens are listed by their flat index
+ * b*N + t; outputs are rows in the order listed.
+ *
+ * oracle_route: window, slot and region bits of each listed token (the
+ * token-side route above).
+ */
+int oracle_route(const oracle_desc *d, const int64_t *tok, int64_t n_tok,
+                 int64_t *gid, int32_t *slot, int32_t *reg) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  int64_t N = tokens_per_image(d), nw = windows_per_image(d);
+  for (int64_t x = 0; x < n_tok; ++x) {
+    if (tok[x] < 0 || tok[x] >= d->batch * N) return ORACLE_BAD_ARG;
+    int64_t w;
+    int s, r;
+    route_token(d, tok[x] % N, &w, &s, &r);
+    if (gid) gid[x] = (tok[x] / N) * nw + w;
+    if (slot) slot[x] = s;
+    if (reg) reg[x] = r;
+  }
+  return ORACLE_OK;
+}
+
+/* Logits of query slot i against every slot of its window for head h:
+ * s[j] = scale q_i.k_j + bias(i, j) for visible keys, -inf otherwise.
+ * Returns the log-sum-exp over the visible keys (-inf if there is none). */
+static double query_logits(const oracle_desc *d, const window_view *wv,
+                           const float *q, const float *k, const float *bias,
+                           int64_t img_off, int h, int i, double *s) {
+  int n = wv->n, hd = d->head_dim, C = d->heads * d->head_dim, H = d->heads;
+  double scale = 1.0 / sqrt((double)hd), m = -INFINITY;
+  const float *qi = q + (img_off + wv->src[i]) * C + (int64_t)h * hd;
+  for (int j = 0; j < n; ++j) {
+    s[j] = -INFINITY;
+    if (!visible(wv, i, j)) continue;
+    const float *kj = k + (img_off + wv->src[j]) * C + (int64_t)h * hd;
+    double dot = 0.0;
+    for (int c = 0; c < hd; ++c) dot += (double)qi[c] * (double)kj[c];
+    s[j] = scale * dot + (double)bias[(int64_t)rel_row(d, i, j) * H + h];
+    if (s[j] > m) m = s[j];
+  }
+  if (m == -INFINITY) return -INFINITY;
+  double l = 0.0;
+  for (int j = 0; j < n; ++j)
+    if (s[j] != -INFINITY) l += exp(s[j] - m);
+  return m + log(l);
+}
+
+/* delta_i = sum_j P_ij dP_ij, dP_ij = dout_i . v_j, over the visible keys
+ * whose logits are in s (P_ij = exp(s[j] - lse)). */
+static double query_delta(const oracle_desc *d, const window_view *wv,
+                          const float *v, const float *dout, int64_t img_off,
+                          int h, int i, const double *s, double lse) {
+  int n = wv->n, hd = d->head_dim, C = d->heads * d->head_dim;
+  const float *go = dout + (img_off + wv->src[i]) * C + (int64_t)h * hd;
+  double delta = 0.0;
+  for (int j = 0; j < n; ++j) {
+    if (s[j] == -INFINITY) continue;
+    const float *vj = v + (img_off + wv->src[j]) * C + (int64_t)h * hd;
+    double dp = 0.0;
+    for (int c = 0; c < hd; ++c) dp += (double)go[c] * (double)vj[c];
+    delta += exp(s[j] - lse) * dp;
+  }
+  return delta;
+}
+
+/* Query rows: for each listed token, O [n_tok][C], LSE [n_tok][heads]
+ * (natural log; -inf for land) and, when dout and dq_rows are given,
+ * dQ [n_tok][C] = scale sum_j P_ij (dP_ij - delta_i) k_j. Land tokens get
+ * zero rows. lse_rows and dq_rows may be NULL. */
+int oracle_query_rows(const oracle_desc *d, const float *q, const float *k,
+                      const float *v, const float *bias, const uint8_t *land,
+                      const float *dout, const int64_t *tok, int64_t n_tok,
+                      double *o_rows, double *lse_rows, double *dq_rows) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  if (!q || !k || !v || !bias || !tok || !o_rows) return ORACLE_BAD_ARG;
+  if (d->has_land && !land) return ORACLE_BAD_ARG;
+  if (dq_rows && !dout) return ORACLE_BAD_ARG;
+  int64_t N = tokens_per_image(d), nw = windows_per_image(d);
+  for (int64_t x = 0; x < n_tok; ++x)
+    if (tok[x] < 0 || tok[x] >= d->batch * N) return ORACLE_BAD_ARG;
+  int n = slots_per_window(d), H = d->heads, hd = d->head_dim, C = H * hd;
+  double scale = 1.0 / sqrt((double)hd);
+  window_tables t;
+  if (load_tables(d, &t)) {
+    free_tables(&t);
+    return ORACLE_NO_MEMORY;
+  }
+  int failed = 0;
+#pragma omp parallel
+  {
+    double *s = (double *)malloc(sizeof(double) * n);
+    uint8_t *lnd = (uint8_t *)malloc((size_t)n);
+    if (!s || !lnd) {
+#pragma omp atomic write
+      failed = 1;
+    } else {
+#pragma omp for schedule(dynamic, 1)
+      for (int64_t it = 0; it < n_tok * H; ++it) {
+        int64_t x = it / H;
+        int h = (int)(it % H);
+        int64_t b = tok[x] / N, w;
+        int i, reg;
+        route_token(d, tok[x] % N, &w, &i, &reg);
+        window_view wv;
+        make_view(d, &t, land, b * nw + w, lnd, &wv);
+        double *oi = o_rows + x * C + (int64_t)h * hd;
+        double *gq = dq_rows ? dq_rows + x * C + (int64_t)h * hd : NULL;
+        for (int c = 0; c < hd; ++c) {
+          oi[c] = 0.0;
+          if (gq) gq[c] = 0.0;
+        }
+        if (wv.lnd[i]) {
+          if (lse_rows) lse_rows[x * H + h] = -INFINITY;
+          continue;
+        }
+        double lse = query_logits(d, &wv, q, k, bias, b * N, h, i, s);
+        if (lse_rows) lse_rows[x * H + h] = lse;
+        for (int j = 0; j < n; ++j) {
+          if (s[j] == -INFINITY) continue;
+          double p = exp(s[j] - lse);
+          const float *vj = v + (b * N + wv.src[j]) * C + (int64_t)h * hd;
+          for (int c = 0; c < hd; ++c) oi[c] += p * (double)vj[c];
+        }
+        if (!gq) continue;
+        double delta = query_delta(d, &wv, v, dout, b * N, h, i, s, lse);
+        const float *go = dout + (b * N + wv.src[i]) * C + (int64_t)h * hd;
+        for (int j = 0; j < n; ++j) {
+          if (s[j] == -INFINITY) continue;
+          const float *vj = v + (b * N + wv.src[j]) * C + (int64_t)h * hd;
+          const float *kj = k + (b * N + wv.src[j]) * C + (int64_t)h * hd;
+          double dp = 0.0;
+          for (int c = 0; c < hd; ++c) dp += (double)go[c] * (double)vj[c];
+          double ds = exp(s[j] - lse) * (dp - delta);
+          for (int c = 0; c < hd; ++c) gq[c] += scale * ds * (double)kj[c];
+        }
+      }
+    }
+    free(s);
+    free(lnd);
+  }
+  free_tables(&t);
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
+/* Key rows: for each listed token as a key, dK [n_tok][C] and dV [n_tok][C]:
+ *   dV_j = sum_i P_ij dout_i,  dK_j = scale sum_i P_ij (dP_ij - delta_i) q_i
+ * over the queries i that see key j (live queries of its window with its
+ * region bits). These need the LSE and delta of every such query, so the
+ * work is O(n_r^2 hd) per (window, head) for a window whose sampled keys'
+ * regions hold n_r queries. Land tokens get zero rows. Either output may be
+ * NULL. */
+int oracle_key_rows(const oracle_desc *d, const float *q, const float *k,
+                    const float *v, const float *bias, const uint8_t *land,
+                    const float *dout, const int64_t *tok, int64_t n_tok,
+                    double *dk_rows, double *dv_rows) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  if (!q || !k || !v || !bias || !dout || !tok) return ORACLE_BAD_ARG;
+  if (d->has_land && !land) return ORACLE_BAD_ARG;
+  int64_t N = tokens_per_image(d), nw = windows_per_image(d);
+  for (int64_t x = 0; x < n_tok; ++x)
+    if (tok[x] < 0 || tok[x] >= d->batch * N) return ORACLE_BAD_ARG;
+  int n = slots_per_window(d), H = d->heads, hd = d->head_dim, C = H * hd;
+  double scale = 1.0 / sqrt((double)hd);
+  window_tables t;
+  if (load_tables(d, &t)) {
+    free_tables(&t);
+    return ORACLE_NO_MEMORY;
+  }
+  int64_t *gid = (int64_t *)malloc(sizeof(int64_t) * (n_tok > 0 ? n_tok : 1));
+  int *slot = (int *)malloc(sizeof(int) * (n_tok > 0 ? n_tok : 1));
+  double *lse = (double *)malloc(sizeof(double) * n);
+  double *delta = (double *)malloc(sizeof(double) * n);
+  uint8_t *lnd = (uint8_t *)malloc((size_t)n);
+  uint8_t *done = (uint8_t *)calloc((size_t)(n_tok > 0 ? n_tok : 1), 1);
+  int failed = !gid || !slot || !lse || !delta || !lnd || !done;
+  for (int64_t x = 0; !failed && x < n_tok; ++x) {
+    int64_t w;
+    int reg;
+    route_token(d, tok[x] % N, &w, &slot[x], &reg);
+    gid[x] = (tok[x] / N) * nw + w;
+    for (int c = 0; c < C; ++c) {
+      if (dk_rows) dk_rows[x * C + c] = 0.0;
+      if (dv_rows) dv_rows[x * C + c] = 0.0;
+    }
+  }
+  /* one window at a time: the window of the first key not yet done */
+  for (int64_t x0 = 0; !failed && x0 < n_tok; ++x0) {
+    if (done[x0]) continue;
+    int64_t g = gid[x0], b = g / nw;
+    window_view wv;
+    make_view(d, &t, land, g, lnd, &wv);
+    /* regions of this window's listed keys */
+    int need[8] = {0};
+    for (int64_t x = x0; x < n_tok; ++x)
+      if (gid[x] == g && wv.src[slot[x]] >= 0) need[wv.reg[slot[x]] & 7] = 1;
+    for (int h = 0; h < H && !failed; ++h) {
+      /* LSE and delta of every live query of those regions */
+#pragma omp parallel
+      {
+        double *s = (double *)malloc(sizeof(double) * n);
+        if (!s) {
+#pragma omp atomic write
+          failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 16)
+          for (int i = 0; i < n; ++i) {
+            lse[i] = -INFINITY;
+            delta[i] = 0.0;
+            if (wv.src[i] < 0 || wv.lnd[i] || !need[wv.reg[i] & 7]) continue;
+            lse[i] = query_logits(d, &wv, q, k, bias, b * N, h, i, s);
+            delta[i] = query_delta(d, &wv, v, dout, b * N, h, i, s, lse[i]);
+          }
+        }
+        free(s);
+      }
+      if (failed) break;
+      /* each listed key of this window, against every query that sees it */
+#pragma omp parallel for schedule(dynamic, 1)
+      for (int64_t x = x0; x < n_tok; ++x) {
+        if (gid[x] != g) continue;
+        int j = slot[x];
+        double *gk = dk_rows ? dk_rows + x * C + (int64_t)h * hd : NULL;
+        double *gv = dv_rows ? dv_rows + x * C + (int64_t)h * hd : NULL;
+        const float *kj = k + (b * N + wv.src[j]) * C + (int64_t)h * hd;
+        const float *vj = v + (b * N + wv.src[j]) * C + (int64_t)h * hd;
+        for (int i = 0; i < n; ++i) {
+          if (lse[i] == -INFINITY || !visible(&wv, i, j)) continue;
+          const float *qi = q + (b * N + wv.src[i]) * C + (int64_t)h * hd;
+          const float *go = dout + (b * N + wv.src[i]) * C + (int64_t)h * hd;
+          double dot = 0.0, dp = 0.0;
+          for (int c = 0; c < hd; ++c) {
+            dot += (double)qi[c] * (double)kj[c];
+            dp += (double)go[c] * (double)vj[c];
+          }
+          double p = exp(scale * dot + (double)bias[(int64_t)rel_row(d, i, j) * H + h] - lse[i]);
+          for (int c = 0; c < hd; ++c) {
+            if (gv) gv[c] += p * (double)go[c];
+            if (gk) gk[c] += scale * p * (dp - delta[i]) * (double)qi[c];
+          }
+        }
+      }
+    }
+    for (int64_t x = x0; x < n_tok; ++x)
+      if (gid[x] == g) done[x] = 1;
+  }
+  free(gid);
+  free(slot);
+  free(lse);
+  free(delta);
+  free(lnd);
+  free(done);
+  free_tables(&t);
+  return failed ? ORACLE_NO_MEMORY : ORACLE_OK;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
