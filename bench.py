@@ -63,7 +63,7 @@ def workload_counts(wl, win_src, land, lse_written=True):
     fwd_flop = 4.0 * wl.batch * float((n_real ** 2).sum()) * C
     bwd_flop = 2.5 * fwd_flop
     land_b = N if land is not None else 0
-    bias_b = rows * H * 4
+    bias_b = rows * H * 4 if wl.bias else 0
     lse_b = 4 * N * H
     fwd_bytes = 4 * N * C * e + (lse_b if lse_written else 0) + land_b + bias_b
     bwd_bytes = 8 * N * C * e + 2 * lse_b + land_b + 2 * bias_b
@@ -81,8 +81,12 @@ def roof_us(flop, nbytes, peaks):
 TARGETS = {"tiny_fp32": None, "grid1deg": {"fwd": 0.50}, "ragged": {"fwd": 0.50, "bwd": 0.35},
            "eddy_ocean": {"fwd": 0.50, "bwd": 0.35}, "depth3d": {"fwd": 0.50, "bwd": 0.35}}
 # timed beside the five configurations (no bar of its own): the large-window regime
-EXTRA = ["terra_w32"]
+EXTRA = ["terra_w32", "beast_w64k"]
+# launches of one of these take a large part of a second: fewer repetitions
+EXTRA_REPS = {"beast_w64k": (5, 2)}
 NOTES = {"terra_w32": "windows of 1 024 tokens, head_dim 128: key-tiled tcgen05 kernels; tensor-bound",
+         "beast_w64k": "windows of 64 800 tokens (507 key tiles), head_dim 128, no bias: key-tiled tcgen05 kernels; "
+                       "tensor-bound; FLOPs count every pair of real slots of a window (regions included)",
          "tiny_fp32": "fp32 SIMT path, 512 tokens: launch-bound, parity only",
          "grid1deg": "forward only (inference: no LSE written, its bytes not counted)",
          "eddy_ocean": "not ragged: 256 = 32 x 8 rows divide into 8-row windows; irregular through the land mask"}
@@ -104,12 +108,12 @@ def time_config(wl, x, peaks, flush, reps=50, warmup=10, kernels="auto"):
                                                                          lse_written=wl.backward)
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
     d = {k_: torch.from_numpy(x[k_]).to(dev).to(tdt) for k_ in ("q", "k", "v", "dout")}
-    bias = torch.from_numpy(x["bias"]).to(dev)
+    bias = torch.from_numpy(x["bias"]).to(dev) if wl.bias else None
     land = torch.from_numpy(x["land"]).to(dev) if x["land"] is not None else None
     o = torch.empty(attn.shape, dtype=tdt, device=dev)
     lse = torch.empty(attn.lse_shape, dtype=torch.float32, device=dev)
     dq, dk, dv = (torch.empty(attn.shape, dtype=tdt, device=dev) for _ in range(3))
-    dbias = attn.new_bias()
+    dbias = attn.new_bias() if wl.bias else None
     ws = attn.workspace()
     stream = torch.cuda.current_stream()
     fwd_t, bwd_t, bwdo_t = [], [], []
@@ -569,7 +573,8 @@ def config_of(wl):
     tensor_mb = wl.batch * wl.tokens * wl.channels * (2 if wl.dtype == "bf16" else 4) / 1e6
     return {"workload": "%s: B=%d grid %s C=%d heads %dx%d window %s shift %s periodic %s land p %s %s" %
                         (wl.name, wl.batch, "x".join(map(str, wl.grid)), wl.channels, wl.heads, wl.head_dim,
-                         "x".join(map(str, wl.window)), tuple(wl.shift), tuple(wl.periodic), wl.land_p, wl.dtype),
+                         "x".join(map(str, wl.window)), tuple(wl.shift), tuple(wl.periodic), wl.land_p, wl.dtype)
+                        + ("" if wl.bias else " no bias"),
             "global_batch": wl.batch, "tokens_per_batch": wl.batch * wl.tokens,
             "parallelism": "replicas (independent problem per GPU)",
             "l2": ("inputs larger than L2 (each tensor %.0f MB > 129 MB), no flush" if tensor_mb > 129 else
@@ -773,7 +778,8 @@ def main():
         for name in list(TARGETS) + EXTRA:
             cwl = workloads.WORKLOADS[name]
             cx = x if name == wl.name else workloads.generate(cwl)
-            configs[name] = time_config(cwl, cx, peaks, flush, reps=args.config_reps, warmup=10)
+            reps, warm = EXTRA_REPS.get(name, (args.config_reps, 10))
+            configs[name] = time_config(cwl, cx, peaks, flush, reps=min(reps, args.config_reps), warmup=warm)
             configs[name]["config"] = config_of(cwl)["workload"]
         # the W-MSA + SW-MSA pair on the eddy-resolving ocean grid (TERRA's Wenhai stand-in)
         configs["block_pair_eddy_ocean"] = time_pair(workloads.WORKLOADS["eddy_ocean"], peaks, flush,

@@ -46,6 +46,7 @@ class Workload:
     head_dim: int
     land_p: tuple | None  # None = no land; else (p at level 0, p at last level)
     backward: bool
+    bias: bool = True     # False: the attention runs without a relative-position bias (NULL bias)
 
     @property
     def has_land(self):
@@ -79,6 +80,14 @@ WORKLOADS = {
                           True),
     # half of depth3d (8 levels, same window/shift/land recipe): the profiling
     # case for ncu captures, still larger than L2 (302 MB per tensor)
+    # BEAST's outer windows: [360, 180] lat x lon = 64 800 tokens per window,
+    # heads of 128 channels (BEAST page, model-configuration table), on a
+    # 720 x 720 grid (two lat windows, four lon windows wrapping the periodic
+    # lon seam, shift (180, 90); lat window 1 splits in two regions) with 2 of
+    # the configuration's 16 heads. No relative-position bias: the page runs
+    # these windows through FlashAttention / cuDNN attention.
+    "beast_w64k": Workload("beast_w64k", 7, "bf16", 1, (720, 720), (360, 180), (180, 90), (0, 1), 2, 128, None,
+                           True, bias=False),
     "depth3d_8lvl": Workload("depth3d_8lvl", 5, "bf16", 1, (8, 192, 384), (2, 8, 8), (1, 4, 4), (0, 0, 1), 8, 32,
                              (0.3, 0.6), True),
 }
