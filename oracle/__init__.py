@@ -133,14 +133,15 @@ def num_threads() -> int:
     return _load().oracle_num_threads()
 
 
-def tables(pb: Problem):
+def tables(pb: Problem, with_relidx: bool = True):
     """Routing tables of one image: (win_src [nwin, n] int32 with -1 pads,
-    region [nwin, n] uint8, tok_dst [N] int32, relidx [n, n] int32)."""
+    region [nwin, n] uint8, tok_dst [N] int32, relidx [n, n] int32, or None
+    when with_relidx is false: n x n entries are too many for large windows)."""
     lib = _load()
     win_src = np.empty((pb.nwin, pb.slots), np.int32)
     region = np.empty((pb.nwin, pb.slots), np.uint8)
     tok_dst = np.empty((pb.tokens,), np.int32)
-    relidx = np.empty((pb.slots, pb.slots), np.int32)
+    relidx = np.empty((pb.slots, pb.slots), np.int32) if with_relidx else None
     d = pb._c()
     rc = lib.oracle_tables(ctypes.byref(d), _ptr(win_src), _ptr(region), _ptr(tok_dst), _ptr(relidx))
     if rc:
