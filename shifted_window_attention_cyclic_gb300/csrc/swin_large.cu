@@ -55,6 +55,11 @@ constexpr int kStageBytes = 68 * 1024;
 // the key tiles: slot t mod 4 is rewritten with key tile t + 4, which cannot
 // start before the softmax of tile t has finished (see the barriers below)
 constexpr int kRoffSlots = 4;
+// Key/value tiles load their 16-slot runs as boxes only in windows of at
+// least this many key tiles: measured faster there (64 800-slot windows,
+// 507 tiles: -16 % forward time) and slower in windows of 43-128 tiles
+// (+2-7 %), where row gathers alone are used.
+constexpr int kRunMinKeyTiles = 256;
 constexpr int kRoff = kStage0 + kStages * kStageBytes;
 constexpr int kBcol = kRoff + kRoffSlots * 256;  // bias column of the current head (bias*log2e)
 constexpr int kMaxBiasRows = 4096;
@@ -96,6 +101,9 @@ __device__ __forceinline__ LItem decode_pair(const Geo &g, int64_t it) {
   return x;
 }
 
+// kRuns: key/value tiles load 16-slot runs as boxes (windows of at least
+// kRunMinKeyTiles key tiles); otherwise every row by gather4.
+template <bool kRuns>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_large_kernel(const FwdArgs a, const __grid_constant__ TileMaps tmq, const __grid_constant__ TileMaps tmk,
                      const __grid_constant__ TileMaps tmv) {
@@ -172,10 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows_b = has_b ? min(128, g.n - (x.qt + 1) * 128) : 0, nqb = (rows_b + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(bQFull), (uint32_t)(nqa + nqb) * 1024u);
       __syncwarp();
-      // row gathers (measured faster here than tile boxes, unlike in the backward)
-      const int cz[3] = {0, 0, 0};
-      load_tile(sbase + kQA, &tmq, false, cz, qa, x.b, g.tokens, x.h, lane, nqa, bar(bQFull));
-      if (has_b) load_tile(sbase + kQB, &tmq, false, cz, qb, x.b, g.tokens, x.h, lane, nqb, bar(bQFull));
+      // row gathers (measured faster here than tile boxes or 16-slot runs, unlike in the backward)
+      const Run16 rows_only{false, {0, 0, 0}};
+      for (int hf = 0; hf < 2; ++hf)
+        load_half(sbase + kQA + hf * kHalfBytes, &tmq, rows_only, qa, x.b, g.tokens, x.h, hf, lane, nqa, bar(bQFull));
+      for (int hf = 0; has_b && hf < 2; ++hf)
+        load_half(sbase + kQB + hf * kHalfBytes, &tmq, rows_only, qb, x.b, g.tokens, x.h, hf, lane, nqb, bar(bQFull));
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         *reinterpret_cast<uint4 *>(smem + kQmA + sw32(4 * lane + j, 0)) = mask_chunk(la[j], qa.reg[j], false);
@@ -204,13 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = min(128, g.n - kt * 128), nq4 = (rows + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(full_b + s), (uint32_t)nq4 * 512u);
       __syncwarp();
-      if (lane < nq4) {
-        // rows 4*lane .. 4*lane+3 of this warp's channel half (pads read token 0 of the image)
-        const CUtensorMap *m = kw ? &tmk.rows : &tmv.rows;
+      // this warp's channel half of the tile rows (pads read token 0): 16-slot
+      // runs along the grid's last dimension as boxes, other rows by gather4
+      if constexpr (kRuns) {
+        const Run16 run = run16(g, q, lane);
+        load_half(st + (kw ? kK : kV) + half * kHalfBytes, kw ? &tmk : &tmv, run, q, x.b, g.tokens, x.h, half, lane,
+                  nq4, bar(full_b + s));
+      } else if (lane < nq4) {
         const int r0 = x.b * g.tokens;
-        tma_gather4(st + (kw ? kK : kV) + half * kHalfBytes + 512u * lane, m, x.h * kHd + 64 * half,
-                    r0 + max(q.src[0], 0), r0 + max(q.src[1], 0), r0 + max(q.src[2], 0), r0 + max(q.src[3], 0),
-                    bar(full_b + s));
+        tma_gather4(st + (kw ? kK : kV) + half * kHalfBytes + 512u * lane, kw ? &tmk.rows : &tmv.rows,
+                    x.h * kHd + 64 * half, r0 + max(q.src[0], 0), r0 + max(q.src[1], 0), r0 + max(q.src[2], 0),
+                    r0 + max(q.src[3], 0), bar(full_b + s));
       }
       if (meta) {
 #pragma unroll
@@ -542,10 +556,11 @@ int launch_fwd_large(const FwdArgs &a, void *stream) {
   lg::TileMaps mq, mk, mv;
   if (!lg::tile_maps(&mq, a.q, a.g) || !lg::tile_maps(&mk, a.k, a.g) || !lg::tile_maps(&mv, a.v, a.g))
     return SWIN_ERR_CUDA;
-  if (cudaFuncSetAttribute(lg::fwd_large_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lg::kSmemBytes) !=
+  auto kern = a.g.nqt >= lg::kRunMinKeyTiles ? lg::fwd_large_kernel<true> : lg::fwd_large_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lg::kSmemBytes) !=
       cudaSuccess)
     return SWIN_ERR_CUDA;
-  lg::fwd_large_kernel<<<a.ctas, lg::kThreads, lg::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mk, mv);
+  kern<<<a.ctas, lg::kThreads, lg::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(a, mq, mk, mv);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
 }
 

@@ -124,8 +124,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       int c[3];
       const bool box = tile_box(g, x.omega, x.qt, c);
-      load_tile(sbase + kQ, &tmq, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bQFull));
-      load_tile(sbase + kdO, &tmdo, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bQFull));
+      load_tile(sbase + kQ, &tmq, g, box, c, q, x.b, x.h, lane, nq4, bar(bQFull));
+      load_tile(sbase + kdO, &tmdo, g, box, c, q, x.b, x.h, lane, nq4, bar(bQFull));
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         *reinterpret_cast<uint4 *>(smem + kQm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], false);
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       int c[3];
       const bool box = tile_box(g, x.omega, kt, c);
-      load_tile(st + (kw ? kK : kV), kw ? &tmk : &tmv, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bFull + s));
+      load_tile(st + (kw ? kK : kV), kw ? &tmk : &tmv, g, box, c, q, x.b, x.h, lane, nq4, bar(bFull + s));
       if (kw) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -395,24 +395,40 @@ constexpr int kStage = kKm + kMaskBytes;                         // one query-ti
 constexpr int kQ = 0, kdO = kTileBytes, kQm = 2 * kTileBytes, kLse = kQm + kMaskBytes, kDelta = kLse + 512,
               kRbase = kDelta + 512;
 constexpr int kStageBytes = 70 * 1024;
-constexpr int kBcol = kStage + kStageBytes;
 constexpr int kMaxBiasRows = 8192;
-constexpr int kBacc = kBcol + kMaxBiasRows * 4;  // float dBias accumulator of the current head
-// float [8 warps][32 keys][17]: one warp's dS of 16 queries, staged for the diagonal sums
-constexpr int kDiag = kBacc + kMaxBiasRows * 4;
-constexpr int kBarOff = kDiag + 8 * 32 * 17 * 4;
-constexpr int bKVFull = 0, bKVFree = 1, bFull = 2, bEmpty = 3, bSFull = 4, bPFull = 5, bDKVFull = 6, bTFree = 7,
-              bNever = 8, bDrain = 9, bBsync = 10, kNumBars = 11;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;
-constexpr int kSmemBytes = kMiscOff + 16 + 1024;
 static_assert(kStage % 1024 == 0 && kStageBytes % 1024 == 0 && kRbase + 512 <= kStageBytes, "layout");
-static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
+// Shared memory with kQS query-tile stages. One stage leaves room for the
+// head's bias column, the dBias accumulator and the diagonal-sum scratch; two
+// stages (a launch with neither bias nor dBias) load the next query tile
+// while this one is computed.
+template <int kQS>
+struct Lay {
+  static constexpr int kBcol = kStage + kQS * kStageBytes;
+  static constexpr int kBacc = kBcol + kMaxBiasRows * 4;  // float dBias accumulator of the current head
+  // float [8 warps][32 keys][17]: one warp's dS of 16 queries, staged for the diagonal sums
+  static constexpr int kDiag = kBacc + kMaxBiasRows * 4;
+  static constexpr int kBarOff = kQS == 1 ? kDiag + 8 * 32 * 17 * 4 : kStage + kQS * kStageBytes;
+  // stage s: bFull + s (its query tile landed), bEmpty + s (its MMAs are done)
+  static constexpr int bKVFull = 0, bKVFree = 1, bFull = 2, bEmpty = bFull + kQS, bSFull = bEmpty + kQS,
+                       bPFull = bSFull + 1, bDKVFull = bSFull + 2, bTFree = bSFull + 3, bNever = bSFull + 4,
+                       bDrain = bSFull + 5, bBsync = bSFull + 6, kNumBars = bSFull + 7;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+  static_assert(kSmemBytes <= 232448, "over the 227 KB of shared memory a CTA may use");
+};
 constexpr int kKVWarp = 12, kQWarp = 13, kdOWarp = 14;
 constexpr uint32_t kColS = 0, kColdP = 128, kColdV = 256, kColdK = 384;
 
+template <int kQS>
 __global__ void __launch_bounds__(kThreads, 1)
     bwdkv_kernel(const BwdArgs a, const __grid_constant__ TileMaps tmq, const __grid_constant__ TileMaps tmk,
                  const __grid_constant__ TileMaps tmv, const __grid_constant__ TileMaps tmdo) {
+  using L_ = Lay<kQS>;
+  constexpr int kBcol = L_::kBcol, kBacc = L_::kBacc, kDiag = L_::kDiag, kBarOff = L_::kBarOff,
+                kMiscOff = L_::kMiscOff;
+  constexpr int bKVFull = L_::bKVFull, bKVFree = L_::bKVFree, bFull = L_::bFull, bEmpty = L_::bEmpty,
+                bSFull = L_::bSFull, bPFull = L_::bPFull, bDKVFull = L_::bDKVFull, bTFree = L_::bTFree,
+                bNever = L_::bNever, bDrain = L_::bDrain, bBsync = L_::bBsync;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -431,8 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(bKVFull), 1);
     mbar_init(bar(bKVFree), 1);
-    mbar_init(bar(bFull), 2);
-    mbar_init(bar(bEmpty), 1);
+    for (int s = 0; s < kQS; ++s) {
+      mbar_init(bar(bFull + s), 2);
+      mbar_init(bar(bEmpty + s), 1);
+    }
     mbar_init(bar(bSFull), 1);
     mbar_init(bar(bPFull), kSoftmaxWarps);
     mbar_init(bar(bDKVFull), 1);
@@ -473,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       int c[3];
       const bool box = tile_box(g, x.omega, x.qt, c);
-      load_tile(sbase + kK, &tmk, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bKVFull));
-      load_tile(sbase + kV, &tmv, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bKVFull));
+      load_tile(sbase + kK, &tmk, g, box, c, q, x.b, x.h, lane, nq4, bar(bKVFull));
+      load_tile(sbase + kV, &tmv, g, box, c, q, x.b, x.h, lane, nq4, bar(bKVFull));
 #pragma unroll
       for (int j = 0; j < 4; ++j)
         *reinterpret_cast<uint4 *>(smem + kKm + sw32(4 * lane + j, 0)) = mask_chunk(live[j], q.reg[j], true);
@@ -486,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool qw = warp == kQWarp;
     int64_t t = 0;
     for (; t < ntiles; ++t) {
+      const int s = (int)(t % kQS);
       const LItem x = decode(g, L + t / nqt);
       const int qt = (int)(t % nqt);
       const Quad q = route_quad(g, x.omega, qt, lane);
@@ -501,14 +520,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           dl[j] = live[j] ? __ldcg(a.delta + base + q.src[j]) : 0.f;
         }
       }
-      if (t >= 1 && !mbar_wait_warp(bar(bEmpty), (uint32_t)(t - 1) & 1u, ctl)) break;
-      uint8_t *sp = smem + kStage;
+      if (t >= kQS && !mbar_wait_warp(bar(bEmpty + s), (uint32_t)((t / kQS) - 1) & 1u, ctl)) break;
+      uint8_t *sp = smem + kStage + s * kStageBytes;
       const int rows = min(128, g.n - qt * 128), nq4 = (rows + 3) >> 2;
-      if (lane == 0) mbar_expect_tx(bar(bFull), (uint32_t)nq4 * 1024u);
+      if (lane == 0) mbar_expect_tx(bar(bFull + s), (uint32_t)nq4 * 1024u);
       __syncwarp();
       int c[3];
       const bool box = tile_box(g, x.omega, qt, c);
-      load_tile(sbase + kStage + (qw ? kQ : kdO), qw ? &tmq : &tmdo, box, c, q, x.b, g.tokens, x.h, lane, nq4, bar(bFull));
+      load_tile(sbase + kStage + s * kStageBytes + (qw ? kQ : kdO), qw ? &tmq : &tmdo, g, box, c, q, x.b, x.h, lane,
+                nq4, bar(bFull + s));
       if (qw) {
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -518,21 +538,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<int4 *>(sp + kRbase + 16 * lane) = make_int4(q.rbase[0], q.rbase[1], q.rbase[2], q.rbase[3]);
         fence_proxy_async_smem();
       }
-      mbar_arrive_warp(bar(bFull));
+      mbar_arrive_warp(bar(bFull + s));
     }
+    // copies still in flight must land before the CTA exits
     volatile int no_abort = 0;
     const WaitCtl dctl{&no_abort, ctl.status, ctl.limit_ns < 50000000ull ? ctl.limit_ns : 50000000ull};
-    if (t > 0) mbar_wait_warp(bar(bFull), (uint32_t)(t - 1) & 1u, dctl);
+    for (int64_t k = t > kQS ? t - kQS : 0; k < t; ++k)
+      mbar_wait_warp(bar(bFull + (int)(k % kQS)), (uint32_t)(k / kQS) & 1u, dctl);
   } else if (warp == kMmaWarp) {
     // --------------------------------------------------------------- MMA ---
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16(128, 128, 0, 0), idesc_acc = idesc_bf16(128, 128, 0, 1);
-      const uint32_t st = sbase + kStage;
       bool ok = true;
       for (int64_t t = 0; ok && t < ntiles; ++t) {
-        const int qt = (int)(t % nqt);
+        const int qt = (int)(t % nqt), s = (int)(t % kQS);
         const int64_t it = t / nqt;
-        ok = mbar_wait(bar(bFull), (uint32_t)t & 1u, ctl) &&
+        const uint32_t st = sbase + kStage + s * kStageBytes;
+        ok = mbar_wait(bar(bFull + s), (uint32_t)(t / kQS) & 1u, ctl) &&
              (qt != 0 || mbar_wait(bar(bKVFull), (uint32_t)it & 1u, ctl)) &&
              (t == 0 || mbar_wait(bar(bPFull), (uint32_t)(t - 1) & 1u, ctl));
         if (!ok) break;
@@ -557,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + kColdK, tmem + kColdP + 16u * kk, nmajor_desc(st + kQ, 16 * kk), idesc_acc,
                  (qt > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(bar(bEmpty));
+        mma_commit(bar(bEmpty + s));
         if (qt == nqt - 1) mma_commit(bar(bDKVFull));
       }
       mma_commit(bar(bDrain));
@@ -619,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *bcol = reinterpret_cast<float *>(smem + kBcol);
     float *bacc = reinterpret_cast<float *>(smem + kBacc);
     const float cs = a.scale * kLog2e;
-    const bool has_bias = a.bias != nullptr, want_db = a.ws != nullptr;
+    // (the host picks two query stages only without bias and dBias)
+    const bool has_bias = kQS == 1 && a.bias != nullptr, want_db = kQS == 1 && a.ws != nullptr;
     int cur_h = -1, h_first = -1, roff = 0;
     uint32_t bs_phase = 0;
     bool ok = true;
@@ -665,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!mbar_wait_warp(bar(bSFull), (uint32_t)t & 1u, ctl)) break;
       tc_fence_after();
-      const uint8_t *sp = smem + kStage;
+      const uint8_t *sp = smem + kStage + (int)(t % kQS) * kStageBytes;
       const float *lse2 = reinterpret_cast<const float *>(sp + kLse) + 64 * grp;
       const float *dl = reinterpret_cast<const float *>(sp + kDelta) + 64 * grp;
       const int *rb = reinterpret_cast<const int *>(sp + kRbase) + 64 * grp;
@@ -759,10 +782,14 @@ int launch_bwd_large(const BwdArgs &a, void *stream) {
   if (!lg::tile_maps(&mq, a.q, a.g) || !lg::tile_maps(&mk, a.k, a.g) || !lg::tile_maps(&mv, a.v, a.g) ||
       !lg::tile_maps(&mdo, a.dout, a.g))
     return SWIN_ERR_CUDA;
+  // two query stages in the key-tile kernel when neither the bias column nor
+  // the dBias accumulator needs its shared memory
+  const bool two = a.bias == nullptr && a.ws == nullptr;
+  auto kv = two ? lg::bkv::bwdkv_kernel<2> : lg::bkv::bwdkv_kernel<1>;
+  const int kv_smem = two ? lg::bkv::Lay<2>::kSmemBytes : lg::bkv::Lay<1>::kSmemBytes;
   if (cudaFuncSetAttribute(lg::bq::bwdq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lg::bq::kSmemBytes) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(lg::bkv::bwdkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lg::bkv::kSmemBytes) !=
-          cudaSuccess)
+      cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, kv_smem) != cudaSuccess)
     return SWIN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a.o) {
@@ -770,7 +797,7 @@ int launch_bwd_large(const BwdArgs &a, void *stream) {
     lg::delta_kernel<<<(unsigned)((toks + 7) / 8), 256, 0, s>>>(a);
   }
   lg::bq::bwdq_kernel<<<a.ctas, lg::kThreads, lg::bq::kSmemBytes, s>>>(a, mq, mk, mv, mdo);
-  lg::bkv::bwdkv_kernel<<<a.ctas, lg::kThreads, lg::bkv::kSmemBytes, s>>>(a, mq, mk, mv, mdo);
+  kv<<<a.ctas, lg::kThreads, kv_smem, s>>>(a, mq, mk, mv, mdo);
   return cudaPeekAtLastError() == cudaSuccess ? SWIN_OK : SWIN_ERR_CUDA;
 }
 
