@@ -55,10 +55,10 @@ constexpr int kStageBytes = 68 * 1024;
 // the key tiles: slot t mod 4 is rewritten with key tile t + 4, which cannot
 // start before the softmax of tile t has finished (see the barriers below)
 constexpr int kRoffSlots = 4;
-// Key/value tiles load their 16-slot runs as boxes only in windows of at
-// least this many key tiles: measured faster there (64 800-slot windows,
-// 507 tiles: -16 % forward time) and slower in windows of 43-128 tiles
-// (+2-7 %), where row gathers alone are used.
+// Key/value tiles load their runs of consecutive slots as boxes only in
+// windows of at least this many key tiles: measured faster there (64 800-slot
+// windows, 507 tiles: -16 % forward time) and slower in windows of 43-128
+// tiles (+2-7 %), where row gathers alone are used.
 constexpr int kRunMinKeyTiles = 256;
 constexpr int kRoff = kStage0 + kStages * kStageBytes;
 constexpr int kBcol = kRoff + kRoffSlots * 256;  // bias column of the current head (bias*log2e)
@@ -101,7 +101,7 @@ __device__ __forceinline__ LItem decode_pair(const Geo &g, int64_t it) {
   return x;
 }
 
-// kRuns: key/value tiles load 16-slot runs as boxes (windows of at least
+// kRuns: key/value tiles load runs of slots as boxes (windows of at least
 // kRunMinKeyTiles key tiles); otherwise every row by gather4.
 template <bool kRuns>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -180,8 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows_b = has_b ? min(128, g.n - (x.qt + 1) * 128) : 0, nqb = (rows_b + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(bQFull), (uint32_t)(nqa + nqb) * 1024u);
       __syncwarp();
-      // row gathers (measured faster here than tile boxes or 16-slot runs, unlike in the backward)
-      const Run16 rows_only{false, {0, 0, 0}};
+      // row gathers (measured faster here than tile boxes or runs, unlike in the backward)
+      const Run rows_only{false, false, {0, 0, 0}};
       for (int hf = 0; hf < 2; ++hf)
         load_half(sbase + kQA + hf * kHalfBytes, &tmq, rows_only, qa, x.b, g.tokens, x.h, hf, lane, nqa, bar(bQFull));
       for (int hf = 0; has_b && hf < 2; ++hf)
@@ -214,10 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = min(128, g.n - kt * 128), nq4 = (rows + 3) >> 2;
       if (lane == 0) mbar_expect_tx(bar(full_b + s), (uint32_t)nq4 * 512u);
       __syncwarp();
-      // this warp's channel half of the tile rows (pads read token 0): 16-slot
-      // runs along the grid's last dimension as boxes, other rows by gather4
+      // this warp's channel half of the tile rows (pads read token 0): runs
+      // along the grid's last dimension as boxes, other rows by gather4
       if constexpr (kRuns) {
-        const Run16 run = run16(g, q, lane);
+        const Run run = find_run(g, q, lane);
         load_half(st + (kw ? kK : kV) + half * kHalfBytes, kw ? &tmk : &tmv, run, q, x.b, g.tokens, x.h, half, lane,
                   nq4, bar(full_b + s));
       } else if (lane < nq4) {

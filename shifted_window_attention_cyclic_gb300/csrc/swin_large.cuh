@@ -94,29 +94,37 @@ __device__ __forceinline__ void quad_live(const Quad &q, const uint8_t *land, in
 
 // The three TMA views of one [B, G0, G1, G2, C] bf16 tensor: 128-slot tile
 // boxes (64 channels x w2 x tb1 x tb0), the [B*T, C] row view for gather4 and
-// 16-slot runs along the grid's last dimension (64 channels x 16).
+// runs of run_len(g) slots along the grid's last dimension (64 channels x
+// run_len). (A fourth view per tensor measured slower throughout.)
 struct TileMaps {
   CUtensorMap box, rows, run;
 };
 
-// Whether the 16 slots of the lane's group of four quads (lanes 4c .. 4c+3,
-// tile rows 16c .. 16c+15) hold 16 consecutive positions along the grid's
-// last dimension within one grid row (no pad, no seam wrap, no slot past the
-// window), and the grid coordinates of the group's first slot. Such a run
-// loads as one 16-row box instead of four gather4 rows: a quarter of the TMA
-// instructions. Warp-collective: every lane of the warp calls it.
-struct Run16 {
-  bool run;
-  int c[3];  // grid coordinates (dims 0, 1, 2) of the group's first slot
+// Slots per run: 16 where window rows hold 16-slot runs well (w2 a multiple
+// of 16, or at least 64), else 8. Measured: 16-slot boxes beat row gathers
+// and 32-slot boxes; in windows 30 slots wide 8-slot boxes beat 16-slot ones.
+__host__ __device__ __forceinline__ int run_len(const Geo &g) { return g.w[2] % 16 == 0 || g.w[2] >= 64 ? 16 : 8; }
+
+// Whether the run_len slots of the lane's group of quads (run_len / 4 lanes,
+// tile rows from 4 x the group's first lane) hold consecutive positions along
+// the grid's last dimension within one grid row (no pad, no seam wrap, no
+// slot past the window), and the grid coordinates of the group's first slot.
+// Such a run loads as one box instead of one gather4 per four rows.
+// Warp-collective: every lane of the warp calls it.
+struct Run {
+  bool run, lead;  // lead: this lane is the group's first (it issues the run's box)
+  int c[3];        // grid coordinates (dims 0, 1, 2) of the group's first slot
 };
-__device__ __forceinline__ Run16 run16(const Geo &g, const Quad &q, int lane) {
-  const int s0 = __shfl_sync(0xffffffffu, q.src[0], lane & ~3);
-  const bool step = q.src[0] >= 0 && q.src[0] == s0 + 4 * (lane & 3) && q.src[1] == q.src[0] + 1 &&
+__device__ __forceinline__ Run find_run(const Geo &g, const Quad &q, int lane) {
+  const int len = run_len(g), gl = len >> 2, gm = gl - 1;  // lanes per run, and the lane mask within one
+  const int s0 = __shfl_sync(0xffffffffu, q.src[0], lane & ~gm);
+  const bool step = q.src[0] >= 0 && q.src[0] == s0 + 4 * (lane & gm) && q.src[1] == q.src[0] + 1 &&
                     q.src[2] == q.src[0] + 2 && q.src[3] == q.src[0] + 3;
-  const uint32_t bal = __ballot_sync(0xffffffffu, step);
-  Run16 r;
+  const uint32_t bal = __ballot_sync(0xffffffffu, step), all = (1u << gl) - 1u;
+  Run r;
   const int x2 = s0 >= 0 ? s0 % g.G[2] : 0, rest = s0 >= 0 ? s0 / g.G[2] : 0;
-  r.run = ((bal >> (lane & ~3)) & 0xFu) == 0xFu && x2 + 16 <= g.G[2];
+  r.run = ((bal >> (lane & ~gm)) & all) == all && x2 + len <= g.G[2];
+  r.lead = (lane & gm) == 0;
   r.c[2] = x2;
   r.c[1] = rest % g.G[1];
   r.c[0] = rest / g.G[1];
@@ -124,13 +132,13 @@ __device__ __forceinline__ Run16 run16(const Geo &g, const Quad &q, int lane) {
 }
 
 // One 64-channel half (channels h*128 + 64*half ..) of the lane's quad of
-// tile rows into the half-tile at dst_half: lane 4c copies its group's run as
-// one box, lanes of other groups gather their four rows (pads read token 0).
-__device__ __forceinline__ void load_half(uint32_t dst_half, const TileMaps *m, const Run16 &r, const Quad &q, int b,
+// tile rows into the half-tile at dst_half: the first lane of a run copies it
+// as one box, lanes outside runs gather their four rows (pads read token 0).
+__device__ __forceinline__ void load_half(uint32_t dst_half, const TileMaps *m, const Run &r, const Quad &q, int b,
                                           int tokens, int h, int half, int lane, int nq4, uint32_t bar) {
   const int ch = h * kHd + 64 * half;
   if (r.run) {
-    if ((lane & 3) == 0) tma_load_5d(dst_half + 512u * lane, &m->run, ch, r.c[2], r.c[1], r.c[0], b, bar);
+    if (r.lead) tma_load_5d(dst_half + 512u * lane, &m->run, ch, r.c[2], r.c[1], r.c[0], b, bar);
   } else if (lane < nq4) {
     const int r0 = b * tokens;
     tma_gather4(dst_half + 512u * lane, &m->rows, ch, r0 + max(q.src[0], 0), r0 + max(q.src[1], 0),
@@ -157,7 +165,7 @@ __device__ __forceinline__ bool tile_box(const Geo &g, int omega, int tile, int 
 }
 
 // One 128-slot tile of head h into `dst` (two 64-channel halves): two box
-// copies from lane 0 when the tile is a box, else 16-row runs and row
+// copies from lane 0 when the tile is a box, else runs and row
 // gathers (load_half). Completion is counted on `bar` (32 KB for a full tile
 // either way). Warp-collective: `box` is the same on every lane.
 __device__ __forceinline__ void load_tile(uint32_t dst, const TileMaps *m, const Geo &g, bool box, const int (&c)[3],
@@ -168,7 +176,7 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const TileMaps *m, const
       tma_load_5d(dst + kHalfBytes, &m->box, h * kHd + 64, c[2], c[1], c[0], b, bar);
     }
   } else {
-    const Run16 r = run16(g, q, lane);
+    const Run r = find_run(g, q, lane);
     load_half(dst, m, r, q, b, g.tokens, h, 0, lane, nq4, bar);
     load_half(dst + kHalfBytes, m, r, q, b, g.tokens, h, 1, lane, nq4, bar);
   }
@@ -234,11 +242,11 @@ inline bool box128_map(CUtensorMap *m, const void *base, const Geo &g) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Run view of the same tensor: (64 channels, 16, 1, 1, 1) per copy.
-inline bool run16_map(CUtensorMap *m, const void *base, const Geo &g) {
+// Run view of the same tensor: (64 channels, run_len, 1, 1, 1) per copy.
+inline bool run_map(CUtensorMap *m, const void *base, const Geo &g) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return false;
-  if (g.G[2] < 16) {  // no run fits in a grid row: a valid map of the row view stands in (never used)
+  if (g.G[2] < run_len(g)) {  // no run fits in a grid row: a valid map of the row view stands in (never used)
     return rows128_map(m, base, g);
   }
   const cuuint64_t e = 2;
@@ -246,7 +254,7 @@ inline bool run16_map(CUtensorMap *m, const void *base, const Geo &g) {
                         (cuuint64_t)g.batch};
   cuuint64_t strides[4] = {dims[0] * e, dims[0] * dims[1] * e, dims[0] * dims[1] * dims[2] * e,
                            dims[0] * dims[1] * dims[2] * dims[3] * e};
-  cuuint32_t box[5] = {64u, 16u, 1u, 1u, 1u};
+  cuuint32_t box[5] = {64u, (cuuint32_t)run_len(g), 1u, 1u, 1u};
   cuuint32_t es[5] = {1u, 1u, 1u, 1u, 1u};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -254,7 +262,7 @@ inline bool run16_map(CUtensorMap *m, const void *base, const Geo &g) {
 }
 
 inline bool tile_maps(TileMaps *t, const void *base, const Geo &g) {
-  return box128_map(&t->box, base, g) && run16_map(&t->run, base, g) && rows128_map(&t->rows, base, g);
+  return box128_map(&t->box, base, g) && run_map(&t->run, base, g) && rows128_map(&t->rows, base, g);
 }
 
 }  // namespace lg
