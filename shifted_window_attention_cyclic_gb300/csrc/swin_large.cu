@@ -118,9 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Geo &g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkt = g.nqt;  // key tiles per window
-  int64_t L, R;
-  eq4_range(a.items, a.ctas, blockIdx.x, L, R);
-  const int64_t count = R - L;
+  const Items its = strided_items(a.items, a.ctas);
+  const int64_t count = its.count;
   const int64_t ntiles = count * nkt;  // key tiles this CTA streams, over all its items
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns};
 
@@ -168,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kQWarp) {
     // ----------------------------------------------------------- Q tiles ---
     for (int64_t it = 0; it < count; ++it) {
-      const LItem x = decode_pair(g, L + it);
+      const LItem x = decode_pair(g, its[it]);
       const bool has_b = x.qt + 1 < g.nqt;
       const Quad qa = route_quad(g, x.omega, x.qt, lane);
       const Quad qb = route_quad(g, x.omega, has_b ? x.qt + 1 : x.qt, lane);
@@ -202,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t t = 0;
     for (; t < ntiles; ++t) {
       const int s = (int)(t % kStages);
-      const LItem x = decode_pair(g, L + t / nkt);
+      const LItem x = decode_pair(g, its[t / nkt]);
       const int kt = (int)(t % nkt);
       const Quad q = route_quad(g, x.omega, kt, lane);
       const bool meta = warp == kKWarp;  // writes the key mask rows and bias offsets
@@ -291,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int64_t t = 0; ok && t < ntiles; ++t) {
         const int kt = (int)(t % nkt);
-        const LItem x = decode_pair(g, L + t / nkt);
+        const LItem x = decode_pair(g, its[t / nkt]);
         const bool has_b = x.qt + 1 < g.nqt;
         if (kt == 0) {  // the item's first S's (its Q tiles came in after the previous item's last S's)
           ok = issue_s(0, t) && (!has_b || issue_s(1, t));
@@ -342,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (a.debug_force_timeout && xq == 0) ok = mbar_wait_warp(bar(bNever), 0, ctl);
     for (int64_t t = 0; ok && t < ntiles; ++t) {
       const int kt = (int)(t % nkt);
-      const LItem x = decode_pair(g, L + t / nkt);
+      const LItem x = decode_pair(g, its[t / nkt]);
       if (kt == 0) {
         if (has_bias && x.h != cur_h) {
           // the head's bias column (bias * log2e) and its largest value

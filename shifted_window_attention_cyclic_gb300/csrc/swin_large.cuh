@@ -44,6 +44,25 @@ __device__ __forceinline__ LItem decode(const Geo &g, int64_t it) {
   return x;
 }
 
+// The work items of this CTA: item k is first + k * step, k < count.
+// Strided (CTA r takes r, r + ctas, ...): the CTAs running at one time work on
+// neighbouring items, tiles of one window and head, whose key/value or query
+// tiles then stay in L2 for all of them. Contiguous (TERRA Eq. (4) ranges)
+// where the dBias workspace slots follow those ranges.
+struct Items {
+  int64_t first, step, count;
+  __device__ __forceinline__ int64_t operator[](int64_t k) const { return first + k * step; }
+};
+__device__ __forceinline__ Items strided_items(int64_t items, int ctas) {
+  const int64_t r = blockIdx.x;
+  return Items{r, ctas, r < items ? (items - 1 - r) / ctas + 1 : 0};
+}
+__device__ __forceinline__ Items range_items(int64_t items, int ctas) {
+  int64_t L, R;
+  eq4_range(items, ctas, blockIdx.x, L, R);
+  return Items{L, 1, R - L};
+}
+
 // Mask row chunk 0 (region codes < 8): query rows carry a one-hot of the
 // region code (live queries), key rows 0 in the column of their code if live
 // and -2^100 elsewhere; columns 8..15 are constant (0 / -2^100).

@@ -71,9 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // was computed from the forward's output before this kernel
   const bool delta_given = a.o != nullptr;
   const int nkt = g.nqt, per_item = delta_given ? nkt : 2 * nkt;
-  int64_t L, R;
-  eq4_range(a.items, a.ctas, blockIdx.x, L, R);
-  const int64_t count = R - L, ntiles = count * per_item;
+  const Items its = strided_items(a.items, a.ctas);
+  const int64_t count = its.count, ntiles = count * per_item;
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns};
 
   if (threadIdx.x == 0) {
@@ -114,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kQWarp) {
     // -------------------------------------------------- Q, dO and masks ---
     for (int64_t it = 0; it < count; ++it) {
-      const LItem x = decode(g, L + it);
+      const LItem x = decode(g, its[it]);
       const Quad q = route_quad(g, x.omega, x.qt, lane);
       bool live[4];
       quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
@@ -138,7 +137,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t t = 0;
     for (; t < ntiles; ++t) {
       const int s = (int)(t % kStages);
-      const LItem x = decode(g, L + t / per_item);
+      const LItem x = decode(g, its[t / per_item]);
       const int kt = (int)((t % per_item) % nkt);
       const Quad q = route_quad(g, x.omega, kt, lane);
       bool live[4];
@@ -214,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3, i = q4 * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     for (int64_t it = 0; it < count; ++it) {
-      const LItem x = decode(g, L + it);
+      const LItem x = decode(g, its[it]);
       const int slot = x.qt * 128 + i;
       int wc[3];
       window_coords(g, x.omega, wc);
@@ -267,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = (int)(t % kStages), u = (int)(t % per_item), kt = u % nkt;
       const int64_t it = t / per_item;
       const bool second = delta_given || u >= nkt;
-      const LItem x = decode(g, L + it);
+      const LItem x = decode(g, its[it]);
       if (u == 0) {
         if (has_bias && x.h != cur_h) {
           if (cur_h >= 0) {
@@ -439,9 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Geo &g = a.g;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqt = g.nqt;
-  int64_t L, R;
-  eq4_range(a.items, a.ctas, blockIdx.x, L, R);
-  const int64_t count = R - L, ntiles = count * nqt;  // query tiles streamed over all items
+  // (the dBias workspace slots of a launch with dBias follow the contiguous ranges)
+  const Items its = kQS == 2 ? strided_items(a.items, a.ctas) : range_items(a.items, a.ctas);
+  const int64_t count = its.count, ntiles = count * nqt;  // query tiles streamed over all items
   WaitCtl ctl{abort_flag, a.status, a.wait_limit_ns};
 
   if (threadIdx.x == 0) {
@@ -481,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kKVWarp) {
     // --------------------------------------------- K, V and key mask rows ---
     for (int64_t it = 0; it < count; ++it) {
-      const LItem x = decode(g, L + it);  // x.qt is the key tile here
+      const LItem x = decode(g, its[it]);  // x.qt is the key tile here
       const Quad q = route_quad(g, x.omega, x.qt, lane);
       bool live[4];
       quad_live(q, a.land, (int64_t)x.b * g.tokens, live);
@@ -505,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t t = 0;
     for (; t < ntiles; ++t) {
       const int s = (int)(t % kQS);
-      const LItem x = decode(g, L + t / nqt);
+      const LItem x = decode(g, its[t / nqt]);
       const int qt = (int)(t % nqt);
       const Quad q = route_quad(g, x.omega, qt, lane);
       bool live[4];
@@ -593,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q4 = warp & 3, j = q4 * 32 + lane;
     const uint32_t lane_addr = (uint32_t)(q4 * 32) << 16;
     for (int64_t it = 0; it < count; ++it) {
-      const LItem x = decode(g, L + it);
+      const LItem x = decode(g, its[it]);
       const int slot = x.qt * 128 + j;
       int wc[3];
       window_coords(g, x.omega, wc);
@@ -666,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qt = (int)(t % nqt);
       const int64_t it = t / nqt;
       if (qt == 0) {
-        const LItem x = decode(g, L + it);
+        const LItem x = decode(g, its[it]);
         if (x.h != cur_h) {
           if (cur_h >= 0) {
             if (!bsync()) break;  // every accumulation and bias read of the previous head is done
