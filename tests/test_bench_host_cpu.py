@@ -60,3 +60,25 @@ def test_parity_sample_reads_the_bar():
     outs["dk"][(0,) + tuple(sea)][3] += 0.05
     res = bench.parity_sample(wl, x, outs, windows=10 ** 6)  # every window
     assert not res["within_bar"] and res["dk"]["max_abs"] > 2e-2
+
+
+def test_counts_of_a_workload_without_bias():
+    # beast_w64k: BEAST's [360, 180] windows, no relative-position bias. Its
+    # algorithmic bytes carry no bias table, its FLOPs count every pair of
+    # real slots of the 8 full windows, and the bench times it with fewer
+    # repetitions
+    from shifted_window_attention_cyclic_gb300 import workloads
+    wl = workloads.WORKLOADS["beast_w64k"]
+    assert not wl.bias and wl.head_dim == 128 and int(np.prod(wl.window)) == 64800
+    assert "beast_w64k" in bench.EXTRA and bench.EXTRA_REPS["beast_w64k"][0] <= 10
+    n = int(np.prod(wl.window))
+    win_src = np.arange(8 * n, dtype=np.int32).reshape(8, n)  # 8 full windows (720 x 720 grid)
+    f, b, fb, bb, bm = bench.workload_counts(wl, win_src, None)
+    assert f == 4.0 * 8 * n * n * wl.channels and b == 2.5 * f
+    N, e = wl.tokens, 2
+    assert fb == 4 * N * wl.channels * e + 4 * N * wl.heads  # Q, K, V, O + LSE: no bias, no land
+    with_bias = workloads.Workload(**{**wl.__dict__, "bias": True})
+    rows = int(np.prod([2 * w - 1 for w in wl.window]))
+    assert bench.workload_counts(with_bias, win_src, None)[2] == fb + rows * wl.heads * 4
+    # its windows are beyond the per-window oracle legs of the bench
+    assert n > bench.ORACLE_WINDOW_SLOTS
