@@ -56,10 +56,11 @@ constexpr int kStageBytes = 68 * 1024;
 // start before the softmax of tile t has finished (see the barriers below)
 constexpr int kRoffSlots = 4;
 // Key/value tiles load their runs of consecutive slots as boxes only in
-// windows of at least this many key tiles: measured faster there (64 800-slot
-// windows, 507 tiles: -16 % forward time) and slower in windows of 43-128
-// tiles (+2-7 %), where row gathers alone are used.
-constexpr int kRunMinKeyTiles = 256;
+// windows of at least this many key tiles. Measured with the strided item
+// schedule: faster at 32-507 tiles (-8 % forward time at 32, -5 % at 128).
+// Windows of 8 tiles (1 024 slots) gather every row; runs measured no faster
+// there with contiguous item ranges.
+constexpr int kRunMinKeyTiles = 32;
 constexpr int kRoff = kStage0 + kStages * kStageBytes;
 constexpr int kBcol = kRoff + kRoffSlots * 256;  // bias column of the current head (bias*log2e)
 constexpr int kMaxBiasRows = 4096;
