@@ -11,13 +11,17 @@
 // window and in-window coordinates, Q, K and V rows are gathered straight from
 // the [B, grid, C] tensors by TMA, and O rows are stored at their tokens.
 //
-// Work item = (head, image, window, pair of query tiles of 128 slots); each
-// CTA takes a contiguous range of items (TERRA Eq. (4)). Both query tiles stay
+// Work item = (head, image, window, pair of query tiles of 128 slots); the
+// items are strided over the CTAs (CTA r takes r, r + ctas, ...), so the CTAs
+// running together stream the same window's key/value tiles from L2. Both
+// query tiles stay
 // in shared memory and every key tile of the window, streamed through two
 // stages, serves both (half the key/value loads per FLOP of one tile per item):
 //  * warp 12 loads the two Q tiles (TMA gather4, two 64-channel halves each)
 //    and writes their query mask rows; warps 13 and 8 load K (one channel
-//    half each; 13 also writes the key mask rows and, into a four-slot int16
+//    half each, by gather4 rows, or in windows of at least kRunMinKeyTiles
+//    key tiles by boxes of runs of consecutive slots where a run lies in one
+//    grid row; 13 also writes the key mask rows and, into a four-slot int16
 //    ring, the key side of the bias offsets with the 16-key chunks whose
 //    offsets step by one marked), warps 14 and 9 load V. A stage's key half
 //    is released after the tile's last S, its value half after its last PV;

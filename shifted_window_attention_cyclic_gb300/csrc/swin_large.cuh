@@ -1,6 +1,7 @@
 // swin_large.cuh -- shared pieces of the head_dim-128 kernels (windows of any
-// size, key-tiled): tile layouts, work-item decoding, slot routing of a
-// 128-slot tile, TMA row gathers and the mask rows.
+// size, key-tiled): tile layouts, the CTAs' item schedules, work-item
+// decoding, slot routing of a 128-slot tile, its TMA loads (whole-tile boxes,
+// boxes of runs of consecutive slots, gather4 rows) and the mask rows.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>

@@ -22,7 +22,12 @@
 // and dP, so this backward reads neither O nor an fp32 copy of it; the form
 // from O (TERRA's FlashAttention-style backward) saves sweep 1 and carries
 // O's bf16 rounding. Routing, masks and the bias column are those of the
-// forward; whole-row tiles load as 5-D boxes, others as row gathers.
+// forward. Whole-row tiles load as 5-D boxes, others as boxes of runs of
+// consecutive slots and gather4 rows. Items are strided over the CTAs
+// (neighbouring tiles of one window stay in L2), except in the key-tile
+// kernel with dBias, whose workspace slots follow contiguous item ranges;
+// that kernel takes two query-tile stages when there is neither bias nor
+// dBias, one otherwise.
 #include <cuda_bf16.h>
 
 #include "swin_large.cuh"
