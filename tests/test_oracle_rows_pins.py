@@ -124,3 +124,33 @@ def test_rows_reject_bad_tokens(oracle_mod):
             oracle.query_rows(pb, q, k, v, bias, land, bad)
         with pytest.raises(ValueError):
             oracle.key_rows(pb, q, k, v, bias, land, dout, bad)
+
+
+def _random_cases():
+    from tests.test_oracle_pins import _random_problems
+    return _random_problems(24, 4711)
+
+
+@pytest.mark.parametrize("pb", _random_cases(), ids=lambda pb: "g%s_w%s_s%s_p%s" % (
+    "x".join(map(str, pb.grid)), "x".join(map(str, pb.window)), "".join(map(str, pb.shift)),
+    "".join(map(str, pb.periodic))))
+def test_rows_match_the_token_pair_form_on_random_geometries(oracle_mod, pb):
+    # every token of seeded tiny geometries over the whole descriptor space
+    # (2-D and 3-D, windows that do not divide or exceed the grid, every shift
+    # and periodic combination, land, batch 2): O and LSE against the
+    # token-pair brute force, dQ, dK and dV against torch autograd through the
+    # same token-pair form; neither forms a window table
+    from tests.test_oracle_pins import _bruteforce_grads
+    q, k, v, bias, dout, land = _inputs(pb, 61)
+    tok = np.arange(pb.batch * pb.tokens)
+    o, lse, dq = oracle.query_rows(pb, q, k, v, bias, land, tok, dout)
+    dk, dv = oracle.key_rows(pb, q, k, v, bias, land, dout, tok)
+    o_bf, lse_bf = bruteforce.fwd(pb, q, k, v, bias, land)
+    g = _bruteforce_grads(pb, q, k, v, bias, land, dout)
+    flat = lambda a: np.asarray(a).reshape(pb.batch * pb.tokens, -1)
+    np.testing.assert_allclose(o, flat(o_bf), rtol=0, atol=1e-12)
+    lb = np.transpose(np.asarray(lse_bf).reshape(pb.batch, pb.heads, pb.tokens), (0, 2, 1)).reshape(-1, pb.heads)
+    assert np.array_equal(np.isfinite(lse), np.isfinite(lb))
+    np.testing.assert_allclose(lse[np.isfinite(lse)], lb[np.isfinite(lb)], rtol=0, atol=1e-12)
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        np.testing.assert_allclose(got, flat(g[name]), rtol=0, atol=1e-11, err_msg=name)
